@@ -1,0 +1,243 @@
+/*
+ * pa_oracle.c — plain fp64 CPU oracle for paged attention in a
+ * speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness reference that the
+ * CUDA path is checked against.  Only the test suite, the package smoke test
+ * and the benchmark's CPU-baseline leg may load it.  The product library never
+ * links, loads or calls it, and it shares no code, header, table or helper
+ * with the CUDA path: the storage layouts below are restated here from their
+ * definitions, not included.
+ *
+ * What it computes (the plain definition; the method reaches exactly this
+ * result up to rounding order):
+ *
+ *   For every sequence b, every new token i < T_b and every query head h
+ *     p   = past_len_b + i                       absolute position of token i
+ *     g   = h / (Hq / Hkv)                       KV head shared by the GQA group
+ *     lo  = W > 0 ? max(0, p - W + 1) : 0         first visible key
+ *     for j in [lo, p]:  K_j, V_j = stored key / value of position j, read
+ *                         through the block table page bt[b][j / ps], slot j % ps
+ *     s_j = scale * sum_d q[t, h, d] * K_j[d]
+ *     out[t, h, :] = sum_j exp(s_j - max s) V_j / sum_j exp(s_j - max s)
+ *   with t = subsequence_begins[b] + i.
+ *
+ * Sources (web pages on paged attention for speculative verification):
+ *  - OpenVINO issue 38153, "Performance issue description" and "Cause":
+ *    a verify step sends k+1 query tokens of one sequence against a long
+ *    past_len; the suggested single-token handling gives query token i the key
+ *    limit past_len + i + 1 (i.e. keys 0 .. past_len + i), and GQA heads share
+ *    one KV head ("GQA read-once").
+ *  - OpenVINO issue 38153, "Step-by-step reproduction", step 3: the operation's
+ *    inputs are past_lens, subsequence_begins, max_context_len and a block
+ *    table; u8 KV cache precision (step 1).
+ *  - SGLang discussion 36314, "Observation 3", and the dual-radeon-vllm
+ *    article's per-call section: sliding-window layers attend only the last
+ *    window of keys (window 1024 on those pages).
+ *
+ * Readings where the pages are silent (each restated in the design notes):
+ *  - GQA groups are contiguous: query head h uses KV head h / G, G = Hq / Hkv.
+ *  - A window W admits exactly W keys ending at the token itself (j > p - W).
+ *    W = 0 means no window.
+ *  - The new tokens' own K/V already sit in the cache at positions
+ *    past_len .. past_len + T - 1.
+ *  - u8 dequantisation is (u8 - zp) * scale with fp16 scale and zero-point,
+ *    one pair per token per KV head, separately for K and for V.
+ *  - scale multiplies q.k before the softmax; no soft-cap, no bias.
+ *
+ * Storage layouts read here (restated, not shared):
+ *  - q   [total_tokens, Hq, D] in q_dtype (0 f32, 1 f16, 2 bf16).
+ *  - float KV cache  [num_blocks, Hkv, ps, D] in kv_dtype (0, 1 or 2).
+ *  - u8 KV cache (kv_dtype 3): per (block, KV head) one record of
+ *    ps*D bytes of codes (slot-major), then ps fp16 scales, then ps fp16
+ *    zero-points; records are ps*(D+4) bytes, [num_blocks, Hkv, record].
+ *  - block_tables [num_seqs, max_blocks_per_seq] int32 physical block ids.
+ *
+ * Every stored value is converted exactly to double; all arithmetic is fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_U8 = 3 };
+
+/* IEEE binary16 -> double, exact (normals, subnormals, inf, nan). */
+static double half_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int expo = (h >> 10) & 0x1f;
+  int mant = h & 0x3ff;
+  double v;
+  if (expo == 0) {
+    v = ldexp((double)mant, -24); /* subnormal: mant * 2^-14 * 2^-10 */
+  } else if (expo == 31) {
+    v = mant ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(mant | 0x400), expo - 25); /* (1.mant) * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* bfloat16 -> double, exact: the top 16 bits of an IEEE binary32. */
+static double bf16_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static double load_float(const void* base, int dtype, size_t idx) {
+  if (dtype == OR_F32) {
+    float f;
+    memcpy(&f, (const char*)base + idx * 4, 4);
+    return (double)f;
+  }
+  uint16_t h;
+  memcpy(&h, (const char*)base + idx * 2, 2);
+  return dtype == OR_F16 ? half_to_double(h) : bf16_to_double(h);
+}
+
+/* The dequantised value of element d of slot `slot` of KV head g in physical
+ * block `blk` (OpenVINO issue 38153, reproduction step 1: u8 KV cache). */
+static double cache_value(const void* cache, int kv_dtype, int Hkv, int ps, int D,
+                          int blk, int g, int slot, int d) {
+  if (kv_dtype != OR_U8) {
+    size_t idx = (((size_t)blk * Hkv + g) * ps + slot) * (size_t)D + d;
+    return load_float(cache, kv_dtype, idx);
+  }
+  size_t rec_bytes = (size_t)ps * (D + 4);
+  const unsigned char* rec = (const unsigned char*)cache + ((size_t)blk * Hkv + g) * rec_bytes;
+  double code = (double)rec[(size_t)slot * D + d];
+  uint16_t s16, z16;
+  memcpy(&s16, rec + (size_t)ps * D + 2 * (size_t)slot, 2);
+  memcpy(&z16, rec + (size_t)ps * D + 2 * (size_t)ps + 2 * (size_t)slot, 2);
+  return (code - half_to_double(z16)) * half_to_double(s16);
+}
+
+/*
+ * pa_oracle_forward: the definition above, one output row at a time.
+ * Returns 0, or -1 on inconsistent inputs (a block id outside
+ * [0, num_blocks), a key position beyond the block table, bad begins).
+ * out is [total_tokens, Hq, D] doubles.  nthreads <= 0 uses the OpenMP default.
+ */
+int pa_oracle_forward(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                      int kv_dtype, const int32_t* block_tables, const int32_t* past_lens,
+                      const int32_t* subsequence_begins, int num_seqs, int num_q_heads,
+                      int num_kv_heads, int head_dim, int page_size, int num_blocks,
+                      int max_blocks_per_seq, double scale, int sliding_window, double* out,
+                      int nthreads) {
+  const int Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, ps = page_size;
+  if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || ps <= 0 || num_seqs < 0) return -1;
+  const int G = Hq / Hkv;
+  const int total_tokens = subsequence_begins[num_seqs];
+
+  /* Flatten (token, head) so each output row is one independent work item. */
+  int* row_seq = (int*)malloc(sizeof(int) * (size_t)(total_tokens > 0 ? total_tokens : 1));
+  if (!row_seq) return -1;
+  for (int b = 0; b < num_seqs; ++b) {
+    if (subsequence_begins[b] > subsequence_begins[b + 1] || past_lens[b] < 0) {
+      free(row_seq);
+      return -1;
+    }
+    for (int t = subsequence_begins[b]; t < subsequence_begins[b + 1]; ++t) row_seq[t] = b;
+  }
+
+  int bad = 0;
+  const long n_items = (long)total_tokens * Hq;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+  for (long item = 0; item < n_items; ++item) {
+    const int t = (int)(item / Hq), h = (int)(item % Hq);
+    const int b = row_seq[t];
+    const int i = t - subsequence_begins[b];
+    const int g = h / G;
+    const long p = (long)past_lens[b] + i;
+    const long lo = sliding_window > 0 ? (p - sliding_window + 1 > 0 ? p - sliding_window + 1 : 0) : 0;
+    const long n = p - lo + 1;
+    double* o = out + ((size_t)t * Hq + h) * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (p / ps >= max_blocks_per_seq) {
+      bad = 1;
+      continue;
+    }
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    if (!s) {
+      bad = 1;
+      continue;
+    }
+    /* scores s_j = scale * q . K_j */
+    const size_t qoff = ((size_t)t * Hq + h) * D;
+    double smax = -INFINITY;
+    int row_bad = 0;
+    for (long j = lo; j <= p; ++j) {
+      const int blk = block_tables[(size_t)b * max_blocks_per_seq + j / ps];
+      if (blk < 0 || blk >= num_blocks) {
+        row_bad = 1;
+        break;
+      }
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d)
+        acc += load_float(q, q_dtype, qoff + d) *
+               cache_value(k_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d);
+      s[j - lo] = scale * acc;
+      if (s[j - lo] > smax) smax = s[j - lo];
+    }
+    if (row_bad) {
+      free(s);
+      bad = 1;
+      continue;
+    }
+    /* softmax weights and the weighted sum of V */
+    double denom = 0.0;
+    for (long j = lo; j <= p; ++j) {
+      const double w = exp(s[j - lo] - smax);
+      denom += w;
+      const int blk = block_tables[(size_t)b * max_blocks_per_seq + j / ps];
+      for (int d = 0; d < D; ++d)
+        o[d] += w * cache_value(v_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d);
+    }
+    for (int d = 0; d < D; ++d) o[d] /= denom;
+    free(s);
+  }
+  free(row_seq);
+  return bad ? -1 : 0;
+}
+
+/*
+ * pa_oracle_pages_touched: which logical pages of each sequence the definition
+ * reads, and through which physical block.  For sequence b with T_b >= 1 the
+ * rows' key ranges [lo_i, past_len + i] have the union
+ * [lo_0, past_len + T_b - 1]; every logical page overlapping it is read.
+ * expected[b * max_blocks_per_seq + lp] = block_tables[b][lp] + 1 for a read
+ * page, 0 otherwise (0 marks "not read", so block id 0 stays distinguishable).
+ * Returns 0, or -1 if a range runs past the block table.
+ */
+int pa_oracle_pages_touched(const int32_t* block_tables, const int32_t* past_lens,
+                            const int32_t* subsequence_begins, int num_seqs, int page_size,
+                            int max_blocks_per_seq, int sliding_window, int32_t* expected) {
+  memset(expected, 0, sizeof(int32_t) * (size_t)num_seqs * max_blocks_per_seq);
+  for (int b = 0; b < num_seqs; ++b) {
+    const int T = subsequence_begins[b + 1] - subsequence_begins[b];
+    if (T <= 0) continue;
+    const long L = past_lens[b];
+    const long hi = L + T - 1;
+    const long lo = sliding_window > 0 ? (L - sliding_window + 1 > 0 ? L - sliding_window + 1 : 0) : 0;
+    if (hi / page_size >= max_blocks_per_seq) return -1;
+    for (long lp = lo / page_size; lp <= hi / page_size; ++lp)
+      expected[(size_t)b * max_blocks_per_seq + lp] = block_tables[(size_t)b * max_blocks_per_seq + lp] + 1;
+  }
+  return 0;
+}
+
+int pa_oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,392 @@
+"""Pins for the fp64 oracle (CPU only).
+
+The oracle is checked against things other than itself: hand-derived golden
+values, an independent dense brute force (materialised mask + full softmax),
+a library attention routine on the T=1 case, closed forms (W=1, q=0, equal
+keys, a window covering everything), the invariant that a T-token verify
+equals T single-token decodes with key limits past_len+i+1 (OpenVINO issue
+38153, Suggestion paragraph), block-table permutation, causal and window
+perturbation, the convex-hull bound, and u8 == float on the dequantised cache.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from paged_attention_speculative_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+# ---------------------------------------------------------------------------
+# Independent dense brute force (numpy).  Written from the definition with
+# whole-sequence gathers and a materialised [T, n] mask; no loops over keys.
+# ---------------------------------------------------------------------------
+
+def _decode_cache(case):
+    """-> float64 [nb, Hkv, ps, D] values of the stored cache."""
+    ps, D = case.page_size, case.head_dim
+    if case.kv_dtype != "u8":
+        return (W.storage_to_f64(case.k_cache, case.kv_dtype).reshape(case.num_blocks, case.num_kv_heads, ps, D),
+                W.storage_to_f64(case.v_cache, case.kv_dtype).reshape(case.num_blocks, case.num_kv_heads, ps, D))
+    out = []
+    for rec in (case.k_cache, case.v_cache):
+        rec = rec.reshape(case.num_blocks, case.num_kv_heads, ps * (D + 4))
+        codes = rec[:, :, : ps * D].reshape(case.num_blocks, case.num_kv_heads, ps, D).astype(np.float64)
+        sc = np.ascontiguousarray(rec[:, :, ps * D: ps * D + 2 * ps]).view(np.float16).astype(np.float64)
+        zp = np.ascontiguousarray(rec[:, :, ps * D + 2 * ps:]).view(np.float16).astype(np.float64)
+        out.append((codes - zp[..., None]) * sc[..., None])
+    return tuple(out)
+
+
+def brute_force(case):
+    kc, vc = _decode_cache(case)
+    q = W.storage_to_f64(case.q, case.q_dtype).reshape(case.total_tokens, case.num_q_heads, case.head_dim)
+    G = case.num_q_heads // case.num_kv_heads
+    out = np.zeros_like(q)
+    for b in range(case.num_seqs):
+        T = int(case.query_lens[b])
+        if T == 0:
+            continue
+        L = int(case.past_lens[b])
+        n = L + T
+        pos = np.arange(n)
+        blocks = case.block_tables[b][pos // case.page_size]
+        Kseq = kc[blocks, :, pos % case.page_size, :]          # [n, Hkv, D]
+        Vseq = vc[blocks, :, pos % case.page_size, :]
+        Kh = np.repeat(Kseq, G, axis=1).transpose(1, 0, 2)     # [Hq, n, D]
+        Vh = np.repeat(Vseq, G, axis=1).transpose(1, 0, 2)
+        t0 = int(case.subsequence_begins[b])
+        Qb = q[t0: t0 + T].transpose(1, 0, 2)                   # [Hq, T, D]
+        S = case.scale * np.einsum("htd,hnd->htn", Qb, Kh)
+        i = np.arange(T)[:, None]
+        j = pos[None, :]
+        allowed = j <= L + i
+        if case.sliding_window > 0:
+            allowed &= j >= L + i - case.sliding_window + 1
+        S = np.where(allowed[None], S, -np.inf)
+        S = S - S.max(axis=-1, keepdims=True)
+        P = np.exp(S)
+        P = P / P.sum(axis=-1, keepdims=True)
+        # keys no row may see carry weight exactly 0: drop them (their stored
+        # values may be NaN-poisoned and 0 * NaN would leak into the sum)
+        seen = allowed.any(axis=0)
+        out[t0: t0 + T] = np.einsum("htn,hnd->htd", P[:, :, seen], Vh[:, seen]).transpose(1, 0, 2)
+    return out
+
+
+def run_oracle(oracle_mod, case, **over):
+    kw = dict(num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
+              page_size=case.page_size, num_blocks=case.num_blocks, scale=case.scale,
+              sliding_window=case.sliding_window)
+    kw.update(over)
+    return oracle_mod.forward(case.q, case.q_dtype, case.k_cache, case.v_cache, case.kv_dtype,
+                              case.block_tables, case.past_lens, case.subsequence_begins, **kw)
+
+
+def small_cases():
+    return [
+        W.make_case("tiny_f32", seed=1, query_lens=[3], past_lens=[40], num_q_heads=8, num_kv_heads=2,
+                    head_dim=16, page_size=16, q_dtype="f32", kv_dtype="f32"),
+        W.make_case("bf16_gqa", seed=2, query_lens=[4], past_lens=[70], num_q_heads=8, num_kv_heads=2,
+                    head_dim=32, page_size=16),
+        W.make_case("f16_win", seed=3, query_lens=[3], past_lens=[90], num_q_heads=4, num_kv_heads=2,
+                    head_dim=16, page_size=8, q_dtype="f16", kv_dtype="f16", sliding_window=20),
+        W.make_case("u8", seed=4, query_lens=[3], past_lens=[50], num_q_heads=4, num_kv_heads=1,
+                    head_dim=32, page_size=16, kv_dtype="u8"),
+        W.make_case("batch_mixed_T", seed=5, query_lens=[1, 0, 4, 2], past_lens=[9, 30, 33, 0],
+                    num_q_heads=6, num_kv_heads=3, head_dim=16, page_size=4, sliding_window=7),
+        W.make_case("u8_win_batch", seed=6, query_lens=[2, 3], past_lens=[64, 17], num_q_heads=4,
+                    num_kv_heads=2, head_dim=16, page_size=8, kv_dtype="u8", q_dtype="f16", sliding_window=10),
+    ]
+
+
+@pytest.mark.parametrize("idx", range(6))
+def test_oracle_matches_dense_brute_force(oracle_mod, idx):
+    case = small_cases()[idx]
+    got = run_oracle(oracle_mod, case)
+    want = brute_force(case)
+    assert np.isfinite(got).all(), "oracle read a poisoned slot"
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Hand-derived golden values.
+# ---------------------------------------------------------------------------
+
+def _golden_case(c, kv_dtype="f32", codes=None):
+    Hq, Hkv, D, ps = c["num_q_heads"], c["num_kv_heads"], c["head_dim"], c["page_size"]
+    nb = c["num_blocks"]
+    bt = np.array(c["block_tables"], dtype=np.int32)
+    if "k_positions_per_head" in c:
+        kpos = np.array(c["k_positions_per_head"], dtype=np.float32)   # [Hkv, n, D]
+        vpos = np.array(c["v_positions_per_head"], dtype=np.float32)
+    else:
+        kpos = np.repeat(np.array(c["k_positions"], dtype=np.float32)[None], Hkv, axis=0)
+        vpos = np.repeat(np.array(c["v_positions"], dtype=np.float32)[None], Hkv, axis=0)
+    n = kpos.shape[1]
+    kc = np.zeros((nb, Hkv, ps, D), dtype=np.float32)
+    vc = np.zeros((nb, Hkv, ps, D), dtype=np.float32)
+    for j in range(n):
+        blk = bt[0][j // ps]
+        kc[blk, :, j % ps] = kpos[:, j]
+        vc[blk, :, j % ps] = vpos[:, j]
+    q = np.array(c["q"], dtype=np.float32)
+    return q, kc, vc, bt
+
+
+def test_golden_hand_worked(oracle_mod):
+    g = json.load(open(GOLDEN))
+    for c in g["cases"]:
+        q, kc, vc, bt = _golden_case(c)
+        got = oracle_mod.forward(q, "f32", kc, vc, "f32", bt, c["past_lens"], c["subsequence_begins"],
+                                 num_q_heads=c["num_q_heads"], num_kv_heads=c["num_kv_heads"],
+                                 head_dim=c["head_dim"], page_size=c["page_size"],
+                                 num_blocks=c["num_blocks"], scale=math.log(2.0),
+                                 sliding_window=c["sliding_window"])
+        np.testing.assert_allclose(got, np.array(c["expected"]), rtol=0, atol=1e-12, err_msg=c["name"])
+
+
+def test_golden_u8_records(oracle_mod):
+    g = json.load(open(GOLDEN))
+    c = g["cases"][0]
+    u = g["u8_case"]
+    ps, D, nb = c["page_size"], c["head_dim"], c["num_blocks"]
+    bt = np.array(c["block_tables"], dtype=np.int32)
+    codes_k = np.zeros((nb, 1, ps, D), np.uint8)
+    codes_v = np.zeros((nb, 1, ps, D), np.uint8)
+    for j, (ck, cv) in enumerate(zip(u["k_codes_positions"], u["v_codes_positions"])):
+        blk = bt[0][j // ps]
+        codes_k[blk, 0, j % ps] = ck
+        codes_v[blk, 0, j % ps] = cv
+    sc = np.full((nb, 1, ps), u["scale_fp16"], np.float16)
+    zp = np.full((nb, 1, ps), u["zp_fp16"], np.float16)
+    kr = W.pack_u8_records(codes_k, sc, zp)
+    vr = W.pack_u8_records(codes_v, sc, zp)
+    q = np.array(c["q"], dtype=np.float32)
+    got = oracle_mod.forward(q, "f32", kr, vr, "u8", bt, c["past_lens"], c["subsequence_begins"],
+                             num_q_heads=1, num_kv_heads=1, head_dim=D, page_size=ps, num_blocks=nb,
+                             scale=math.log(2.0), sliding_window=0)
+    np.testing.assert_allclose(got, np.array(u["expected"]), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Library routine on the T = 1 case (plain attention over all L+1 keys).
+# ---------------------------------------------------------------------------
+
+def test_t1_matches_torch_sdpa(oracle_mod):
+    torch = pytest.importorskip("torch")
+    case = W.make_case("t1", seed=11, query_lens=[1], past_lens=[77], num_q_heads=8, num_kv_heads=2,
+                       head_dim=32, page_size=16)
+    got = run_oracle(oracle_mod, case)
+    kc, vc = _decode_cache(case)
+    n = 78
+    pos = np.arange(n)
+    blocks = case.block_tables[0][pos // 16]
+    K = torch.from_numpy(kc[blocks, :, pos % 16, :].transpose(1, 0, 2).copy())   # [Hkv, n, D]
+    V = torch.from_numpy(vc[blocks, :, pos % 16, :].transpose(1, 0, 2).copy())
+    K = K.repeat_interleave(4, dim=0)
+    V = V.repeat_interleave(4, dim=0)
+    q = torch.from_numpy(W.storage_to_f64(case.q, "bf16").reshape(1, 8, 32).transpose(1, 0, 2).copy())
+    ref = torch.nn.functional.scaled_dot_product_attention(q[None], K[None], V[None], scale=case.scale)[0]
+    np.testing.assert_allclose(got[0], ref.numpy().transpose(1, 0, 2)[0], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# The equivalence the pages state: T-token verify == T single-token decodes.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("window", [0, 13])
+def test_t_tokens_equal_t_single_token_decodes(oracle_mod, window):
+    case = W.make_case("eq", seed=21, query_lens=[5], past_lens=[41], num_q_heads=6, num_kv_heads=2,
+                       head_dim=16, page_size=8, sliding_window=window)
+    multi = run_oracle(oracle_mod, case)
+    for i in range(5):
+        # token i alone, as a single-token decode with past_len L+i
+        single = oracle_mod.forward(case.q[i: i + 1], case.q_dtype, case.k_cache, case.v_cache, case.kv_dtype,
+                                    case.block_tables, [41 + i], [0, 1], num_q_heads=6, num_kv_heads=2,
+                                    head_dim=16, page_size=8, num_blocks=case.num_blocks, scale=case.scale,
+                                    sliding_window=window)
+        assert np.array_equal(multi[i], single[0])
+
+
+# ---------------------------------------------------------------------------
+# Closed forms.
+# ---------------------------------------------------------------------------
+
+def test_window_one_returns_own_value(oracle_mod):
+    case = W.make_case("w1", seed=31, query_lens=[4], past_lens=[20], num_q_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=8, sliding_window=1, poison=False)
+    got = run_oracle(oracle_mod, case)
+    _, vc = _decode_cache(case)
+    for i in range(4):
+        p = 20 + i
+        blk = case.block_tables[0][p // 8]
+        for h in range(4):
+            assert np.array_equal(got[i, h], vc[blk, h // 2, p % 8])
+
+
+def test_zero_query_gives_mean_of_visible_values(oracle_mod):
+    case = W.make_case("q0", seed=32, query_lens=[3], past_lens=[25], num_q_heads=2, num_kv_heads=1,
+                       head_dim=8, page_size=4, sliding_window=9)
+    case.q[:] = 0
+    got = run_oracle(oracle_mod, case)
+    _, vc = _decode_cache(case)
+    for i in range(3):
+        p = 25 + i
+        js = np.arange(p - 8, p + 1)
+        vals = vc[case.block_tables[0][js // 4], 0, js % 4]
+        np.testing.assert_allclose(got[i, 0], vals.mean(axis=0), rtol=0, atol=1e-13)
+
+
+def test_equal_keys_give_mean(oracle_mod):
+    case = W.make_case("eqk", seed=33, query_lens=[2], past_lens=[10], num_q_heads=2, num_kv_heads=1,
+                       head_dim=8, page_size=4, q_dtype="f32", kv_dtype="f32", poison=False)
+    kc = case.k_cache.reshape(case.num_blocks, 1, 4, 8)
+    kc[:] = kc[0, 0, 0]
+    got = run_oracle(oracle_mod, case)
+    _, vc = _decode_cache(case)
+    for i in range(2):
+        js = np.arange(0, 11 + i)
+        vals = vc[case.block_tables[0][js // 4], 0, js % 4]
+        np.testing.assert_allclose(got[i, 0], vals.mean(axis=0), rtol=0, atol=1e-12)
+
+
+def test_window_covering_everything_equals_no_window(oracle_mod):
+    case = W.make_case("wbig", seed=34, query_lens=[3], past_lens=[30], num_q_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=8)
+    a = run_oracle(oracle_mod, case)
+    b = run_oracle(oracle_mod, case, sliding_window=33)
+    c = run_oracle(oracle_mod, case, sliding_window=10_000)
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+# ---------------------------------------------------------------------------
+# Invariants.
+# ---------------------------------------------------------------------------
+
+def test_block_table_permutation_moves_pages(oracle_mod):
+    case = W.make_case("perm", seed=41, query_lens=[3], past_lens=[45], num_q_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=8)
+    a = run_oracle(oracle_mod, case)
+    rng = np.random.default_rng(7)
+    perm = rng.permutation(case.num_blocks)       # new physical id of each old block
+    inv = np.argsort(perm)
+    k2 = case.k_cache.reshape(case.num_blocks, -1)[inv].copy()
+    v2 = case.v_cache.reshape(case.num_blocks, -1)[inv].copy()
+    bt2 = perm[case.block_tables].astype(np.int32)
+    b = oracle_mod.forward(case.q, case.q_dtype, k2, v2, case.kv_dtype, bt2, case.past_lens,
+                           case.subsequence_begins, num_q_heads=4, num_kv_heads=2, head_dim=16, page_size=8,
+                           num_blocks=case.num_blocks, scale=case.scale)
+    assert np.array_equal(a, b)
+
+
+def test_future_and_out_of_window_keys_do_not_matter(oracle_mod):
+    L, T, Wn, ps = 30, 4, 6, 8
+    case = W.make_case("pert", seed=42, query_lens=[T], past_lens=[L], num_q_heads=2, num_kv_heads=1,
+                       head_dim=8, page_size=ps, q_dtype="f32", kv_dtype="f32", sliding_window=Wn)
+    a = run_oracle(oracle_mod, case)
+    kc = case.k_cache.reshape(case.num_blocks, 1, ps, 8)
+    vc = case.v_cache.reshape(case.num_blocks, 1, ps, 8)
+    # change the last new token's key/value: only token T-1 may move
+    p_last = L + T - 1
+    blk = case.block_tables[0][p_last // ps]
+    kc[blk, 0, p_last % ps] += 3.0
+    vc[blk, 0, p_last % ps] -= 5.0
+    b = run_oracle(oracle_mod, case)
+    assert np.array_equal(a[: T - 1], b[: T - 1])
+    assert not np.array_equal(a[T - 1], b[T - 1])
+    # change the key just before token 2's window: tokens >= 2 stay, token 1 moves
+    j = L + 2 - Wn
+    blk = case.block_tables[0][j // ps]
+    vc[blk, 0, j % ps] += 7.0
+    c = run_oracle(oracle_mod, case)
+    assert np.array_equal(b[2:], c[2:])
+    assert not np.array_equal(b[1], c[1])
+
+
+def test_output_inside_value_hull(oracle_mod):
+    case = small_cases()[1]
+    got = run_oracle(oracle_mod, case)
+    _, vc = _decode_cache(case)
+    L = int(case.past_lens[0])
+    for i in range(int(case.query_lens[0])):
+        js = np.arange(0, L + i + 1)
+        for h in range(case.num_q_heads):
+            vals = vc[case.block_tables[0][js // 16], h // 4, js % 16]
+            assert (got[i, h] >= vals.min(axis=0) - 1e-12).all()
+            assert (got[i, h] <= vals.max(axis=0) + 1e-12).all()
+
+
+def test_u8_equals_float_on_dequantised_cache(oracle_mod):
+    case = W.make_case("u8deq", seed=51, query_lens=[3], past_lens=[37], num_q_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=8, kv_dtype="u8", q_dtype="f32")
+    a = run_oracle(oracle_mod, case)
+    kc, vc = _decode_cache(case)
+    b = oracle_mod.forward(case.q, "f32", kc.astype(np.float32), vc.astype(np.float32), "f32",
+                           case.block_tables, case.past_lens, case.subsequence_begins, num_q_heads=4,
+                           num_kv_heads=2, head_dim=16, page_size=8, num_blocks=case.num_blocks,
+                           scale=case.scale)
+    finite = np.isfinite(a)
+    assert finite.all()
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Stored-value decoding over every 16-bit pattern (single visible key: out = V).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_every_16bit_pattern_decodes_exactly(oracle_mod, dtype):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = W.storage_to_f64(bits, dtype)
+    keep = np.isfinite(vals)
+    bits, vals = bits[keep], vals[keep]
+    n = bits.shape[0]
+    # n sequences, each L=0, T=1, its own page (page_size 1, D=1); V holds one pattern.
+    bt = np.arange(n, dtype=np.int32)[:, None]
+    q = np.zeros((n, 1, 1), dtype=np.uint16)
+    k = np.zeros((n, 1, 1, 1), dtype=np.uint16)
+    v = bits.reshape(n, 1, 1, 1)
+    got = oracle_mod.forward(q, dtype, k, v, dtype, bt, np.zeros(n, np.int32), np.arange(n + 1, dtype=np.int32),
+                             num_q_heads=1, num_kv_heads=1, head_dim=1, page_size=1, num_blocks=n, scale=1.0)
+    assert np.array_equal(got.reshape(n), vals)
+
+
+# ---------------------------------------------------------------------------
+# Pages touched: brute force over every row's key range.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("idx", range(6))
+def test_pages_touched_brute_force(oracle_mod, idx):
+    case = small_cases()[idx]
+    got = oracle_mod.pages_touched(case.block_tables, case.past_lens, case.subsequence_begins,
+                                   page_size=case.page_size, sliding_window=case.sliding_window)
+    want = np.zeros_like(case.block_tables)
+    for b in range(case.num_seqs):
+        L = int(case.past_lens[b])
+        for i in range(int(case.query_lens[b])):
+            p = L + i
+            lo = max(0, p - case.sliding_window + 1) if case.sliding_window > 0 else 0
+            for j in range(lo, p + 1):
+                want[b, j // case.page_size] = case.block_tables[b, j // case.page_size] + 1
+    assert np.array_equal(got, want)
+
+
+def test_bad_block_id_is_reported(oracle_mod):
+    case = small_cases()[1]
+    case.block_tables[0, 1] = case.num_blocks + 5
+    with pytest.raises(ValueError):
+        run_oracle(oracle_mod, case)
+
+
+def test_workload_families_have_stated_shapes():
+    c = W.tiny()
+    assert (c.num_q_heads, c.num_kv_heads, c.head_dim, c.page_size, c.total_tokens) == (8, 2, 64, 16, 3)
+    assert c.q_dtype == "f32" and int(c.past_lens[0]) == 512
+    a = W.batched_mix_a()
+    assert a.num_seqs == 8 and a.sliding_window == 1024
+    assert ((a.query_lens >= 1) & (a.query_lens <= 4)).all()
+    assert ((a.past_lens >= 2000) & (a.past_lens <= 4000)).all()
