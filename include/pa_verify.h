@@ -1,0 +1,191 @@
+/*
+ * pa_verify.h — C ABI of the paged verify-attention library (libpa_verify.so).
+ *
+ * One call computes, for a batch of sequences that each bring T_b = 1..8 new
+ * query tokens against a long paged KV cache, the attention output of every
+ * new token, the way a speculative-decoding verify step needs it:
+ *
+ *   query token i of sequence b sits at position p = past_len_b + i and
+ *   attends keys lo..p, lo = (W > 0) ? max(0, p - W + 1) : 0;
+ *   out[t, h, :] = softmax_j(scale * q[t, h, :] . K_j) weighted sum of V_j,
+ *   t = subsequence_begins[b] + i, with K_j / V_j of KV head h / (Hq / Hkv).
+ *
+ * Sources for the operation (web pages on paged attention in speculative
+ * decoding):
+ *  - OpenVINO issue 38153, "Performance issue description": a verify forward
+ *    hands the paged-attention op k+1 query tokens of one sequence with a long
+ *    past_len; the suggested handling gives query token i the key limit
+ *    past_len + i + 1, equal to i single-token decodes.  "Cause": the fast
+ *    single-token stage reads each KV head once for all GQA heads and splits
+ *    the context into partitions — both kept here for T > 1.
+ *  - OpenVINO issue 38153, "Step-by-step reproduction" step 3: the op inputs
+ *    past_lens, subsequence_begins, max_context_len and the block table; step 1:
+ *    u8 KV cache precision.
+ *  - dual-radeon-vllm article (speculative decoding net loss), section on the
+ *    use_3d gate: the split-KV segment buffer must be indexed per query token,
+ *    not per sequence; a segment reduction merges the partial results.
+ *  - SGLang discussion 36314, "Observation 3": sliding-window layers (window
+ *    1024) read only the last window of keys.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *    owned by the caller.  The library allocates nothing, keeps no per-call
+ *    state and never synchronises (except pa_verify_get_device_status, which
+ *    synchronises the given stream).  All work is enqueued on `cuda_stream`
+ *    (a cudaStream_t; NULL = legacy default stream).
+ *  - q, k_cache, v_cache, out and workspace must be 16-byte aligned; the int32
+ *    arrays 4-byte aligned.
+ *  - Return value: PA_OK (0) or a negative PA_ERR_* code.  On a negative code
+ *    nothing was enqueued (except PA_ERR_CUDA, which reports a failed launch).
+ *  - Inconsistencies only visible on the device (a query length outside
+ *    0..8, past_len + T_b > max_context_len, a block id outside
+ *    [0, num_blocks), malformed subsequence_begins) set bits of a sticky
+ *    status word inside the workspace (PA_STATUS_*), skip the affected work
+ *    and leave the affected sequence's output rows zero.  Nothing traps.
+ */
+#ifndef PA_VERIFY_H
+#define PA_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  PA_U8 is valid only as a KV-cache type. */
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_U8 = 3 } pa_dtype;
+
+/* Host-detected errors (returned; nothing launched). */
+enum {
+  PA_OK = 0,
+  PA_ERR_NULL = -1,        /* a required pointer is NULL                          */
+  PA_ERR_DTYPE = -2,       /* unsupported q / kv / out dtype combination          */
+  PA_ERR_SHAPE = -3,       /* non-positive count, Hq % Hkv != 0, bad table width  */
+  PA_ERR_HEAD_DIM = -4,    /* head_dim not in {64, 128, 256} (u8: {128, 256})     */
+  PA_ERR_PAGE_SIZE = -5,   /* page_size not a power of two in [8, 256]           */
+  PA_ERR_ALIGN = -6,       /* a pointer misses its alignment                      */
+  PA_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than pa_verify_workspace_size */
+  PA_ERR_CONTEXT = -8,     /* max_context_len < 1 while tokens are present, or too large */
+  PA_ERR_CUDA = -9,        /* a CUDA runtime call or kernel launch failed          */
+  PA_ERR_UNSUPPORTED = -10 /* (Hq/Hkv) * min(8, total_tokens) query rows exceed the
+                              per-KV-head row capacity (64; 32 for head_dim 256)  */
+};
+
+/* Device-detected status bits (sticky until read by pa_verify_get_device_status). */
+#define PA_STATUS_QUERY_LEN 0x1u  /* a sequence has T_b > 8 (or T_b < 0)          */
+#define PA_STATUS_CONTEXT   0x2u  /* past_len_b + T_b > max_context_len            */
+#define PA_STATUS_BLOCK_ID  0x4u  /* a block id read is outside [0, num_blocks)    */
+#define PA_STATUS_BEGINS    0x8u  /* subsequence_begins not monotone / wrong total */
+#define PA_STATUS_PAST_LEN  0x10u /* past_len_b < 0                                 */
+#define PA_STATUS_ROWS      0x20u /* T_b * (Hq/Hkv) above the row capacity          */
+#define PA_STATUS_TIMEOUT   0x40u /* a bounded wait inside a kernel gave up         */
+
+#define PA_MAX_QUERY_LEN 8
+
+/* Problem dimensions. */
+typedef struct {
+  int32_t num_seqs;           /* B                                                   */
+  int32_t total_tokens;       /* sum_b T_b = subsequence_begins[B]                    */
+  int32_t num_q_heads;        /* Hq                                                  */
+  int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0, query head h uses KV head h/(Hq/Hkv) */
+  int32_t head_dim;           /* D                                                   */
+  int32_t page_size;          /* ps: tokens per KV page                              */
+  int32_t num_blocks;         /* physical pages in each cache                        */
+  int32_t max_blocks_per_seq; /* width of the block table                            */
+  pa_dtype q_dtype;           /* F32, F16 or BF16                                    */
+  pa_dtype out_dtype;         /* F32, F16 or BF16                                    */
+} pa_dims;
+
+/* The launch plan the partition heuristic picks (exposed for inspection). */
+typedef struct {
+  int32_t num_partitions;  /* P: KV partitions per (sequence, KV head), grid.x   */
+  int32_t part_tokens;     /* keys per partition (multiple of the stage size)     */
+  int32_t stage_keys;      /* keys staged per pipeline step                       */
+  int32_t row_tiles;       /* n-tiles of 8 query rows per warp (1 or 2)           */
+  int32_t kernel;          /* 0 = tensor-core path (16-bit / u8 KV), 1 = fp32 path */
+  int32_t num_sms;         /* SM count the plan was made for                       */
+  int32_t ctas;            /* grid size B * Hkv * P                                */
+  int32_t smem_bytes;      /* dynamic shared memory per partition CTA             */
+} pa_plan;
+
+/*
+ * Storage layouts (the pages leave these open; this library fixes them):
+ *  q    [total_tokens, Hq, D] in q_dtype, rows ordered by subsequence_begins.
+ *  out  [total_tokens, Hq, D] in out_dtype.
+ *  float / 16-bit caches: [num_blocks, Hkv, ps, D] in kv_dtype — one page of
+ *       one KV head is a contiguous [ps, D] tile.
+ *  u8 caches: [num_blocks, Hkv, ps*(D+4)] bytes — per page per KV head one
+ *       record: ps*D code bytes (slot-major), then ps fp16 scales, then ps
+ *       fp16 zero-points; value = (code - zero_point) * scale.
+ *  block_tables [B, max_blocks_per_seq] int32: logical page j/ps of sequence b
+ *       lives in physical page block_tables[b][j/ps].
+ *  past_lens [B] int32, subsequence_begins [B+1] int32 (device memory).
+ *  The cache already holds the new tokens' K/V at positions past_len..past_len+T-1.
+ */
+
+/* Bytes of workspace pa_verify_forward needs for these dimensions (0 on bad
+ * arguments).  Plans for the current device's SM count.  The workspace holds
+ * the per-token split-KV partials and the status word; zero it once before
+ * its first use (the status word must start at 0). */
+size_t pa_verify_workspace_size(const pa_dims* dims, int32_t max_context_len,
+                                int32_t sliding_window, pa_dtype kv_dtype);
+
+/* The partition heuristic for an explicit SM count (host only, no CUDA call).
+ * Returns PA_OK or a PA_ERR_* code for arguments pa_verify_forward would reject. */
+int pa_verify_plan(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window,
+                   pa_dtype kv_dtype, int32_t num_sms, pa_plan* plan);
+
+/*
+ * The verify step: split-KV partition kernel (page gather once per KV head
+ * for all T_b x group query rows, online softmax, fused u8 dequantisation,
+ * per-token partials) followed by the per-token log-sum-exp combine.
+ * max_context_len (host) must be >= past_len_b + T_b for every b; it sizes
+ * the partition grid.  sliding_window = 0 means no window.  scale multiplies
+ * q.k before the softmax.  Asynchronous on cuda_stream.
+ */
+int pa_verify_forward(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* past_lens,
+                      const int32_t* subsequence_begins, int32_t max_context_len, float scale,
+                      int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* As pa_verify_forward, and also records the page gather: for every page the
+ * partition kernel fetches it adds (physical block id + 1) to
+ * gather_trace[(b * Hkv + kv_head) * max_blocks_per_seq + logical_page]
+ * (device int32 buffer, zeroed by the caller).  A page fetched once therefore
+ * reads block_id + 1; pages never fetched stay 0. */
+int pa_verify_forward_traced(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* past_lens,
+                             const int32_t* subsequence_begins, int32_t max_context_len,
+                             float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out,
+                             const pa_dims* dims, void* workspace, size_t workspace_bytes,
+                             void* cuda_stream, int32_t* gather_trace);
+
+/* The two steps of pa_verify_forward as separate launches (same arguments),
+ * so a caller can time or overlap them individually.  pa_verify_partition
+ * writes the per-token partials (and the output of every sequence whose
+ * context fits one partition); pa_verify_combine merges the partials of the
+ * others into out.  Calling both in order equals one pa_verify_forward. */
+int pa_verify_partition(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* past_lens,
+                        const int32_t* subsequence_begins, int32_t max_context_len, float scale,
+                        int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                        void* workspace, size_t workspace_bytes, void* cuda_stream);
+int pa_verify_combine(const int32_t* past_lens, const int32_t* subsequence_begins,
+                      int32_t max_context_len, int32_t sliding_window, pa_dtype kv_dtype,
+                      void* out, const pa_dims* dims, void* workspace, size_t workspace_bytes,
+                      void* cuda_stream);
+
+/* Synchronises cuda_stream, then reads and clears the workspace's status word
+ * into *bits (PA_STATUS_* flags, 0 = clean). */
+int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits);
+
+/* Static description of a PA_OK / PA_ERR_* code. */
+const char* pa_verify_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_VERIFY_H */

@@ -1,0 +1,269 @@
+// pa_device.cuh — device-side building blocks of the paged verify-attention
+// kernels for sm_103a: mbarrier / TMA / bulk-copy wrappers, warp-level mma
+// fragments, and the per-sequence bookkeeping shared by the partition and
+// combine kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <climits>
+
+#include "../../include/pa_verify.h"
+
+namespace pa {
+
+enum KvKind : int { KV_BF16 = 0, KV_F16 = 1, KV_U8 = 2 };
+
+constexpr int kConsumerWarps = 4;            // warps that do the math
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one TMA producer warp
+constexpr int kMaxPagesPerCta = 1024;        // block ids staged in shared memory
+constexpr uint32_t kWaitLimit = 1u << 22;    // bounded mbarrier polls before giving up
+
+// Arguments common to the partition kernels (plain values, passed by value).
+struct PartArgs {
+  const void* q;
+  const uint8_t* k_bytes;       // cache bases (u8 records need byte addressing)
+  const uint8_t* v_bytes;
+  const int32_t* block_tables;
+  const int32_t* past_lens;
+  const int32_t* begins;
+  void* out;
+  float* po;                    // [total_tokens, Hq, P, D] unnormalised partial outputs
+  float* pm;                    // [total_tokens, Hq, P] running max (log2 domain)
+  float* pl;                    // [total_tokens, Hq, P] softmax denominators (-1 = poisoned)
+  uint32_t* status;
+  int32_t* trace;               // optional gather trace
+  int num_seqs, total_tokens, Hq, Hkv, G, D, ps, ps_log2, num_blocks, max_blocks;
+  int max_ctx, window, part_tokens, num_parts, box_log2, row_cap;
+  int q_dtype, out_dtype;
+  float scale_log2;             // softmax scale * log2(e)
+};
+
+struct CombineArgs {
+  const int32_t* past_lens;
+  const int32_t* begins;
+  void* out;
+  const float* po;
+  const float* pm;
+  const float* pl;
+  uint32_t* status;
+  int num_seqs, total_tokens, Hq, Hkv, G, ps, max_ctx, window, part_tokens, num_parts, row_cap, out_dtype;
+};
+
+// ---------------------------------------------------------------------------
+// Per-sequence bookkeeping (identical in the partition and combine kernels).
+// ---------------------------------------------------------------------------
+struct SeqInfo {
+  int t0, T, L;          // first token row, new tokens, past length
+  int klo, khi;          // union of the rows' key ranges [klo, khi]
+  int kbase;             // klo rounded down to a page boundary
+  int nparts;            // partitions this sequence needs
+  uint32_t err;          // PA_STATUS_* bits that make the sequence invalid
+  bool rows_ok;          // t0 / T can be trusted to index output rows
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const int32_t* begins, const int32_t* past_lens, int b,
+                                            int total_tokens, int G, int ps, int max_ctx, int window,
+                                            int part_tokens, int row_capacity) {
+  SeqInfo s;
+  s.t0 = __ldg(begins + b);
+  const int t1 = __ldg(begins + b + 1);
+  s.L = __ldg(past_lens + b);
+  s.T = t1 - s.t0;
+  s.err = 0;
+  s.rows_ok = (s.t0 >= 0 && t1 >= s.t0 && t1 <= total_tokens);
+  if (!s.rows_ok) s.err |= PA_STATUS_BEGINS;
+  if (s.T > PA_MAX_QUERY_LEN) s.err |= PA_STATUS_QUERY_LEN;
+  if (s.L < 0) s.err |= PA_STATUS_PAST_LEN;
+  if ((long long)s.L + s.T > (long long)max_ctx) s.err |= PA_STATUS_CONTEXT;
+  if (s.T * G > row_capacity) s.err |= PA_STATUS_ROWS;
+  s.khi = s.L + s.T - 1;
+  s.klo = window > 0 ? max(0, s.L - window + 1) : 0;
+  s.kbase = (s.klo / ps) * ps;
+  s.nparts = (s.err || s.T <= 0) ? 0 : (s.khi + 1 - s.kbase + part_tokens - 1) / part_tokens;
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// Small numeric helpers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float load_q_elem(const void* q, int dtype, size_t idx) {
+  if (dtype == PA_F32) return __ldg(reinterpret_cast<const float*>(q) + idx);
+  const unsigned short bits = __ldg(reinterpret_cast<const unsigned short*>(q) + idx);
+  if (dtype == PA_BF16) return __bfloat162float(__ushort_as_bfloat16(bits));
+  return __half2float(__ushort_as_half(bits));
+}
+
+__device__ __forceinline__ void store_out(void* out, int dtype, size_t idx, float v) {
+  if (dtype == PA_F32) {
+    reinterpret_cast<float*>(out)[idx] = v;
+  } else if (dtype == PA_BF16) {
+    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory barriers and asynchronous copies (PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true when the phase completed, false after kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// 4-D tiled TMA load into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Named barrier among the consumer warps only (the producer warp skips it).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core fragments (mma.sync m16n8k16, fp32 accumulate).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (kBf16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// Transpose an 8x8 16-bit matrix held in mma fragment layout across the warp.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kBf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// Two u8 codes (bytes sel0 / sel1 of w) -> exact f16x2: place each byte in
+// the mantissa of 1024.0 (0x6400) and subtract 1024.
+__device__ __forceinline__ uint32_t u8pair_to_f16x2(uint32_t w, uint32_t selector) {
+  uint32_t h = __byte_perm(w, 0x64646464u, selector);
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&h), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Row permutation of the 16 keys of an mma tile: m -> key offset.  Pairs of
+// keys read by one quarter-warp land in different shared-memory bank halves
+// under the 128-byte swizzle (see the u8 fragment loaders).
+__device__ __forceinline__ int key_perm(int m) { return (m & 8) | ((5 * m) & 7); }
+
+// Byte offset of (key k of the stage, 128-byte column chunk c) in a stage tile
+// laid out as [segment][chunk][box_rows][128 B], box_rows = 1 << box_log2.
+__device__ __forceinline__ uint32_t tile_row_off(int k, int c, int box_log2, int n_chunks) {
+  const int br = 1 << box_log2;
+  return static_cast<uint32_t>((((k >> box_log2) * n_chunks + c) * br + (k & (br - 1))) * 128);
+}
+
+// 128-byte swizzle: 16-byte unit j of the row of key k sits at unit j ^ (k & 7).
+__device__ __forceinline__ uint32_t swz(int unit, int k) { return static_cast<uint32_t>(((unit ^ (k & 7)) << 4)); }
+
+}  // namespace pa

@@ -1,0 +1,31 @@
+// pa_launch.h — host-side launch helpers shared by the C-ABI implementation
+// and the per-head-dim instantiation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+// Static facts about one tensor-core partition kernel instantiation.
+struct MmaKernelInfo {
+  int stage_keys;   // keys per pipeline stage
+  int smem_bytes;   // dynamic shared memory
+};
+
+// Per head dim: info and launch of pa_partition_mma<D, kv, nt>.  kv is a
+// KvKind, nt the number of 8-row n-tiles per consumer warp.  Return false in
+// *ok if the combination is not instantiated.
+MmaKernelInfo mma_info_d64(int kv, int nt, bool* ok);
+MmaKernelInfo mma_info_d128(int kv, int nt, bool* ok);
+MmaKernelInfo mma_info_d256(int kv, int nt, bool* ok);
+cudaError_t launch_mma_d64(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                           cudaStream_t st);
+cudaError_t launch_mma_d128(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                            cudaStream_t st);
+cudaError_t launch_mma_d256(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                            cudaStream_t st);
+
+}  // namespace pa

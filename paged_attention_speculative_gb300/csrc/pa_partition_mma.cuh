@@ -1,0 +1,584 @@
+// pa_partition_mma.cuh — split-KV partition kernel, tensor-core path
+// (16-bit KV caches, and u8 caches dequantised on the fly).
+//
+// One CTA owns one (KV partition p, KV head g, sequence b).  It streams the
+// partition's pages once — for ALL T_b x G query rows of the GQA group (the
+// "GQA read-once, 256-token partitions" single-token stage of OpenVINO issue
+// 38153, "Cause", kept for T > 1) — and writes per-query-token partials
+// (max, denominator, unnormalised output) indexed [token, head, partition]
+// (the per-token segment buffer the dual-radeon-vllm article, use_3d section,
+// shows must replace a per-sequence one).
+//
+// Warp roles: warp 4 is the producer — it looks each page up in the block
+// table and issues 128-byte-swizzled TMA tile loads of the page's K and V
+// rows (plus 1-D bulk copies of u8 scales / zero-points) into a ring of
+// NS shared-memory stages guarded by full / empty mbarriers.  Warps 0..3 are
+// consumers: each owns a set of query rows (8 or 16) and a share of every
+// stage's 16-key chunks, and keeps its own online-softmax state, so no warp
+// waits on another inside the loop.  Scores are computed transposed,
+// S^T[key, row] = K . Q^T with mma.sync m16n8k16 (keys on M, query rows on N,
+// so 1..8 rows waste nothing), P is transposed in registers with movmatrix,
+// and O^T[d, row] += V^T . P^T.  The warps' states merge through shared
+// memory at the end.
+//
+// u8 caches: codes are exact in f16 (code = f16(0x6400 | code) - 1024), so
+// q.K = scale_j (q.code_j - zp_j sum(q)) and the value sum is
+// sum_j p_j scale_j code_j - sum_j p_j scale_j zp_j — the dequantisation costs
+// one FMA per key, not per element.
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+template <int D, int KV>
+struct MmaCfg {
+  static constexpr bool kU8 = (KV == KV_U8);
+  static constexpr bool kBf16 = (KV == KV_BF16);       // u8 math runs in f16
+  static constexpr int EB = kU8 ? 1 : 2;               // bytes per cache element
+  static constexpr int ROW_BYTES = D * EB;             // one key's row
+  static constexpr int CHUNKS = ROW_BYTES / 128;       // 128-byte swizzle rows per key
+  static constexpr int ELEMS_128 = 128 / EB;           // elements per 128-byte row
+  static constexpr int SK = (ROW_BYTES >= 512) ? 32 : 64;  // keys per pipeline stage
+  static constexpr int TILE = SK * ROW_BYTES;          // bytes of one K (or V) stage tile
+  static constexpr int SZ = kU8 ? SK * 2 : 0;          // one fp16 scale (or zp) array
+  static constexpr int STAGE = 2 * TILE + 4 * SZ;
+  static constexpr int NS = (STAGE <= 20 * 1024) ? 5 : 3;  // stages in flight
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MTILES = D / 16;
+  static constexpr int CHUNKS_PER_STAGE = SK / 16;
+  static_assert(CHUNKS >= 1, "head_dim too small for the swizzled layout");
+};
+
+template <int D, int KV, int NT>
+struct MmaSmem {
+  using C = MmaCfg<D, KV>;
+  static constexpr int RPW = 8 * NT;                   // rows per consumer warp
+  static constexpr int MERGE_LD = D + 4;
+  static constexpr int MERGE_BYTES = kConsumerWarps * RPW * (MERGE_LD + 2) * 4;
+  static_assert(MERGE_BYTES <= C::NS * C::STAGE, "merge area must fit in the stage ring");
+  static constexpr int BAR_OFF = C::NS * C::STAGE;
+  static constexpr int BLK_OFF = BAR_OFF + 2 * C::NS * 8;
+  static constexpr int BYTES = BLK_OFF + 4 * kMaxPagesPerCta + 1024;  // + alignment slack
+};
+
+// Physical head-dim index of mma row m of m-tile mt in the O^T accumulator.
+template <int D, bool kU8>
+__device__ __forceinline__ int out_dim(int mt, int m) {
+  if constexpr (kU8) return (D / 8) * (m & 7) + 2 * mt + (m >> 3);
+  else return 16 * mt + m;
+}
+
+template <int D, int KV, int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    pa_partition_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const PartArgs a) {
+  using C = MmaCfg<D, KV>;
+  using S = MmaSmem<D, KV, NT>;
+  constexpr bool kBf = C::kBf16;
+  constexpr int RPW = S::RPW;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+  uint64_t* empty = full + C::NS;
+  int32_t* blk = reinterpret_cast<int32_t*>(smem + S::BLK_OFF);
+  __shared__ int s_timeout;
+
+  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
+                              a.part_tokens, a.row_cap);
+  pdl_launch_dependents();
+
+  if (si.err) {
+    if (p == 0 && threadIdx.x == 0) atomicOr(a.status, si.err);
+    if (p == 0 && si.rows_ok) {  // leave the sequence's rows of this KV group zero
+      const int n = si.T * a.G * D;
+      for (int idx = threadIdx.x; idx < n; idx += kThreads) {
+        const int r = idx / D, d = idx % D;
+        const int t = si.t0 + r / a.G, h = g * a.G + r % a.G;
+        store_out(a.out, a.out_dtype, (static_cast<size_t>(t) * a.Hq + h) * D + d, 0.f);
+      }
+    }
+    return;
+  }
+  if (si.T <= 0 || p >= si.nparts) return;
+
+  const int kstart = si.kbase + p * a.part_tokens;
+  const int kend = min(kstart + a.part_tokens, si.khi + 1);
+  const int lp0 = kstart >> a.ps_log2;
+  const int npages = ((kend - 1) >> a.ps_log2) - lp0 + 1;
+  const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
+  const int R = si.T * a.G;
+
+  if (threadIdx.x == 0) {
+    s_timeout = 0;
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  int bad = 0;
+  for (int j = threadIdx.x; j < npages; j += kThreads) {
+    int id = __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+    if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+      bad = 1;
+      id = 0;
+    }
+    blk[j] = id;
+  }
+  if (__syncthreads_or(bad)) {
+    // A corrupt block table: report, and make this partition's contribution
+    // poison the rows (the combine, or the direct write below, zeroes them).
+    if (threadIdx.x == 0) atomicOr(a.status, PA_STATUS_BLOCK_ID);
+    for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+      const int r = idx / D, d = idx % D;
+      const size_t row = static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G;
+      if (si.nparts == 1) {
+        store_out(a.out, a.out_dtype, row * D + d, 0.f);
+      } else if (d == 0) {
+        a.pm[row * a.num_parts + p] = 0.f;
+        a.pl[row * a.num_parts + p] = -1.f;
+      }
+    }
+    return;
+  }
+
+  // =========================== producer warp ===============================
+  if (warp == kConsumerWarps) {
+    const int br_log2 = a.box_log2;
+    const int br = 1 << br_log2;
+    int issued = 0;
+    bool ok = true;
+    for (int s = 0; s < n_stages; ++s) {
+      const int slot = s % C::NS;
+      if (s >= C::NS && !mbar_wait(&empty[slot], ((s / C::NS) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const int key0 = kstart + s * C::SK;
+      const int nk = min(C::SK, kend - key0);
+      const int nseg = (nk + br - 1) >> br_log2;
+      uint32_t bytes = static_cast<uint32_t>(nseg * br * C::ROW_BYTES * 2);
+      if constexpr (C::kU8) bytes += static_cast<uint32_t>(nseg * br * 2 * 4);
+      uint8_t* st = smem + slot * C::STAGE;
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
+      __syncwarp();
+      for (int j = lane; j < nseg * C::CHUNKS; j += 32) {
+        const int seg = j / C::CHUNKS, c = j % C::CHUNKS;
+        const int key = key0 + (seg << br_log2);
+        const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+        const int id = blk[lp - lp0];
+        const uint32_t off = static_cast<uint32_t>(((seg * C::CHUNKS + c) << br_log2) * 128);
+        tma_load_4d(st + off, &tmK, c * C::ELEMS_128, slot0, g, id, &full[slot]);
+        tma_load_4d(st + C::TILE + off, &tmV, c * C::ELEMS_128, slot0, g, id, &full[slot]);
+        if (a.trace != nullptr && c == 0 && slot0 == 0)
+          atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
+      }
+      if constexpr (C::kU8) {
+        const size_t rec = static_cast<size_t>(a.ps) * (D + 4);
+        for (int j = lane; j < nseg; j += 32) {
+          const int key = key0 + (j << br_log2);
+          const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+          const int id = blk[lp - lp0];
+          const size_t roff = (static_cast<size_t>(id) * a.Hkv + g) * rec + static_cast<size_t>(a.ps) * D;
+          uint8_t* dst = st + 2 * C::TILE + 2 * (j << br_log2);
+          bulk_load(dst, a.k_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
+          bulk_load(dst + C::SZ, a.k_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
+          bulk_load(dst + 2 * C::SZ, a.v_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
+          bulk_load(dst + 3 * C::SZ, a.v_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
+        }
+      }
+      issued = s + 1;
+    }
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(a.status, PA_STATUS_TIMEOUT);
+        atomicOr(&s_timeout, 1);
+      }
+      // let the copies already in flight land before the CTA can retire
+      for (int s = max(0, issued - C::NS); s < issued; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
+    }
+    return;
+  }
+
+  // =========================== consumer warps ==============================
+  const int g8 = lane >> 2, tig = lane & 3;
+  int RG = (R + RPW - 1) / RPW;
+  RG = RG <= 1 ? 1 : (RG <= 2 ? 2 : 4);
+  const int KS = kConsumerWarps / RG;
+  const int rg = warp % RG, ks = warp / RG;
+  const int row_base = rg * RPW;
+  const int nvalid = min(max(R - row_base, 0), RPW);
+  const int nt_active = (nvalid + 7) >> 3;
+  const int L = si.L;
+
+  // Key limits of the rows this thread's accumulator columns hold (rows past
+  // R borrow the last valid row's limits so they mask like it).
+  int rlo[NT][2], rhi[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = min(row_base + nt * 8 + 2 * tig + j, R - 1);
+      rhi[nt][j] = L + r / a.G;
+      rlo[nt][j] = a.window > 0 ? rhi[nt][j] - a.window + 1 : INT_MIN;
+    }
+  const int last_row = row_base + max(nvalid, 1) - 1;
+  const int wmin_hi = L + min(row_base, R - 1) / a.G;
+  const int wmax_lo = a.window > 0 ? L + min(last_row, R - 1) / a.G - a.window + 1 : INT_MIN;
+
+  // Q^T fragments (B operand), loaded once.
+  uint32_t qf[C::KSTEPS][NT][2];
+  float qs[NT][2];  // sum of the row's (f16) query, u8 path only
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int r = row_base + nt * 8 + g8;
+    const bool rv = r < R;
+    const int t = si.t0 + (rv ? r / a.G : 0), h = g * a.G + (rv ? r % a.G : 0);
+    const size_t qoff = (static_cast<size_t>(t) * a.Hq + h) * D;
+    float qsum = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < C::KSTEPS; ++kk) {
+      if constexpr (!C::kU8) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(a.q) + qoff);
+        qf[kk][nt][0] = rv ? __ldg(src + (16 * kk + 2 * tig) / 2) : 0u;
+        qf[kk][nt][1] = rv ? __ldg(src + (16 * kk + 8 + 2 * tig) / 2) : 0u;
+      } else {
+        const int dc = kk >> 3, half = (kk >> 2) & 1, sub = kk & 3;
+        const int d0 = 128 * dc + 16 * (tig + 4 * half) + 4 * sub;
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          x[e] = rv ? __half2float(__float2half_rn(load_q_elem(a.q, a.q_dtype, qoff + d0 + e))) : 0.f;
+        qf[kk][nt][0] = pack2<false>(x[0], x[1]);
+        qf[kk][nt][1] = pack2<false>(x[2], x[3]);
+        qsum += (x[0] + x[1]) + (x[2] + x[3]);
+      }
+    }
+    if constexpr (C::kU8) {
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) qs[nt][j] = __shfl_sync(0xffffffffu, qsum, (2 * tig + j) * 4);
+    } else {
+      qs[nt][0] = qs[nt][1] = 0.f;
+    }
+  }
+
+  float m_r[NT][2], l_r[NT][2], zc[NT][2];
+  float o[C::MTILES][NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      m_r[nt][j] = -INFINITY;
+      l_r[nt][j] = 0.f;
+      zc[nt][j] = 0.f;
+    }
+#pragma unroll
+  for (int mt = 0; mt < C::MTILES; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+
+  // Per-lane ldmatrix roles: K tile (A of S^T, not transposed) and V tile
+  // (A of O^T, transposed).
+  const int mK = ((lane >> 3) & 1) * 8 + (lane & 7), hiK = (lane >> 4) & 1;
+  const int mV = ((lane >> 4) & 1) * 8 + (lane & 7), hiV = (lane >> 3) & 1;
+  const float sl2 = a.scale_log2;
+  bool timed_out = false;
+
+  for (int s = 0; s < n_stages; ++s) {
+    const int slot = s % C::NS;
+    if (!mbar_wait(&full[slot], (s / C::NS) & 1)) {
+      timed_out = true;
+      break;
+    }
+    uint8_t* st = smem + slot * C::STAGE;
+    const uint32_t kt = smem_u32(st), vt = kt + C::TILE;
+    const int key0 = kstart + s * C::SK;
+    if (nt_active > 0) {
+      for (int c = ks; c < C::CHUNKS_PER_STAGE; c += KS) {
+        const int ck0 = key0 + 16 * c;
+        if (ck0 >= kend) break;
+        const int kg0 = ck0 + key_perm(g8);  // keys of accumulator rows g8 and g8 + 8
+        const int kg1 = kg0 + 8;
+
+        // ---------------- S^T = K . Q^T ----------------
+        float sa[2][NT][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sa[u][nt][e] = 0.f;
+        float ksc[2] = {1.f, 1.f}, kzp[2] = {0.f, 0.f};
+        if constexpr (!C::kU8) {
+          const int kk = 16 * c + key_perm(mK);
+#pragma unroll
+          for (int k = 0; k < C::KSTEPS; ++k) {
+            const int col = 16 * k;
+            const int ch = col / C::ELEMS_128;
+            const int unit = ((col % C::ELEMS_128) >> 3) + hiK;
+            uint32_t af[4];
+            ldsm_x4(kt + tile_row_off(kk, ch, a.box_log2, C::CHUNKS) + swz(unit, kk), af[0], af[1], af[2], af[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              if (nt < nt_active) mma16816<kBf>(sa[k & 1][nt], af, qf[k][nt][0], qf[k][nt][1]);
+          }
+        } else {
+          uint4 kw[2][C::CHUNKS][2];
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh) {
+            const int kk = 16 * c + key_perm(g8 + 8 * kh);
+#pragma unroll
+            for (int dc = 0; dc < C::CHUNKS; ++dc)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                kw[kh][dc][hf] = *reinterpret_cast<const uint4*>(
+                    st + tile_row_off(kk, dc, a.box_log2, C::CHUNKS) + swz(tig + 4 * hf, kk));
+            const __half* scp = reinterpret_cast<const __half*>(st + 2 * C::TILE);
+            ksc[kh] = __half2float(scp[kk]) * sl2;
+            kzp[kh] = __half2float(scp[C::SK + kk]);
+          }
+#pragma unroll
+          for (int k = 0; k < C::KSTEPS; ++k) {
+            const int dc = k >> 3, hf = (k >> 2) & 1, sub = k & 3;
+            const uint32_t w0 = reinterpret_cast<const uint32_t*>(&kw[0][dc][hf])[sub];
+            const uint32_t w1 = reinterpret_cast<const uint32_t*>(&kw[1][dc][hf])[sub];
+            uint32_t af[4];
+            af[0] = u8pair_to_f16x2(w0, 0x4140u);
+            af[1] = u8pair_to_f16x2(w1, 0x4140u);
+            af[2] = u8pair_to_f16x2(w0, 0x4342u);
+            af[3] = u8pair_to_f16x2(w1, 0x4342u);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              if (nt < nt_active) mma16816<false>(sa[k & 1][nt], af, qf[k][nt][0], qf[k][nt][1]);
+          }
+        }
+
+        // ---------------- scale, mask, online softmax ----------------
+        const bool clean = ck0 >= wmax_lo && ck0 + 15 <= wmin_hi;
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float acc = sa[0][nt][e] + sa[1][nt][e];
+            float v;
+            if constexpr (C::kU8) v = (acc - kzp[e >> 1] * qs[nt][e & 1]) * ksc[e >> 1];
+            else v = acc * sl2;
+            if (!clean) {
+              const int key = (e >> 1) ? kg1 : kg0;
+              const bool okk = key >= rlo[nt][e & 1] && key <= rhi[nt][e & 1];
+              v = okk ? v : -INFINITY;
+            }
+            sc[nt][e] = v;
+          }
+        float alpha[NT][2];
+        bool need_rescale = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(sc[nt][j], sc[nt][2 + j]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mnew = fmaxf(m_r[nt][j], mx);
+            const float mu = (mnew == -INFINITY) ? 0.f : mnew;
+            alpha[nt][j] = ex2(m_r[nt][j] - mu);
+            need_rescale |= (mnew != m_r[nt][j]);
+            m_r[nt][j] = mnew;
+            sc[nt][j] = ex2(sc[nt][j] - mu);
+            sc[nt][2 + j] = ex2(sc[nt][2 + j] - mu);
+            l_r[nt][j] = l_r[nt][j] * alpha[nt][j] + sc[nt][j] + sc[nt][2 + j];
+          }
+        if (__any_sync(0xffffffffu, need_rescale)) {
+#pragma unroll
+          for (int mt = 0; mt < C::MTILES; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o[mt][nt][e] *= alpha[nt][e & 1];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) zc[nt][j] *= alpha[nt][j];
+        }
+
+        // ---------------- P^T (B operand of O^T = V^T P^T) ----------------
+        uint32_t pb[NT][2];
+        if constexpr (!C::kU8) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            pb[nt][0] = movmatrix_t(pack2<kBf>(sc[nt][0], sc[nt][1]));
+            pb[nt][1] = movmatrix_t(pack2<kBf>(sc[nt][2], sc[nt][3]));
+          }
+        } else {
+          const __half* scp = reinterpret_cast<const __half*>(st + 2 * C::TILE + 2 * C::SZ);
+          float vsc[2], vzp[2];
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh) {
+            const int kk = 16 * c + key_perm(g8 + 8 * kh);
+            const int key = kk + key0;
+            const bool in_union = key >= si.klo && key <= si.khi;
+            vsc[kh] = in_union ? __half2float(scp[kk]) : 0.f;
+            vzp[kh] = in_union ? __half2float(scp[C::SK + kk]) : 0.f;
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t h0 = pack2<false>(sc[nt][0] * vsc[0], sc[nt][1] * vsc[0]);
+            const uint32_t h1 = pack2<false>(sc[nt][2] * vsc[1], sc[nt][3] * vsc[1]);
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+            zc[nt][0] += f0.x * vzp[0] + f1.x * vzp[1];
+            zc[nt][1] += f0.y * vzp[0] + f1.y * vzp[1];
+            pb[nt][0] = movmatrix_t(h0);
+            pb[nt][1] = movmatrix_t(h1);
+          }
+        }
+
+        // ---------------- O^T += V^T . P^T ----------------
+        if constexpr (!C::kU8) {
+          if (ck0 < si.klo || ck0 + 15 > si.khi) {
+            // keys outside every row's range may hold garbage (even NaN);
+            // their weight is 0, but 0 * NaN is not, so clear those V rows.
+            constexpr int UNITS = C::ROW_BYTES / 16;
+            for (int idx = lane; idx < 16 * UNITS; idx += 32) {
+              const int m = idx / UNITS, u = idx % UNITS;
+              const int key = ck0 + m;
+              if (key < si.klo || key > si.khi)
+                *reinterpret_cast<uint4*>(st + C::TILE + tile_row_off(16 * c + m, u >> 3, a.box_log2, C::CHUNKS) +
+                                          16 * (u & 7)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async();
+            __syncwarp();
+          }
+          const int kk = 16 * c + key_perm(mV);
+#pragma unroll
+          for (int mt = 0; mt < C::MTILES; ++mt) {
+            const int col = 16 * mt;
+            const int ch = col / C::ELEMS_128;
+            const int unit = ((col % C::ELEMS_128) >> 3) + hiV;
+            uint32_t af[4];
+            ldsm_x4_t(vt + tile_row_off(kk, ch, a.box_log2, C::CHUNKS) + swz(unit, kk), af[0], af[1], af[2], af[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              if (nt < nt_active) mma16816<kBf>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
+          }
+        } else {
+          // thread (g8, tig) needs keys k-slots 2tig, 2tig+1, 2tig+8, 2tig+9 at
+          // head-dim range [(D/8) g8, (D/8)(g8+1)) — one or two 16-byte units.
+          constexpr int VW = C::CHUNKS;  // uint4 words per key
+          uint4 vw[4][VW];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int slotk = 2 * tig + (q4 & 1) + 8 * (q4 >> 1);
+            const int kk = 16 * c + key_perm(slotk);
+#pragma unroll
+            for (int w = 0; w < VW; ++w) {
+              const int unit = (VW == 1) ? g8 : ((2 * g8 + w) & 7);
+              const int dc = (VW == 1) ? 0 : (g8 >> 2);
+              vw[q4][w] = *reinterpret_cast<const uint4*>(st + C::TILE + tile_row_off(kk, dc, a.box_log2, C::CHUNKS) +
+                                                          swz(unit, kk));
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < C::MTILES; ++mt) {
+            const int wi = mt >> 1;
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vw[0][wi >> 2])[wi & 3];
+            const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vw[1][wi >> 2])[wi & 3];
+            const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vw[2][wi >> 2])[wi & 3];
+            const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vw[3][wi >> 2])[wi & 3];
+            const uint32_t t01 = __byte_perm(w0, w1, sel);
+            const uint32_t t23 = __byte_perm(w2, w3, sel);
+            uint32_t af[4];
+            af[0] = u8pair_to_f16x2(t01, 0x4140u);
+            af[1] = u8pair_to_f16x2(t01, 0x4342u);
+            af[2] = u8pair_to_f16x2(t23, 0x4140u);
+            af[3] = u8pair_to_f16x2(t23, 0x4342u);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              if (nt < nt_active) mma16816<false>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+  if (timed_out && lane == 0) {
+    atomicOr(a.status, PA_STATUS_TIMEOUT);
+    atomicOr(&s_timeout, 1);
+  }
+
+  // =========================== merge & write ===============================
+  consumer_sync();  // every consumer is done with the stage ring
+  float* mo = reinterpret_cast<float*>(smem);
+  float* mm = mo + kConsumerWarps * RPW * S::MERGE_LD;
+  float* ml = mm + kConsumerWarps * RPW;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float l = l_r[nt][j], z = zc[nt][j];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      z += __shfl_xor_sync(0xffffffffu, z, 4);
+      z += __shfl_xor_sync(0xffffffffu, z, 8);
+      z += __shfl_xor_sync(0xffffffffu, z, 16);
+      l_r[nt][j] = l;
+      zc[nt][j] = z;
+      if (g8 == 0) {
+        mm[warp * RPW + nt * 8 + 2 * tig + j] = m_r[nt][j];
+        ml[warp * RPW + nt * 8 + 2 * tig + j] = l;
+      }
+    }
+#pragma unroll
+  for (int mt = 0; mt < C::MTILES; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int rl = nt * 8 + 2 * tig + (e & 1);
+        const int d = out_dim<D, C::kU8>(mt, g8 + 8 * (e >> 1));
+        mo[(warp * RPW + rl) * S::MERGE_LD + d] = o[mt][nt][e] - zc[nt][e & 1];
+      }
+  consumer_sync();
+
+  const bool poisoned = s_timeout != 0;
+  for (int idx = threadIdx.x; idx < R * D; idx += kConsumerWarps * 32) {
+    const int r = idx / D, d = idx % D;
+    const int rgr = r / RPW, rl = r % RPW;
+    float M = -INFINITY;
+    for (int k2 = 0; k2 < KS; ++k2) M = fmaxf(M, mm[(k2 * RG + rgr) * RPW + rl]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float acc = 0.f, lsum = 0.f;
+    for (int k2 = 0; k2 < KS; ++k2) {
+      const int wr = (k2 * RG + rgr) * RPW + rl;
+      const float wgt = ex2(mm[wr] - Mu);
+      acc += wgt * mo[wr * S::MERGE_LD + d];
+      lsum += wgt * ml[wr];
+    }
+    const size_t row = static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G;
+    if (si.nparts == 1) {
+      store_out(a.out, a.out_dtype, row * D + d, (poisoned || !(lsum > 0.f)) ? 0.f : acc / lsum);
+    } else {
+      const size_t pr = row * a.num_parts + p;
+      a.po[pr * D + d] = acc;
+      if (d == 0) {
+        a.pm[pr] = M;
+        a.pl[pr] = poisoned ? -1.f : lsum;
+      }
+    }
+  }
+}
+
+}  // namespace pa

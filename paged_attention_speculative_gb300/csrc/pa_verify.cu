@@ -1,0 +1,444 @@
+// pa_verify.cu — C-ABI implementation: argument checks, the partition-count
+// heuristic, TMA descriptor set-up and the kernel launches.
+//
+// The heuristic follows the split-KV idea of the pages (OpenVINO issue 38153,
+// "Cause": 256-token partitions of the single-token stage; dual-radeon-vllm
+// article: the 3D kernel splits a long KV sequence into segments reduced in
+// parallel, and a fix derives its threshold from the SM count): the key range
+// every (sequence, KV head) must stream is cut into equal partitions so that
+// the grid fills the GPU's SMs about once, partitions never shrink below the
+// size at which per-token partials would cost more than ~10 % of the KV bytes,
+// and the split does not depend on how many query tokens a sequence brings.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pa_verify.h"
+#include "pa_combine.cuh"
+#include "pa_launch.h"
+#include "pa_partition_f32.cuh"
+
+namespace {
+
+using pa::CombineArgs;
+using pa::PartArgs;
+
+constexpr size_t kStatusBytes = 256;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+long long round_up(long long a, long long q) { return ceil_div(a, q) * q; }
+
+int dtype_bytes(pa_dtype t) { return t == PA_F32 ? 4 : (t == PA_U8 ? 1 : 2); }
+
+// Optional tuning override of the partition size (keys), read once.
+int env_part_tokens() {
+  static const int v = [] {
+    const char* s = std::getenv("PA_VERIFY_PART_TOKENS");
+    return s ? std::atoi(s) : 0;
+  }();
+  return v;
+}
+
+int mma_kind(pa_dtype kv) { return kv == PA_BF16 ? pa::KV_BF16 : (kv == PA_F16 ? pa::KV_F16 : pa::KV_U8); }
+
+pa::MmaKernelInfo mma_info(int D, int kind, int nt, bool* ok) {
+  if (D == 64) return pa::mma_info_d64(kind, nt, ok);
+  if (D == 128) return pa::mma_info_d128(kind, nt, ok);
+  if (D == 256) return pa::mma_info_d256(kind, nt, ok);
+  *ok = false;
+  return pa::MmaKernelInfo{0, 0};
+}
+
+// Argument checks shared by every entry point; fills the plan.
+int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, int32_t num_sms, pa_plan* plan) {
+  if (d == nullptr || plan == nullptr) return PA_ERR_NULL;
+  std::memset(plan, 0, sizeof(*plan));
+  if (d->num_seqs < 1 || d->num_seqs > 65535 || d->total_tokens < 0 || d->num_q_heads < 1 ||
+      d->num_kv_heads < 1 || d->num_kv_heads > 65535 || d->num_q_heads % d->num_kv_heads != 0 ||
+      d->num_blocks < 1 || d->max_blocks_per_seq < 1 || window < 0 || num_sms < 1)
+    return PA_ERR_SHAPE;
+  const int D = d->head_dim;
+  if (D != 64 && D != 128 && D != 256) return PA_ERR_HEAD_DIM;
+  if (kv == PA_U8 && D == 64) return PA_ERR_HEAD_DIM;
+  const int ps = d->page_size;
+  if (!pow2(ps) || ps < 8 || ps > 256) return PA_ERR_PAGE_SIZE;
+  const pa_dtype qd = d->q_dtype, od = d->out_dtype;
+  if (od != PA_F32 && od != PA_F16 && od != PA_BF16) return PA_ERR_DTYPE;
+  bool combo = (kv == PA_F32 && (qd == PA_F32 || qd == PA_F16 || qd == PA_BF16)) ||
+               (kv == PA_BF16 && qd == PA_BF16) || (kv == PA_F16 && qd == PA_F16) ||
+               (kv == PA_U8 && (qd == PA_BF16 || qd == PA_F16));
+  if (!combo) return PA_ERR_DTYPE;
+  if (d->total_tokens > 0 &&
+      (max_ctx < 1 || static_cast<long long>(max_ctx) > static_cast<long long>(d->max_blocks_per_seq) * ps))
+    return PA_ERR_CONTEXT;
+  if (max_ctx < 0) return PA_ERR_CONTEXT;
+
+  const int G = d->num_q_heads / d->num_kv_heads;
+  const int tmax = std::min(PA_MAX_QUERY_LEN, std::max(d->total_tokens, 1));
+  const long long rows = static_cast<long long>(G) * tmax;
+  int kernel = (kv == PA_F32) ? 1 : 0;
+  int nt = 0, sk = 64, smem = 0, ctas_per_sm = 4;
+  if (kernel == 0) {
+    nt = (D == 256 || rows <= 8) ? 1 : 2;
+    const int cap = pa::kConsumerWarps * 8 * nt;
+    if (rows > cap) return PA_ERR_UNSUPPORTED;
+    bool ok = false;
+    pa::MmaKernelInfo info = mma_info(D, mma_kind(kv), nt, &ok);
+    if (!ok) return PA_ERR_UNSUPPORTED;
+    sk = info.stage_keys;
+    smem = info.smem_bytes;
+    ctas_per_sm = 2;
+  }
+  const long long quantum = std::max(sk, ps);
+  const long long ctx = std::max<long long>(max_ctx, 1);
+  long long span = window > 0 ? std::min<long long>(ctx, static_cast<long long>(window) + tmax - 1 + ps - 1) : ctx;
+  const long long units = static_cast<long long>(d->num_seqs) * d->num_kv_heads;
+  const long long per_key = 2LL * D * dtype_bytes(kv) + (kv == PA_U8 ? 8 : 0);
+  const long long target = static_cast<long long>(num_sms) * ctas_per_sm;
+  long long part = ceil_div(span * units, target);
+  const long long min_part = ceil_div(10LL * rows * (D + 2) * 4, per_key);
+  part = std::max(part, min_part);
+  if (env_part_tokens() > 0) part = env_part_tokens();
+  part = round_up(std::max<long long>(part, 1), quantum);
+  part = std::min(part, round_up(span, quantum));
+  const long long page_cap = (static_cast<long long>(pa::kMaxPagesPerCta - 1) * ps / quantum) * quantum;
+  part = std::min(part, std::max(page_cap, quantum));
+  const long long P = ceil_div(span, part);
+  if (P > 65535 || P * units > (1LL << 31)) return PA_ERR_UNSUPPORTED;
+
+  plan->num_partitions = static_cast<int32_t>(P);
+  plan->part_tokens = static_cast<int32_t>(part);
+  plan->stage_keys = sk;
+  plan->row_tiles = nt;
+  plan->kernel = kernel;
+  plan->num_sms = num_sms;
+  plan->ctas = static_cast<int32_t>(P * units);
+  plan->smem_bytes = smem;
+  return PA_OK;
+}
+
+size_t workspace_bytes_for(const pa_dims* d, const pa_plan& plan) {
+  const size_t rows = static_cast<size_t>(d->total_tokens) * d->num_q_heads * plan.num_partitions;
+  return kStatusBytes + align256(rows * d->head_dim * 4) + 2 * align256(rows * 4);
+}
+
+struct Workspace {
+  uint32_t* status;
+  float* po;
+  float* pm;
+  float* pl;
+};
+
+Workspace carve(void* ws, const pa_dims* d, const pa_plan& plan) {
+  const size_t rows = static_cast<size_t>(d->total_tokens) * d->num_q_heads * plan.num_partitions;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  Workspace w;
+  w.status = reinterpret_cast<uint32_t*>(base);
+  w.po = reinterpret_cast<float*>(base + kStatusBytes);
+  w.pm = reinterpret_cast<float*>(base + kStatusBytes + align256(rows * d->head_dim * 4));
+  w.pl = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(w.pm) + align256(rows * 4));
+  return w;
+}
+
+int device_sm_count(int* out) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *out = v;
+      return PA_OK;
+    }
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return PA_ERR_CUDA;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  *out = n;
+  return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// TMA descriptor over one cache: dims {D, ps, Hkv, num_blocks}, box
+// {128 bytes of a row, box_rows slots, 1 head, 1 page}, 128-byte swizzle.
+int encode_cache_map(CUtensorMap* m, const void* base, pa_dtype kv, const pa_dims* d, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PA_ERR_CUDA;
+  const int eb = dtype_bytes(kv);
+  const cuuint64_t D = d->head_dim, ps = d->page_size;
+  const cuuint64_t head_stride = (kv == PA_U8) ? ps * (D + 4) : ps * D * eb;
+  cuuint64_t dims[4] = {D, ps, static_cast<cuuint64_t>(d->num_kv_heads), static_cast<cuuint64_t>(d->num_blocks)};
+  cuuint64_t strides[3] = {D * eb, head_stride, head_stride * d->num_kv_heads};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t = kv == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                : kv == PA_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = enc(m, t, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+struct Call {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* bt;
+  const int32_t* past_lens;
+  const int32_t* begins;
+  int32_t max_ctx;
+  float scale;
+  int32_t window;
+  pa_dtype kv;
+  void* out;
+  const pa_dims* d;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+  int32_t* trace;
+};
+
+int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
+  const pa_dims* d = c.d;
+  PartArgs a;
+  a.q = c.q;
+  a.k_bytes = static_cast<const uint8_t*>(c.k);
+  a.v_bytes = static_cast<const uint8_t*>(c.v);
+  a.block_tables = c.bt;
+  a.past_lens = c.past_lens;
+  a.begins = c.begins;
+  a.out = c.out;
+  a.po = w.po;
+  a.pm = w.pm;
+  a.pl = w.pl;
+  a.status = w.status;
+  a.trace = c.trace;
+  a.num_seqs = d->num_seqs;
+  a.total_tokens = d->total_tokens;
+  a.Hq = d->num_q_heads;
+  a.Hkv = d->num_kv_heads;
+  a.G = d->num_q_heads / d->num_kv_heads;
+  a.D = d->head_dim;
+  a.ps = d->page_size;
+  a.ps_log2 = ilog2(d->page_size);
+  a.num_blocks = d->num_blocks;
+  a.max_blocks = d->max_blocks_per_seq;
+  a.max_ctx = c.max_ctx;
+  a.window = c.window;
+  a.part_tokens = plan.part_tokens;
+  a.num_parts = plan.num_partitions;
+  const int box_rows = std::min(d->page_size, plan.stage_keys);
+  a.box_log2 = ilog2(box_rows);
+  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (1 << 30);
+  a.q_dtype = d->q_dtype;
+  a.out_dtype = d->out_dtype;
+  a.scale_log2 = c.scale * 1.4426950408889634f;
+  const dim3 grid(plan.num_partitions, d->num_kv_heads, d->num_seqs);
+
+  cudaError_t e;
+  if (plan.kernel == 0) {
+    CUtensorMap mk, mv;
+    int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
+    if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
+    if (rc != PA_OK) return rc;
+    const int kind = mma_kind(c.kv);
+    if (d->head_dim == 64) e = pa::launch_mma_d64(kind, plan.row_tiles, mk, mv, a, grid, c.stream);
+    else if (d->head_dim == 128) e = pa::launch_mma_d128(kind, plan.row_tiles, mk, mv, a, grid, c.stream);
+    else e = pa::launch_mma_d256(kind, plan.row_tiles, mk, mv, a, grid, c.stream);
+  } else {
+    if (d->head_dim == 64) pa::pa_partition_f32<64><<<grid, 128, 0, c.stream>>>(a);
+    else if (d->head_dim == 128) pa::pa_partition_f32<128><<<grid, 128, 0, c.stream>>>(a);
+    else pa::pa_partition_f32<256><<<grid, 128, 0, c.stream>>>(a);
+    e = cudaGetLastError();
+  }
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
+  const pa_dims* d = c.d;
+  if (plan.num_partitions <= 1) return PA_OK;  // every sequence was written directly
+  CombineArgs a;
+  a.past_lens = c.past_lens;
+  a.begins = c.begins;
+  a.out = c.out;
+  a.po = w.po;
+  a.pm = w.pm;
+  a.pl = w.pl;
+  a.status = w.status;
+  a.num_seqs = d->num_seqs;
+  a.total_tokens = d->total_tokens;
+  a.Hq = d->num_q_heads;
+  a.Hkv = d->num_kv_heads;
+  a.G = d->num_q_heads / d->num_kv_heads;
+  a.ps = d->page_size;
+  a.max_ctx = c.max_ctx;
+  a.window = c.window;
+  a.part_tokens = plan.part_tokens;
+  a.num_parts = plan.num_partitions;
+  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (1 << 30);
+  a.out_dtype = d->out_dtype;
+  const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(rows, 4)));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (d->head_dim == 64) e = cudaLaunchKernelEx(&cfg, pa::pa_combine<64>, a);
+  else if (d->head_dim == 128) e = cudaLaunchKernelEx(&cfg, pa::pa_combine<128>, a);
+  else e = cudaLaunchKernelEx(&cfg, pa::pa_combine<256>, a);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int check_pointers(const Call& c, bool need_tensors) {
+  if (c.begins == nullptr || c.past_lens == nullptr || c.out == nullptr || c.ws == nullptr) return PA_ERR_NULL;
+  if (need_tensors && (c.q == nullptr || c.k == nullptr || c.v == nullptr || c.bt == nullptr)) return PA_ERR_NULL;
+  if (!aligned(c.out, 16) || !aligned(c.ws, 16) || !aligned(c.begins, 4) || !aligned(c.past_lens, 4))
+    return PA_ERR_ALIGN;
+  if (need_tensors && (!aligned(c.q, 16) || !aligned(c.k, 16) || !aligned(c.v, 16) || !aligned(c.bt, 4)))
+    return PA_ERR_ALIGN;
+  if (c.trace != nullptr && !aligned(c.trace, 4)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+int run(const Call& c, bool do_partition, bool do_combine) {
+  if (c.d == nullptr) return PA_ERR_NULL;
+  int sms = 0;
+  pa_plan plan;
+  int rc = make_plan(c.d, c.max_ctx, c.window, c.kv, 1, &plan);  // argument checks first
+  if (rc != PA_OK) return rc;
+  rc = check_pointers(c, do_partition);
+  if (rc != PA_OK) return rc;
+  if (c.d->total_tokens == 0) return PA_OK;
+  rc = device_sm_count(&sms);
+  if (rc != PA_OK) return rc;
+  rc = make_plan(c.d, c.max_ctx, c.window, c.kv, sms, &plan);
+  if (rc != PA_OK) return rc;
+  if (c.ws_bytes < workspace_bytes_for(c.d, plan)) return PA_ERR_WORKSPACE;
+  const Workspace w = carve(c.ws, c.d, plan);
+  if (do_partition) {
+    rc = launch_partition(c, plan, w);
+    if (rc != PA_OK) return rc;
+  }
+  if (do_combine) rc = launch_combine(c, plan, w);
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_verify_workspace_size(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window,
+                                pa_dtype kv_dtype) {
+  int sms = 0;
+  if (device_sm_count(&sms) != PA_OK) return 0;
+  pa_plan plan;
+  if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &plan) != PA_OK) return 0;
+  return workspace_bytes_for(dims, plan);
+}
+
+int pa_verify_plan(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window, pa_dtype kv_dtype,
+                   int32_t num_sms, pa_plan* plan) {
+  return make_plan(dims, max_context_len, sliding_window, kv_dtype, num_sms, plan);
+}
+
+int pa_verify_forward(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                      const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                      float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+               max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(cuda_stream), nullptr};
+  return run(c, true, true);
+}
+
+int pa_verify_forward_traced(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                             const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                             float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                             void* workspace, size_t workspace_bytes, void* cuda_stream, int32_t* gather_trace) {
+  if (gather_trace == nullptr) return PA_ERR_NULL;
+  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+               max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(cuda_stream), gather_trace};
+  return run(c, true, true);
+}
+
+int pa_verify_partition(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                        float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                        void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+               max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(cuda_stream), nullptr};
+  return run(c, true, false);
+}
+
+int pa_verify_combine(const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                      int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims, void* workspace,
+                      size_t workspace_bytes, void* cuda_stream) {
+  const Call c{nullptr, nullptr, nullptr, nullptr, past_lens, subsequence_begins, max_context_len, 1.0f,
+               sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(cuda_stream), nullptr};
+  return run(c, false, true);
+}
+
+int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits) {
+  if (workspace == nullptr || bits == nullptr) return PA_ERR_NULL;
+  if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  uint32_t host = 0;
+  if (cudaMemcpyAsync(&host, workspace, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  *bits = host;
+  return PA_OK;
+}
+
+const char* pa_verify_status_string(int code) {
+  switch (code) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_DTYPE: return "unsupported q / kv / out dtype combination";
+    case PA_ERR_SHAPE: return "invalid dimensions";
+    case PA_ERR_HEAD_DIM: return "unsupported head_dim";
+    case PA_ERR_PAGE_SIZE: return "unsupported page_size";
+    case PA_ERR_ALIGN: return "misaligned pointer";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CONTEXT: return "max_context_len out of range";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_UNSUPPORTED: return "query rows per KV head exceed the supported maximum";
+    default: return "unknown status code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+"""Host-side checks that need no GPU: the library builds and loads, exports
+every entry point include/pa_verify.h declares, the partition heuristic's
+properties, and host-detected argument errors (which return before any CUDA
+call)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import paged_attention_speculative_gb300 as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_attention_speculative_gb300 import build
+    build.build()
+    return pa.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pa_verify.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_verify_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"libpa_verify.so does not export {n}"
+    assert set(names) == set(pa.EXPORTED)
+
+
+def dims(**kw):
+    base = dict(num_seqs=1, total_tokens=4, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                num_blocks=3000, max_blocks_per_seq=2100, q_dtype=pa.PA_BF16, out_dtype=pa.PA_BF16)
+    base.update(kw)
+    return pa.PaDims(**base)
+
+
+def test_plan_fills_the_sms_once_at_long_context(lib):
+    p = pa.plan(dims(), 32772, 0, pa.PA_BF16, 152)
+    assert p.kernel == 0 and p.row_tiles == 2
+    assert p.part_tokens % max(p.stage_keys, 16) == 0
+    assert p.num_partitions * p.part_tokens >= 32772
+    assert (p.num_partitions - 1) * p.part_tokens < 32772
+    assert 0.8 * 304 <= p.ctas <= 1.1 * 304
+
+
+def test_plan_independent_of_query_count(lib):
+    """The split must not collapse when a sequence brings more than one
+    query token (the failure both OpenVINO issue 38153 and the
+    dual-radeon-vllm article describe)."""
+    ps = [pa.plan(dims(total_tokens=t), 32768 + t, 0, pa.PA_BF16, 152).num_partitions for t in (1, 2, 3, 4)]
+    assert min(ps) == max(ps) and ps[0] > 16
+
+
+def test_plan_window_reads_only_the_window(lib):
+    d = dims(num_kv_heads=16, head_dim=256, page_size=64, total_tokens=2)
+    full = pa.plan(d, 32770, 0, pa.PA_BF16, 152)
+    swa = pa.plan(d, 32770, 1024, pa.PA_BF16, 152)
+    assert swa.num_partitions * swa.part_tokens >= 1024 + 1
+    assert swa.num_partitions * swa.part_tokens <= 1024 + 2 + 2 * 64 + swa.part_tokens
+    assert full.num_partitions * full.part_tokens >= 32770
+
+
+def test_plan_bounds_partial_traffic(lib):
+    """Per-token partials (rows x (D+2) x 4 bytes per partition) stay near
+    10 % of the KV bytes a partition streams."""
+    for t, g, hkv, d in [(8, 8, 8, 128), (4, 4, 8, 128), (2, 2, 16, 256)]:
+        dd = dims(total_tokens=t, num_q_heads=g * hkv, num_kv_heads=hkv, head_dim=d)
+        p = pa.plan(dd, 8192 + t, 0, pa.PA_BF16, 152)
+        partial = t * g * (d + 2) * 4
+        kv = p.part_tokens * 2 * d * 2
+        assert partial <= 0.11 * kv
+
+
+def test_plan_scales_with_sm_count(lib):
+    d = dims(max_blocks_per_seq=8200)
+    a = pa.plan(d, 131072, 0, pa.PA_BF16, 76)
+    b = pa.plan(d, 131072, 0, pa.PA_BF16, 152)
+    assert b.num_partitions > a.num_partitions
+
+
+def test_plan_rejections(lib):
+    p = pa.PaPlan()
+    cases = [
+        (dims(head_dim=96), pa.PA_BF16, -4),
+        (dims(head_dim=64), pa.PA_U8, -4),
+        (dims(page_size=12), pa.PA_BF16, -5),
+        (dims(page_size=4), pa.PA_BF16, -5),
+        (dims(num_q_heads=30), pa.PA_BF16, -3),
+        (dims(q_dtype=pa.PA_F16), pa.PA_BF16, -2),
+        (dims(out_dtype=pa.PA_U8), pa.PA_BF16, -2),
+        (dims(num_q_heads=128, num_kv_heads=8, total_tokens=8), pa.PA_BF16, -10),
+    ]
+    for d, kv, want in cases:
+        assert lib.pa_verify_plan(ctypes.byref(d), 4096, 0, kv, 152, ctypes.byref(p)) == want
+    assert lib.pa_verify_plan(ctypes.byref(dims()), 0, 0, pa.PA_BF16, 152, ctypes.byref(p)) == -8
+    assert lib.pa_verify_plan(ctypes.byref(dims()), 2100 * 16 + 1, 0, pa.PA_BF16, 152, ctypes.byref(p)) == -8
+    assert lib.pa_verify_plan(None, 4096, 0, pa.PA_BF16, 152, ctypes.byref(p)) == -1
+
+
+def test_forward_host_errors_need_no_gpu(lib):
+    d = dims()
+    z = ctypes.c_void_p(0)
+    a16 = ctypes.c_void_p(4096)
+    args = [a16, a16, a16, a16, a16, a16, 4096, 0.1, 0, pa.PA_BF16, a16, ctypes.byref(d), a16, 1 << 20, z]
+    bad = list(args)
+    bad[0] = z
+    assert lib.pa_verify_forward(*bad) == -1
+    bad = list(args)
+    bad[0] = ctypes.c_void_p(4098)
+    assert lib.pa_verify_forward(*bad) == -6
+    bad = list(args)
+    bad[9] = pa.PA_F16
+    assert lib.pa_verify_forward(*bad) == -2
+    bad = list(args)
+    bad[11] = None
+    assert lib.pa_verify_forward(*bad) == -1
+
+
+def test_status_strings(lib):
+    for code in range(0, -11, -1):
+        s = pa.status_string(code)
+        assert s and s != "unknown status code"
+    assert pa.status_string(-99) == "unknown status code"
