@@ -1,6 +1,7 @@
 // pa_combine.cuh — per-token log-sum-exp combine of the split-KV partials.
 //
-// One warp per output row (token t, query head h).  The partials are indexed
+// One CTA per output row (token t, query head h); its warps split the
+// partitions and reduce through shared memory.  The partials are indexed
 // per query token — [t, h, partition] — so any number of new tokens per
 // sequence keeps the split (the per-sequence buffer the dual-radeon-vllm
 // article, use_3d section, identifies as the reason the split path was
@@ -15,12 +16,16 @@
 
 namespace pa {
 
+constexpr int kCombineWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128) pa_combine(const CombineArgs a) {
+__global__ void __launch_bounds__(kCombineWarps * 32) pa_combine(const CombineArgs a) {
   constexpr int PER = D / 32;
+  __shared__ float s_acc[kCombineWarps][D];
+  __shared__ float s_l[kCombineWarps];
+  __shared__ float s_m[kCombineWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * 4 + warp;
-  if (row >= static_cast<long long>(a.total_tokens) * a.Hq) return;
+  const long long row = blockIdx.x;  // one output row (token t, query head h) per CTA
   const int t = static_cast<int>(row / a.Hq);
   // sequence of token t: last b with begins[b] <= t
   int lo = 0, hi = a.num_seqs - 1;
@@ -34,53 +39,87 @@ __global__ void __launch_bounds__(128) pa_combine(const CombineArgs a) {
   pdl_wait_primary();
   if (si.err || si.T <= 0 || t < si.t0 || t >= si.t0 + si.T) {
     // malformed metadata: the partition kernel reported it; leave zeros
-    for (int e = 0; e < PER; ++e) store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + lane + 32 * e, 0.f);
+    for (int d = threadIdx.x; d < D; d += blockDim.x) store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + d, 0.f);
     return;
   }
   const int np = si.nparts;
   if (np <= 1) return;  // written directly by the partition kernel
   const float* pm = a.pm + static_cast<size_t>(row) * a.num_parts;
   const float* pl = a.pl + static_cast<size_t>(row) * a.num_parts;
-  float M = -INFINITY;
-  bool poisoned = false;
-  for (int q = lane; q < np; q += 32) {
-    M = fmaxf(M, pm[q]);
-    poisoned |= pl[q] < 0.f;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  poisoned = __any_sync(0xffffffffu, poisoned);
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  float lsum = 0.f;
-  for (int q = lane; q < np; q += 32) lsum += ex2(pm[q] - Mu) * pl[q];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-
+  const float* po = a.po + static_cast<size_t>(row) * a.num_parts * D + lane * PER;
+  // Warp w merges partitions w, w + 8, ... with its own running max; the
+  // loads of up to kBatch partitions are issued together (one round trip).
+  constexpr int kBatch = 8;
+  float Mw = -INFINITY, lw = 0.f;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  const float* po = a.po + static_cast<size_t>(row) * a.num_parts * D;
-  for (int q = 0; q < np; ++q) {
-    const float w = ex2(pm[q] - Mu);
-    const float* src = po + static_cast<size_t>(q) * D + lane * PER;
-    if constexpr (PER == 8) {
-      const float4 x0 = *reinterpret_cast<const float4*>(src);
-      const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-      acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-      acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
-    } else if constexpr (PER == 4) {
-      const float4 x0 = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-    } else {
+  bool poisoned = false;
+  for (int q0 = warp; q0 < np; q0 += kCombineWarps * kBatch) {
+    float mq[kBatch], lq[kBatch];
+    float x[kBatch][PER];
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] += w * src[e];
+    for (int j = 0; j < kBatch; ++j) {
+      const int q = q0 + kCombineWarps * j;
+      const bool ok = q < np;
+      mq[j] = ok ? pm[q] : -INFINITY;
+      lq[j] = ok ? pl[q] : 0.f;
+      const float* src = po + static_cast<size_t>(q) * D;
+#pragma unroll
+      for (int e = 0; e < PER; e += 2) {
+        const float2 v = ok ? *reinterpret_cast<const float2*>(src + e) : make_float2(0.f, 0.f);
+        x[j][e] = v.x;
+        x[j][e + 1] = v.y;
+      }
     }
-  }
-  const bool zero = poisoned || !(lsum > 0.f);
-  const float inv = zero ? 0.f : 1.f / lsum;
+    float mnew = Mw;
 #pragma unroll
-  for (int e = 0; e < PER; ++e)
-    store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + lane * PER + e, acc[e] * inv);
+    for (int j = 0; j < kBatch; ++j) {
+      mnew = fmaxf(mnew, mq[j]);
+      poisoned |= lq[j] < 0.f;
+    }
+    const float mu = (mnew == -INFINITY) ? 0.f : mnew;
+    const float alpha = ex2(Mw - mu);
+    lw *= alpha;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] *= alpha;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const float w = ex2(mq[j] - mu);
+      lw += w * lq[j];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += w * x[j][e];
+    }
+    Mw = mnew;
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) s_acc[warp][lane * PER + e] = acc[e];
+  if (lane == 0) {
+    s_l[warp] = lw;
+    s_m[warp] = Mw;
+  }
+  if (__syncthreads_or(poisoned)) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + d, 0.f);
+    return;
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, s_m[w]);
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  float wgt[kCombineWarps];
+  float lsum = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    wgt[w] = ex2(s_m[w] - Mu);
+    lsum += wgt[w] * s_l[w];
+  }
+  const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) v += wgt[w] * s_acc[w][d];
+    store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + d, v * inv);
+  }
 }
 
 }  // namespace pa

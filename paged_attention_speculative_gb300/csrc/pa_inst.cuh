@@ -8,7 +8,7 @@ namespace pa {
 
 template <int D, int KV, int NT>
 MmaKernelInfo mma_info_t() {
-  return MmaKernelInfo{MmaCfg<D, KV>::SK, MmaSmem<D, KV, NT>::BYTES};
+  return MmaKernelInfo{MmaCfg<D, KV>::SK, MmaSmem<D, KV, NT>::BYTES, MmaSmem<D, KV, NT>::CTAS_PER_SM};
 }
 
 template <int D, int KV, int NT>

@@ -11,7 +11,7 @@ MmaKernelInfo mma_info_d128(int kv, int nt, bool* ok) {
   PA_DISPATCH_CASE(128, KV_F16, 2)
   PA_DISPATCH_CASE(128, KV_U8, 1)
   PA_DISPATCH_CASE(128, KV_U8, 2)
-  return MmaKernelInfo{0, 0};
+  return MmaKernelInfo{0, 0, 0};
 }
 
 cudaError_t launch_mma_d128(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,

@@ -9,7 +9,7 @@ MmaKernelInfo mma_info_d256(int kv, int nt, bool* ok) {
   PA_DISPATCH_CASE(256, KV_BF16, 1)
   PA_DISPATCH_CASE(256, KV_F16, 1)
   PA_DISPATCH_CASE(256, KV_U8, 1)
-  return MmaKernelInfo{0, 0};
+  return MmaKernelInfo{0, 0, 0};
 }
 
 cudaError_t launch_mma_d256(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,

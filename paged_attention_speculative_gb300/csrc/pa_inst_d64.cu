@@ -9,7 +9,7 @@ MmaKernelInfo mma_info_d64(int kv, int nt, bool* ok) {
   PA_DISPATCH_CASE(64, KV_BF16, 2)
   PA_DISPATCH_CASE(64, KV_F16, 1)
   PA_DISPATCH_CASE(64, KV_F16, 2)
-  return MmaKernelInfo{0, 0};
+  return MmaKernelInfo{0, 0, 0};
 }
 
 cudaError_t launch_mma_d64(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,

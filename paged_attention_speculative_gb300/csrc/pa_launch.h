@@ -13,6 +13,7 @@ namespace pa {
 struct MmaKernelInfo {
   int stage_keys;   // keys per pipeline stage
   int smem_bytes;   // dynamic shared memory
+  int ctas_per_sm;  // resident CTAs per SM the launch bounds allow
 };
 
 // Per head dim: info and launch of pa_partition_mma<D, kv, nt>.  kv is a

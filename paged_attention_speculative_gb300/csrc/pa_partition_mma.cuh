@@ -42,7 +42,9 @@ struct MmaCfg {
   static constexpr int SK = (ROW_BYTES >= 512) ? 32 : 64;  // keys per pipeline stage
   static constexpr int TILE = SK * ROW_BYTES;          // bytes of one K (or V) stage tile
   static constexpr int SZ = kU8 ? SK * 2 : 0;          // one fp16 scale (or zp) array
-  static constexpr int STAGE = 2 * TILE + 4 * SZ;
+  // stages start on 1024-byte boundaries: the 128-byte swizzle pattern is a
+  // function of the shared-memory address bits 7..9
+  static constexpr int STAGE = ((2 * TILE + 4 * SZ) + 1023) / 1024 * 1024;
   static constexpr int NS = (STAGE <= 20 * 1024) ? 5 : 3;  // stages in flight
   static constexpr int KSTEPS = D / 16;
   static constexpr int MTILES = D / 16;
@@ -54,6 +56,7 @@ template <int D, int KV, int NT>
 struct MmaSmem {
   using C = MmaCfg<D, KV>;
   static constexpr int RPW = 8 * NT;                   // rows per consumer warp
+  static constexpr int CTAS_PER_SM = (NT == 2) ? 1 : 2;  // register budget of the launch bounds
   static constexpr int MERGE_LD = D + 4;
   static constexpr int MERGE_BYTES = kConsumerWarps * RPW * (MERGE_LD + 2) * 4;
   static_assert(MERGE_BYTES <= C::NS * C::STAGE, "merge area must fit in the stage ring");
@@ -70,7 +73,7 @@ __device__ __forceinline__ int out_dim(int mt, int m) {
 }
 
 template <int D, int KV, int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     pa_partition_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const PartArgs a) {
   using C = MmaCfg<D, KV>;
@@ -84,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + C::NS;
   int32_t* blk = reinterpret_cast<int32_t*>(smem + S::BLK_OFF);
   __shared__ int s_timeout;
+  __shared__ int s_bad;
 
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -114,40 +118,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     s_timeout = 0;
+    s_bad = 0;
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
     fence_barrier_init();
   }
-  int bad = 0;
-  for (int j = threadIdx.x; j < npages; j += kThreads) {
-    int id = __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
-    if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
-      bad = 1;
-      id = 0;
-    }
-    blk[j] = id;
-  }
-  if (__syncthreads_or(bad)) {
-    // A corrupt block table: report, and make this partition's contribution
-    // poison the rows (the combine, or the direct write below, zeroes them).
-    if (threadIdx.x == 0) atomicOr(a.status, PA_STATUS_BLOCK_ID);
-    for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
-      const int r = idx / D, d = idx % D;
-      const size_t row = static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G;
-      if (si.nparts == 1) {
-        store_out(a.out, a.out_dtype, row * D + d, 0.f);
-      } else if (d == 0) {
-        a.pm[row * a.num_parts + p] = 0.f;
-        a.pl[row * a.num_parts + p] = -1.f;
-      }
-    }
-    return;
-  }
+  __syncthreads();  // barriers ready; no global loads are in front of this
 
   // =========================== producer warp ===============================
   if (warp == kConsumerWarps) {
+    // Stage this partition's block ids in one coalesced pass and validate
+    // them.  A bad id is reported, clamped to page 0 (so every copy stays in
+    // bounds) and the partition's result is discarded after the loop.
+    int bad = 0;
+    for (int j = lane; j < npages; j += 32) {
+      int id = __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+      if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+        bad = 1;
+        id = 0;
+      }
+      blk[j] = id;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+      s_bad = 1;  // published to the consumers by the first full-barrier arrive
+      atomicOr(a.status, PA_STATUS_BLOCK_ID);
+    }
+    __syncwarp();
     const int br_log2 = a.box_log2;
     const int br = 1 << br_log2;
     int issued = 0;
@@ -302,7 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t kt = smem_u32(st), vt = kt + C::TILE;
     const int key0 = kstart + s * C::SK;
     if (nt_active > 0) {
-      for (int c = ks; c < C::CHUNKS_PER_STAGE; c += KS) {
+      // chunks are dealt round-robin over the key-split warps across stages,
+      // so short stages (two chunks) still keep every warp busy
+      const int c0 = (ks - (s * C::CHUNKS_PER_STAGE) % KS + KS) % KS;
+      for (int c = c0; c < C::CHUNKS_PER_STAGE; c += KS) {
         const int ck0 = key0 + 16 * c;
         if (ck0 >= kend) break;
         const int kg0 = ck0 + key_perm(g8);  // keys of accumulator rows g8 and g8 + 8
@@ -520,6 +521,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // =========================== merge & write ===============================
   consumer_sync();  // every consumer is done with the stage ring
+  if (s_bad) {
+    // corrupt block table: poison this partition (the combine zeroes the rows)
+    for (int idx = threadIdx.x; idx < R * D; idx += kConsumerWarps * 32) {
+      const int r = idx / D, d = idx % D;
+      const size_t row = static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G;
+      if (si.nparts == 1) {
+        store_out(a.out, a.out_dtype, row * D + d, 0.f);
+      } else if (d == 0) {
+        a.pm[row * a.num_parts + p] = 0.f;
+        a.pl[row * a.num_parts + p] = -1.f;
+      }
+    }
+    return;
+  }
   float* mo = reinterpret_cast<float*>(smem);
   float* mm = mo + kConsumerWarps * RPW * S::MERGE_LD;
   float* ml = mm + kConsumerWarps * RPW;

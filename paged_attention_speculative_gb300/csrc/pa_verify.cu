@@ -59,7 +59,7 @@ pa::MmaKernelInfo mma_info(int D, int kind, int nt, bool* ok) {
   if (D == 128) return pa::mma_info_d128(kind, nt, ok);
   if (D == 256) return pa::mma_info_d256(kind, nt, ok);
   *ok = false;
-  return pa::MmaKernelInfo{0, 0};
+  return pa::MmaKernelInfo{0, 0, 0};
 }
 
 // Argument checks shared by every entry point; fills the plan.
@@ -92,7 +92,9 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   int kernel = (kv == PA_F32) ? 1 : 0;
   int nt = 0, sk = 64, smem = 0, ctas_per_sm = 4;
   if (kernel == 0) {
-    nt = (D == 256 || rows <= 8) ? 1 : 2;
+    // one 8-row n-tile per warp keeps a warp's accumulators within the
+    // register budget of two CTAs per SM; rows beyond 8 go to more warps
+    nt = (D == 256 || rows <= 32) ? 1 : 2;
     const int cap = pa::kConsumerWarps * 8 * nt;
     if (rows > cap) return PA_ERR_UNSUPPORTED;
     bool ok = false;
@@ -100,7 +102,7 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
     if (!ok) return PA_ERR_UNSUPPORTED;
     sk = info.stage_keys;
     smem = info.smem_bytes;
-    ctas_per_sm = 2;
+    ctas_per_sm = info.ctas_per_sm;
   }
   const long long quantum = std::max(sk, ps);
   const long long ctx = std::max<long long>(max_ctx, 1);
@@ -110,7 +112,7 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const long long target = static_cast<long long>(num_sms) * ctas_per_sm;
   long long part = ceil_div(span * units, target);
   const long long min_part = ceil_div(10LL * rows * (D + 2) * 4, per_key);
-  part = std::max(part, min_part);
+  part = std::max(part, std::max<long long>(min_part, 2LL * sk));
   if (env_part_tokens() > 0) part = env_part_tokens();
   part = round_up(std::max<long long>(part, 1), quantum);
   part = std::min(part, round_up(span, quantum));
@@ -304,8 +306,8 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.out_dtype = d->out_dtype;
   const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(rows, 4)));
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(pa::kCombineWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];

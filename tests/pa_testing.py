@@ -78,6 +78,40 @@ def run_oracle(case: W.Case, nthreads: int = 0):
                           nthreads=nthreads)
 
 
+UNIT_ROUNDOFF = {"f32": 2.0 ** -24, "f16": 2.0 ** -11, "bf16": 2.0 ** -8, "u8": 2.0 ** -11}
+
+
+def derived_tolerance(case: W.Case, want, out_dtype=None):
+    """Per-element bound for short contexts, where outputs are O(1):
+    2e-3 + u_P * sum_j p_j |v_j| / sum_j p_j + u_out * |ref|.
+    u_P is the unit roundoff of the softmax weights as the tensor cores consume
+    them (the V operand type: bf16 for bf16 caches, f16 for f16 and u8 caches),
+    u_out that of the output dtype.  Rounding every weight by at most u_P moves
+    the weighted mean by at most u_P * sum p |v| / l; rounding the result moves
+    it by at most u_out * |ref|."""
+    import test_oracle_pins as P
+    kc, vc = P._decode_cache(case)
+    q = W.storage_to_f64(case.q, case.q_dtype).reshape(case.total_tokens, case.num_q_heads, case.head_dim)
+    G = case.num_q_heads // case.num_kv_heads
+    spread = np.zeros_like(want)
+    for b in range(case.num_seqs):
+        L, t0 = int(case.past_lens[b]), int(case.subsequence_begins[b])
+        for i in range(int(case.query_lens[b])):
+            p = L + i
+            lo = max(0, p - case.sliding_window + 1) if case.sliding_window > 0 else 0
+            js = np.arange(lo, p + 1)
+            blk = case.block_tables[b][js // case.page_size]
+            for h in range(case.num_q_heads):
+                K = kc[blk, h // G, js % case.page_size]
+                V = vc[blk, h // G, js % case.page_size]
+                s = case.scale * (K @ q[t0 + i, h])
+                w = np.exp(s - s.max())
+                spread[t0 + i, h] = (w @ np.abs(V)) / w.sum()
+    u_p = UNIT_ROUNDOFF[case.kv_dtype]
+    u_o = UNIT_ROUNDOFF[out_dtype or case.out_dtype]
+    return 2e-3 + u_p * spread + u_o * np.abs(want)
+
+
 def max_abs_err(got, want):
     assert got.shape == want.shape
     assert np.isfinite(got).all(), f"{np.count_nonzero(~np.isfinite(got))} non-finite outputs"

@@ -10,17 +10,25 @@ import pytest
 
 from paged_attention_speculative_gb300 import workloads as W
 
-from pa_testing import TOL, max_abs_err, run_gpu, run_oracle, to_device
+from pa_testing import TOL, derived_tolerance, max_abs_err, run_gpu, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
 
 def _check(case, out_dtype=None, tol=TOL):
+    """tol: the flat 2e-3 bound for the pages' long-context workloads, or
+    "derived" (see pa_testing.derived_tolerance) for short-context edge cases
+    whose outputs are O(1), where one bf16 rounding alone exceeds 2e-3."""
     got, bits, trace = run_gpu(case, out_dtype=out_dtype, traced=True)
     assert bits == 0, f"device status {bits:#x}"
     want = run_oracle(case)
     err = max_abs_err(got, want)
-    assert err <= tol, f"{case.name}: max abs err {err:.3e}"
+    if isinstance(tol, str):
+        bound = derived_tolerance(case, want, out_dtype)
+        worst = float(np.max(np.abs(got - want) - bound))
+        assert worst <= 0.0, f"{case.name}: error exceeds the derived bound by {worst:.3e} (max abs {err:.3e})"
+    else:
+        assert err <= tol, f"{case.name}: max abs err {err:.3e}"
     import oracle
     pages = oracle.pages_touched(case.block_tables, case.past_lens, case.subsequence_begins,
                                  page_size=case.page_size, sliding_window=case.sliding_window)
@@ -28,6 +36,8 @@ def _check(case, out_dtype=None, tol=TOL):
         assert np.array_equal(trace[:, g, :], pages), f"{case.name}: gather trace of KV head {g} differs"
     return err
 
+
+EDGE = {"batch_edge", "window1", "f32_win_batch"}
 
 SMALL = [
     lambda: W.tiny(),
@@ -54,6 +64,10 @@ SMALL = [
     lambda: W.make_case("f32_win_batch", seed=16, query_lens=[2, 3], past_lens=[150, 40], num_q_heads=4,
                         num_kv_heads=2, head_dim=128, page_size=16, q_dtype="f32", kv_dtype="f32",
                         sliding_window=33),
+    lambda: W.make_case("d256_rows16", seed=18, query_lens=[8], past_lens=[1500], num_q_heads=32, num_kv_heads=16,
+                        head_dim=256, page_size=64),
+    lambda: W.make_case("rows32_u8", seed=19, query_lens=[8], past_lens=[2500], num_q_heads=32, num_kv_heads=8,
+                        head_dim=128, page_size=16, kv_dtype="u8"),
     lambda: W.make_case("window1", seed=17, query_lens=[4], past_lens=[200], num_q_heads=8, num_kv_heads=2,
                         head_dim=128, page_size=16, sliding_window=1),
 ]
@@ -61,7 +75,8 @@ SMALL = [
 
 @pytest.mark.parametrize("idx", range(len(SMALL)))
 def test_parity_reduced(idx):
-    _check(SMALL[idx]())
+    case = SMALL[idx]()
+    _check(case, tol="derived" if case.name in EDGE else TOL)
 
 
 @pytest.mark.parametrize("out_dtype", ["f32", "f16"])
