@@ -165,6 +165,24 @@ class DeviceWorkload:
         return 1 + (1 if self.plan().num_partitions > 1 else 0)
 
 
+def reduce_max_over_ranks(x: float, device="cpu") -> float:
+    """Max of a per-rank float over the process group (identity when not
+    distributed): the timed interval of the slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: int, world: int, max_us_per_step: float) -> float:
+    """Whole-job throughput: every rank streams its own replica's bytes each
+    step; the job's step time is the slowest rank's."""
+    return world * bytes_per_rank_step / (max_us_per_step * 1e-6) / 1e9
+
+
 def l2_bytes():
     import torch
     return int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20))
@@ -214,35 +232,42 @@ def time_graph(wl, steps, warmup, stream, min_seconds=0.0):
 
 
 def time_partition_kernel(wl, steps, stream):
-    """Average device duration of the partition kernel alone (events on the
-    launching stream around each launch; the combine runs between them)."""
+    """Average device duration of the partition kernel: a CUDA graph of
+    `steps` back-to-back partition launches (rotating replicas), replayed
+    between two events on the launching stream.  Returns (mean, median) µs
+    over trials."""
     import torch
-    evs = []
+    reps = max(1, min(steps, 64))
+    g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        for s in range(3):
-            wl.partition(s % wl.replicas, stream)
-            wl.combine(stream)
-        torch.cuda.synchronize()
-        for s in range(steps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            wl.partition(s % wl.replicas, stream)
-            b.record(stream)
-            wl.combine(stream)
-            evs.append((a, b))
-        torch.cuda.synchronize()
-    ts = [a.elapsed_time(b) * 1e3 for a, b in evs]
-    return statistics.mean(ts), statistics.median(ts)
+        for r in range(min(wl.replicas, reps)):
+            wl.partition(r % wl.replicas, stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                wl.partition(r % wl.replicas, stream)
+        res = []
+        for _ in range(max(5, steps // reps)):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            res.append(e0.elapsed_time(e1) * 1e3 / reps)
+    return statistics.mean(res), statistics.median(res)
 
 
-def time_e2e(wl, steps, warmup, stream):
+def time_e2e(wl, steps, warmup, stream, graph=True):
     """Through the public API with host buffers: every step copies its query
     tokens, block table, past_lens and subsequence_begins from pinned host
-    memory, runs the verify step, and reads the output back to pinned host
-    memory.  The KV cache is resident device state (the cache of a serving
-    engine), as it is between verify steps."""
+    memory, runs the verify step, and copies the output back to pinned host
+    memory, all inside the timed region.  The KV cache is resident device
+    state (the cache of a serving engine), as it is between verify steps.
+    graph=True captures the per-step sequence (copies + launches) in a CUDA
+    graph, as a serving loop would; graph=False issues it eagerly."""
     import torch
+    import paged_attention_speculative_gb300 as pa
     q_h = wl.q.cpu().pin_memory()
     pl_h = wl.past_lens.cpu().pin_memory()
     sb_h = wl.begins.cpu().pin_memory()
@@ -255,7 +280,6 @@ def time_e2e(wl, steps, warmup, stream):
         bt_d.copy_(bt_h[s % wl.replicas], non_blocking=True)
         wl.past_lens.copy_(pl_h, non_blocking=True)
         wl.begins.copy_(sb_h, non_blocking=True)
-        import paged_attention_speculative_gb300 as pa
         pa.forward(wl.q, wl.k, wl.v, bt_d, wl.past_lens, wl.begins, wl.max_ctx, wl.scale, wl.window, wl.kv_code,
                    wl.out, wl.dims, wl.ws, stream=stream)
         out_h.copy_(wl.out, non_blocking=True)
@@ -264,14 +288,33 @@ def time_e2e(wl, steps, warmup, stream):
         for s in range(warmup):
             step(s)
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for s in range(steps):
-            step(s)
-        e1.record(stream)
-        e1.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / steps
+        if graph:
+            reps = max(1, min(steps, 32))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(reps):
+                    step(s)
+            g.replay()
+            torch.cuda.synchronize()
+            n = max(1, steps // reps)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            done = n * reps
+        else:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for s in range(steps):
+                step(s)
+            e1.record(stream)
+            e1.synchronize()
+            done = steps
+    us = e0.elapsed_time(e1) * 1e3 / done
     h2d = wl.q.numel() * wl.q.element_size() + bt_d.numel() * 4 + wl.past_lens.numel() * 4 + wl.begins.numel() * 4
     d2h = wl.out.numel() * wl.out.element_size()
     return us, h2d, d2h
@@ -471,16 +514,14 @@ def run_ours(args, rank, world):
     clk = clocks.stop()
     torch.cuda.synchronize()
     if dist is not None:
-        t = torch.tensor([us], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us = float(t.item())
+        us = reduce_max_over_ranks(us, device="cuda")
         dist.barrier()
-    step_s = us * 1e-6
-    value = world * wl.kv_bytes / step_s / 1e9
+    value = whole_job_gbs(wl.kv_bytes, world, us)
 
     part_mean, part_med = time_partition_kernel(wl, max(args.steps, 20), stream)
     achieved = wl.kv_bytes / (part_mean * 1e-6) / 1e9
-    e2e_us, h2d, d2h = time_e2e(wl, max(args.steps, 20), args.warmup, stream)
+    e2e_us, h2d, d2h = time_e2e(wl, max(args.steps, 20), args.warmup, stream, graph=True)
+    e2e_eager_us, _, _ = time_e2e(wl, max(args.steps, 20), args.warmup, stream, graph=False)
     e2e_value = world * wl.kv_bytes / (e2e_us * 1e-6) / 1e9
 
     # T=1 at the same context (the ratio the pages' fix is about)
@@ -551,11 +592,14 @@ def run_ours(args, rank, world):
                          f" MiB > 2x L2)", "launch": "CUDA graph replay", "trials": len(trials)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": measured_traffic(H["name"]),
-                     "kernel": "pa_partition_mma<128, bf16, 2>", "kernel_us_mean": part_mean,
+                     "kernel": f"pa_partition_mma<D=128, bf16, n-tiles={wl.plan().row_tiles}>",
+                     "kernel_us_mean": part_mean, "kernel_timing": "CUDA graph of back-to-back partition launches",
                      "kernel_us_median": part_med, "algorithmic_bytes_per_launch": wl.kv_bytes,
                      "peak_kind": f"{peak_kind} copy rate (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "us_per_step": e2e_us, "launch": "eager"},
+                "us_per_step": e2e_us, "launch": "CUDA graph of H2D copies + forward + D2H copy per step",
+                "eager_us_per_step": e2e_eager_us,
+                "eager_value": world * wl.kv_bytes / (e2e_eager_us * 1e-6) / 1e9},
         "cpu_baseline": cpu,
         "clocks": clk,
         "gpu_launches": exact * wl.launches_per_step(),
