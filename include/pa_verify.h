@@ -177,6 +177,34 @@ int pa_verify_combine(const int32_t* past_lens, const int32_t* subsequence_begin
                       void* out, const pa_dims* dims, void* workspace, size_t workspace_bytes,
                       void* cuda_stream);
 
+/* pa_verify_forward for callers that cannot allocate device memory.  The
+ * pages have no counterpart of this entry point; it exists for hosts that
+ * cannot hand the library a workspace: for example a C-only host whose GPU
+ * memory is already reserved by another runtime's pool and that has no
+ * allocator to call, or a serving loop that must not call cudaMalloc once it
+ * runs (cudaMalloc can synchronise the device and is not allowed while a
+ * stream is being captured).
+ *
+ * Same arguments and results as pa_verify_forward, minus the workspace: the
+ * split-KV partials live in a 16 MiB device array inside the library (held
+ * by every GPU that loads the library until the process exits).  A call
+ * whose partials need more than that (total_tokens x Hq x partitions x
+ * (4*head_dim + 8) bytes, plus 256) returns PA_ERR_WORKSPACE and launches
+ * nothing; nothing is allocated, on any path.
+ *
+ * The first call on each device resolves the array's device address for
+ * that device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call shares the one array: calls that can overlap on the
+ * GPU (different streams without ordering between them) race on it and give
+ * undefined results.  Device-detected input errors still leave the affected
+ * rows zero; their status bits are cleared at the start of each call and
+ * are not reported by this entry point. */
+int pa_verify_forward_no_alloc(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* past_lens,
+                               const int32_t* subsequence_begins, int32_t max_context_len,
+                               float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out,
+                               const pa_dims* dims, void* cuda_stream);
+
 /* Synchronises cuda_stream, then reads and clears the workspace's status word
  * into *bits (PA_STATUS_* flags, 0 = clean). */
 int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits);

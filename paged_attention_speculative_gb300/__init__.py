@@ -26,7 +26,8 @@ PA_MAX_QUERY_LEN = 8
 STATUS_BITS = {0x1: "QUERY_LEN", 0x2: "CONTEXT", 0x4: "BLOCK_ID", 0x8: "BEGINS", 0x10: "PAST_LEN",
                0x20: "ROWS", 0x40: "TIMEOUT"}
 EXPORTED = ["pa_verify_workspace_size", "pa_verify_plan", "pa_verify_forward", "pa_verify_forward_traced",
-            "pa_verify_partition", "pa_verify_combine", "pa_verify_get_device_status", "pa_verify_status_string"]
+            "pa_verify_partition", "pa_verify_combine", "pa_verify_get_device_status", "pa_verify_status_string",
+            "pa_verify_forward_no_alloc"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -88,6 +89,8 @@ def load_library():
         lib.pa_verify_combine.restype = ctypes.c_int
         lib.pa_verify_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.pa_verify_get_device_status.restype = ctypes.c_int
+        lib.pa_verify_forward_no_alloc.argtypes = fwd[:12] + [vp]
+        lib.pa_verify_forward_no_alloc.restype = ctypes.c_int
         lib.pa_verify_status_string.argtypes = [ctypes.c_int]
         lib.pa_verify_status_string.restype = ctypes.c_char_p
         _lib = lib

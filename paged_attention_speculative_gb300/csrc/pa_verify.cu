@@ -356,6 +356,32 @@ int run(const Call& c, bool do_partition, bool do_combine) {
   return rc;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch for pa_verify_forward_no_alloc: a fixed device array that the
+// library owns, so the caller needs no allocator.  Every GPU that loads the
+// library holds these 16 MiB until the process exits.  All calls share it.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_no_alloc_scratch on the current device, resolved once
+// per device with that device current.  In host code the array's name is
+// only a host-side stand-in; kernels must be given this address instead.
+int no_alloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -412,6 +438,27 @@ int pa_verify_combine(const int32_t* past_lens, const int32_t* subsequence_begin
                sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
                static_cast<cudaStream_t>(cuda_stream), nullptr};
   return run(c, false, true);
+}
+
+int pa_verify_forward_no_alloc(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* past_lens,
+                               const int32_t* subsequence_begins, int32_t max_context_len, float scale,
+                               int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                               void* cuda_stream) {
+  if (dims == nullptr) return PA_ERR_NULL;
+  void* scratch = nullptr;
+  int rc = no_alloc_scratch(&scratch);
+  if (rc != PA_OK) return rc;
+  // The status word is the only part of the scratch that must start at zero
+  // (the partials are written before they are read).  Clear it on the stream
+  // so calls ordered on one stream see a clean word.
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (dims->total_tokens > 0 && cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+               max_context_len, scale, sliding_window, kv_dtype, out, dims, scratch, kNoAllocScratchBytes,
+               st, nullptr};
+  return run(c, true, true);  // PA_ERR_WORKSPACE when the call needs more than the scratch holds
 }
 
 int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits) {
