@@ -103,7 +103,8 @@ typedef struct {
   int32_t part_tokens;     /* keys per partition (multiple of the stage size)     */
   int32_t stage_keys;      /* keys staged per pipeline step                       */
   int32_t row_tiles;       /* n-tiles of 8 query rows per warp (1 or 2)           */
-  int32_t kernel;          /* 0 = tensor-core path (16-bit / u8 KV), 1 = fp32 path */
+  int32_t kernel;          /* 0 = warp-level mma path (16-bit / u8 KV), 1 = fp32 path,
+                              2 = tensor-memory (tcgen05) path (16-bit KV, > 32 rows) */
   int32_t num_sms;         /* SM count the plan was made for                       */
   int32_t ctas;            /* grid size B * Hkv * P                                */
   int32_t smem_bytes;      /* dynamic shared memory per partition CTA             */

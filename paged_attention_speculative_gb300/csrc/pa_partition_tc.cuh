@@ -1,0 +1,453 @@
+// pa_partition_tc.cuh — split-KV partition kernel on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory), for 16-bit KV caches and
+// up to 64 query rows per KV head (T_b x G, e.g. 8 verify tokens x 8 GQA
+// heads), where the QK^T / PV contractions outgrow warp-level mma.
+//
+// Same contract as pa_partition_mma: one CTA per (partition, KV head,
+// sequence); every page of the partition is read once for all rows; per-token
+// partials (or the final output when one partition covers the sequence).
+//
+// Warp roles (128 threads):
+//   warps 0, 1  softmax: thread r owns query row r (TMEM lane r)
+//   warp 2      MMA issuer (one thread)
+//   warp 3      TMA producer (block-table lookup + tile loads, as in the mma path)
+// Per 64-key stage s:
+//   S(s)  = Q . K_s^T          tcgen05.mma M=128 (rows 0..63 real), N=64, K=D   -> TMEM
+//   P(s)  = 2^(S*scale*log2e - m)  (softmax warps, bf16/f16, 128-byte-swizzled smem)
+//   O    += P(s) . V_s          tcgen05.mma M=128, N=D, K=64, V as MN-major B     -> TMEM
+// S(s+1) is issued before PV(s) so the tensor cores work while the softmax
+// runs.  The running max is kept lazily: O is rescaled (TMEM load/store) only
+// when a row's max grows by more than 2^8, otherwise weights are taken
+// relative to the stale max (they stay <= 256, exact enough in 16 bits).
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// tcgen05 / tensor-memory wrappers (PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] . B[smem desc], kind::f16 (f16 or bf16 in, f32 acc).
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on `bar` when every tcgen05 operation this thread issued so far completes.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Thread i of the warp reads 32 consecutive 32-bit columns of TMEM lane
+// (lane base + i); the wait is in the same statement so no use of the
+// registers can be scheduled before the data arrive.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
+// start address, leading / stride byte offsets (16-byte units), version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with f32 accumulation.
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, bool bf16, bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <int D, int KV>
+struct TcCfg {
+  static_assert(KV == KV_BF16 || KV == KV_F16, "tensor-memory path takes 16-bit caches");
+  static_assert(D == 64 || D == 128, "tensor-memory path: head_dim 64 or 128");
+  static constexpr bool kBf16 = (KV == KV_BF16);
+  static constexpr int ROWS = 64;                 // real query rows (TMEM lanes 0..63)
+  static constexpr int M = 128;                   // MMA rows (64..127 are zero padding)
+  static constexpr int SK = 64;                   // keys per stage (= N of the score MMA)
+  static constexpr int CH = D / 64;               // 128-byte chunks per key row
+  static constexpr int TILE = SK * D * 2;         // one K (or V) stage tile
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int Q_BYTES = CH * M * 128;    // [chunk][row][128 B]
+  static constexpr int P_BYTES = M * 128;         // [row][64 keys x 2 B]
+  static constexpr int FIXED = Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + 256 + 1024;
+  static constexpr int NS = ((220 * 1024 - FIXED) / STAGE) > 8 ? 8 : ((220 * 1024 - FIXED) / STAGE);
+  static constexpr int Q_OFF = NS * STAGE;
+  static constexpr int P_OFF = Q_OFF + Q_BYTES;
+  static constexpr int BLK_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int BAR_OFF = BLK_OFF + 4 * kMaxPagesPerCta;
+  static constexpr int BYTES = BAR_OFF + 256 + 1024;
+  static constexpr int TMEM_COLS = 256;           // O: D columns, S: 2 x 64 columns
+  static constexpr uint32_t IDESC_S = tc_idesc(M, SK, kBf16, false);
+  static constexpr uint32_t IDESC_PV = tc_idesc(M, D, kBf16, true);
+  static_assert(NS >= 2, "pipeline needs two stages");
+};
+
+template <int D, int KV>
+__global__ void __launch_bounds__(128, 1)
+    pa_partition_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const PartArgs a) {
+  using C = TcCfg<D, KV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = smem + C::Q_OFF;
+  uint8_t* ps = smem + C::P_OFF;
+  int32_t* blk = reinterpret_cast<int32_t*>(smem + C::BLK_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* full = bars;                 // [NS] TMA landed
+  uint64_t* empty = full + C::NS;        // [NS] stage consumed (MMA commit after PV)
+  uint64_t* s_full = empty + C::NS;      // [2] S buffer written (MMA commit)
+  uint64_t* s_free = s_full + 2;         // [2] S buffer read (2 softmax warps)
+  uint64_t* p_full = s_free + 2;         // [2] P buffer written (2 softmax warps)
+  uint64_t* pv_done = p_full + 2;        // [2] PV of the stage using that P buffer done (MMA commit)
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_bad, s_timeout;
+
+  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
+                              a.part_tokens, a.row_cap);
+  pdl_launch_dependents();
+  if (si.err) {
+    if (p == 0 && threadIdx.x == 0) atomicOr(a.status, si.err);
+    if (p == 0 && si.rows_ok) {
+      const int n = si.T * a.G * D;
+      for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        store_out(a.out, a.out_dtype, (static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G) * D + d,
+                  0.f);
+      }
+    }
+    return;
+  }
+  if (si.T <= 0 || p >= si.nparts) return;
+
+  const int kstart = si.kbase + p * a.part_tokens;
+  const int kend = min(kstart + a.part_tokens, si.khi + 1);
+  const int lp0 = kstart >> a.ps_log2;
+  const int npages = ((kend - 1) >> a.ps_log2) - lp0 + 1;
+  const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
+  const int R = si.T * a.G;
+
+  // ---- set-up: barriers, tensor memory, Q tile, zero padding of P ----
+  if (threadIdx.x == 0) {
+    s_bad = 0;
+    s_timeout = 0;
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 2);
+      mbar_init(&p_full[i], 2);
+      mbar_init(&pv_done[i], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  // Q rows (query row r = token r/G, head g*G + r%G) into [chunk][row][128 B],
+  // 128-byte swizzled; rows R..127 zero.
+  for (int u = threadIdx.x; u < C::M * C::CH * 8; u += blockDim.x) {
+    const int r = u / (C::CH * 8), rem = u % (C::CH * 8), c = rem >> 3, unit = rem & 7;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < R) {
+      const size_t row = static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G;
+      v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + row * D) + c * 8 + unit);
+    }
+    *reinterpret_cast<uint4*>(qs + (c * C::M + r) * 128 + swz(unit, r)) = v;
+  }
+  // P rows 64..127 are padding: zero them once in both buffers.
+  for (int u = threadIdx.x; u < 2 * (C::M - C::ROWS) * 8; u += blockDim.x) {
+    const int buf = u / ((C::M - C::ROWS) * 8), rem = u % ((C::M - C::ROWS) * 8);
+    *reinterpret_cast<uint4*>(ps + buf * C::P_BYTES + (C::ROWS + (rem >> 3)) * 128 + 16 * (rem & 7)) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async();  // generic smem writes -> visible to the tensor cores
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t tm_o = tmem;                      // O: columns [0, D)
+  const uint32_t tm_s0 = tmem + D;                 // S buffers: [D, D + 64), [D + 64, D + 128)
+
+  if (warp == 3) {
+    // =========================== TMA producer ===============================
+    int bad = 0;
+    for (int j = lane; j < npages; j += 32) {
+      int id = __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+      if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+        bad = 1;
+        id = 0;
+      }
+      blk[j] = id;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+      s_bad = 1;
+      atomicOr(a.status, PA_STATUS_BLOCK_ID);
+    }
+    __syncwarp();
+    const int br_log2 = a.box_log2, br = 1 << br_log2;
+    for (int s = 0; s < n_stages; ++s) {
+      const int slot = s % C::NS;
+      if (s >= C::NS && !mbar_wait(&empty[slot], ((s / C::NS) - 1) & 1)) {
+        if (lane == 0) {
+          atomicOr(a.status, PA_STATUS_TIMEOUT);
+          atomicOr(&s_timeout, 1);
+        }
+        break;
+      }
+      const int key0 = kstart + s * C::SK;
+      const int nk = min(C::SK, kend - key0);
+      const int nseg = (nk + br - 1) >> br_log2;
+      uint8_t* st = smem + slot * C::STAGE;
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nseg * br * D * 2 * 2));
+      __syncwarp();
+      for (int j = lane; j < nseg * C::CH; j += 32) {
+        const int seg = j / C::CH, c = j % C::CH;
+        const int key = key0 + (seg << br_log2);
+        const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+        const int id = blk[lp - lp0];
+        // tile layout [chunk][key][128 B]: rows of one chunk are contiguous
+        const uint32_t off = static_cast<uint32_t>((c * C::SK + (seg << br_log2)) * 128);
+        tma_load_4d(st + off, &tmK, c * 64, slot0, g, id, &full[slot]);
+        tma_load_4d(st + C::TILE + off, &tmV, c * 64, slot0, g, id, &full[slot]);
+        if (a.trace != nullptr && c == 0 && slot0 == 0)
+          atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
+      }
+    }
+  } else if (warp == 2) {
+    // =========================== MMA issuer =================================
+    if (lane == 0) {
+      const uint32_t q_base = smem_u32(qs), p_base = smem_u32(ps);
+      bool ok = true;
+      auto issue_pv = [&](int s) -> bool {
+        const int slot = s % C::NS, pb = s & 1;
+        if (!mbar_wait(&p_full[pb], (s >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(smem + slot * C::STAGE + C::TILE);
+#pragma unroll
+        for (int j = 0; j < C::SK / 16; ++j) {
+          const uint64_t ad = sw128_desc(p_base + pb * C::P_BYTES + 32 * j, 16, 1024);
+          const uint64_t bd = sw128_desc(v_base + j * 16 * 128, C::SK * 128, 1024);
+          tc_mma(tm_o, ad, bd, C::IDESC_PV, (s > 0 || j > 0) ? 1u : 0u);
+        }
+        tc_commit(&pv_done[pb]);
+        tc_commit(&empty[slot]);
+        return true;
+      };
+      for (int s = 0; s < n_stages && ok; ++s) {
+        const int slot = s % C::NS, sb = s & 1;
+        if (!mbar_wait(&full[slot], (s / C::NS) & 1)) {
+          ok = false;
+          break;
+        }
+        if (s >= 2 && !mbar_wait(&s_free[sb], ((s >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(smem + slot * C::STAGE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk >> 2, w = kk & 3;
+          const uint64_t ad = sw128_desc(q_base + c * C::M * 128 + 32 * w, 16, 1024);
+          const uint64_t bd = sw128_desc(k_base + c * C::SK * 128 + 32 * w, 16, 1024);
+          tc_mma(tm_s0 + sb * C::SK, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[sb]);
+        if (s >= 1) ok = issue_pv(s - 1);
+      }
+      if (ok && n_stages >= 1) ok = issue_pv(n_stages - 1);
+      if (!ok) {
+        atomicOr(a.status, PA_STATUS_TIMEOUT);
+        atomicOr(&s_timeout, 1);
+      }
+    }
+    __syncwarp();
+  } else {
+    // =========================== softmax warps (rows) =======================
+    const int r = warp * 32 + lane;                          // TMEM lane / query row
+    const int rc = min(r, R - 1);                            // padding rows mask like the last row
+    const int hi = si.L + rc / a.G;
+    const int lo = a.window > 0 ? hi - a.window + 1 : INT_MIN;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int s = 0; s < n_stages; ++s) {
+      const int sb = s & 1;
+      if (!mbar_wait(&s_full[sb], (s >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[C::SK];
+      tmem_ld32(tm_s0 + sb * C::SK + lane_off, x);
+      tmem_ld32(tm_s0 + sb * C::SK + 32 + lane_off, x + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+
+      const int key0 = kstart + s * C::SK;
+      const bool clean = key0 >= lo && key0 + C::SK - 1 <= hi;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < C::SK; ++j) {
+        float v = x[j] * sl2;
+        if (!clean) {
+          const int key = key0 + j;
+          v = (key >= lo && key <= hi) ? v : -INFINITY;
+        }
+        x[j] = v;
+        mt = fmaxf(mt, v);
+      }
+      // lazy running max: move the reference only when the row max grows by
+      // more than 2^8 (or on the first finite score)
+      const bool need = (mt > m_ref + 8.f) || (m_ref == -INFINITY && mt != -INFINITY);
+      const float m_new = need ? mt : m_ref;
+      const float alpha = need ? ex2(m_ref - m_new) : 1.f;  // 0 when m_ref was -inf
+      if (__any_sync(0xffffffffu, need) && s >= 1) {
+        // rescale this warp's O rows once the previous PV has landed
+        if (!mbar_wait(&pv_done[(s - 1) & 1], ((s - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(tm_o + 32 * c + lane_off, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tm_o + 32 * c + lane_off, o);
+        }
+        tc_fence_before();
+      }
+      l *= alpha;
+      m_ref = m_new;
+      const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+      uint32_t pk[C::SK / 2];
+#pragma unroll
+      for (int j = 0; j < C::SK; j += 2) {
+        const float p0 = ex2(x[j] - mu), p1 = ex2(x[j + 1] - mu);
+        l += p0 + p1;
+        pk[j / 2] = pack2<C::kBf16>(p0, p1);
+      }
+      // the P buffer is free once the PV two stages back has finished
+      if (s >= 2 && !mbar_wait(&pv_done[sb], ((s >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = ps + sb * C::P_BYTES + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(prow + swz(u, r)) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      // V rows of keys outside every row's range may hold garbage (even NaN);
+      // their weights are 0 but 0 * NaN is not: clear those rows.
+      if (key0 < si.klo || key0 + C::SK - 1 > si.khi) {
+        uint8_t* vt = smem + (s % C::NS) * C::STAGE + C::TILE;
+        for (int idx = threadIdx.x; idx < C::SK * C::CH * 8; idx += 64) {
+          const int k = idx / (C::CH * 8), rem = idx % (C::CH * 8);
+          const int key = key0 + k;
+          if (key < si.klo || key > si.khi)
+            *reinterpret_cast<uint4*>(vt + ((rem >> 3) * C::SK + k) * 128 + 16 * (rem & 7)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+    }
+    // ---- epilogue: O row from TMEM -> partial or output ----
+    if (ok && n_stages >= 1 && !mbar_wait(&pv_done[(n_stages - 1) & 1], ((n_stages - 1) >> 1) & 1)) ok = false;
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(a.status, PA_STATUS_TIMEOUT);
+        atomicOr(&s_timeout, 1);
+      }
+    }
+    tc_fence_after();
+    const bool poisoned = s_bad != 0 || s_timeout != 0 || !ok;
+    const bool real = r < R;
+    const size_t row = real ? static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float o[32];
+      tmem_ld32(tm_o + 32 * c + lane_off, o);
+      if (real) {
+        if (si.nparts == 1) {
+          const float inv = (poisoned || !(l > 0.f)) ? 0.f : 1.f / l;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, o[e] * inv);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.po + (row * a.num_parts + p) * D + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        }
+      }
+    }
+    if (real && si.nparts > 1) {
+      a.pm[row * a.num_parts + p] = m_ref;
+      a.pl[row * a.num_parts + p] = poisoned ? -1.f : l;
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace pa

@@ -43,6 +43,20 @@ long long round_up(long long a, long long q) { return ceil_div(a, q) * q; }
 
 int dtype_bytes(pa_dtype t) { return t == PA_F32 ? 4 : (t == PA_U8 ? 1 : 2); }
 
+// Optional override of the partition kernel for the 16-bit paths, read once:
+// "tc" forces the tensor-memory kernel wherever it applies, "mma" the
+// warp-level one; unset = chosen by row count.
+int env_kernel_choice() {
+  static const int v = [] {
+    const char* s = std::getenv("PA_VERIFY_KERNEL");
+    if (s == nullptr) return 0;
+    if (std::strcmp(s, "tc") == 0) return 2;
+    if (std::strcmp(s, "mma") == 0) return 1;
+    return 0;
+  }();
+  return v;
+}
+
 // Optional tuning override of the partition size (keys), read once.
 int env_part_tokens() {
   static const int v = [] {
@@ -91,6 +105,20 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const long long rows = static_cast<long long>(G) * tmax;
   int kernel = (kv == PA_F32) ? 1 : 0;
   int nt = 0, sk = 64, smem = 0, ctas_per_sm = 4;
+  // 16-bit caches with more than 32 query rows per KV head (e.g. 8 verify
+  // tokens x 8 GQA heads) outgrow warp-level mma: use the tensor-memory path.
+  const bool tc_ok = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128) && rows <= 64;
+  const int choice = env_kernel_choice();
+  if (tc_ok && choice != 1 && (rows > 32 || choice == 2)) {
+    bool ok = false;
+    pa::MmaKernelInfo info = pa::tc_info(D, mma_kind(kv), &ok);
+    if (ok) {
+      kernel = 2;
+      sk = info.stage_keys;
+      smem = info.smem_bytes;
+      ctas_per_sm = info.ctas_per_sm;
+    }
+  }
   if (kernel == 0) {
     // one 8-row n-tile per warp keeps a warp's accumulators within the
     // register budget of two CTAs per SM; rows beyond 8 go to more warps
@@ -256,14 +284,20 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.num_parts = plan.num_partitions;
   const int box_rows = std::min(d->page_size, plan.stage_keys);
   a.box_log2 = ilog2(box_rows);
-  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (1 << 30);
+  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (plan.kernel == 2 ? 64 : (1 << 30));
   a.q_dtype = d->q_dtype;
   a.out_dtype = d->out_dtype;
   a.scale_log2 = c.scale * 1.4426950408889634f;
   const dim3 grid(plan.num_partitions, d->num_kv_heads, d->num_seqs);
 
   cudaError_t e;
-  if (plan.kernel == 0) {
+  if (plan.kernel == 2) {
+    CUtensorMap mk, mv;
+    int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
+    if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
+    if (rc != PA_OK) return rc;
+    e = pa::launch_tc(d->head_dim, mma_kind(c.kv), mk, mv, a, grid, c.stream);
+  } else if (plan.kernel == 0) {
     CUtensorMap mk, mv;
     int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
     if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
@@ -302,7 +336,7 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.window = c.window;
   a.part_tokens = plan.part_tokens;
   a.num_parts = plan.num_partitions;
-  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (1 << 30);
+  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (plan.kernel == 2 ? 64 : (1 << 30));
   a.out_dtype = d->out_dtype;
   const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
   cudaLaunchConfig_t cfg = {};

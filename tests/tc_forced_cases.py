@@ -1,0 +1,47 @@
+"""Run in a child process with PA_VERIFY_KERNEL=tc: every case below goes
+through the tensor-memory partition kernel; prints one JSON line per case
+with the max abs error against the oracle and the gather-trace check."""
+import json
+import os
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+sys.path.insert(0, os.path.dirname(HERE))
+
+import numpy as np  # noqa: E402
+
+import oracle  # noqa: E402
+from paged_attention_speculative_gb300 import workloads as W  # noqa: E402
+from pa_testing import derived_tolerance, max_abs_err, run_gpu, run_oracle  # noqa: E402
+
+EDGE = {"tc_window_batch"}  # short contexts (O(1) outputs): derived bf16 bound
+
+CASES = [
+    lambda: W.qwen_gqa(1, 1000, seed=71),
+    lambda: W.qwen_gqa(4, 2047, seed=72),
+    lambda: W.long_ctx_b(3000, seed=73),
+    lambda: W.make_case("tc_f16_rows40", seed=74, query_lens=[5], past_lens=[1777], num_q_heads=64, num_kv_heads=8,
+                        head_dim=128, page_size=32, q_dtype="f16", kv_dtype="f16"),
+    lambda: W.make_case("tc_d64_rows64", seed=75, query_lens=[8], past_lens=[900], num_q_heads=32, num_kv_heads=4,
+                        head_dim=64, page_size=16),
+    lambda: W.make_case("tc_window_batch", seed=76, query_lens=[8, 3, 0, 6], past_lens=[1200, 64, 10, 333],
+                        num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=16, sliding_window=300),
+    lambda: W.make_case("tc_ps8_long", seed=77, query_lens=[7], past_lens=[9000], num_q_heads=64, num_kv_heads=8,
+                        head_dim=128, page_size=8),
+]
+
+if __name__ == "__main__":
+    assert os.environ.get("PA_VERIFY_KERNEL") == "tc"
+    for make in CASES:
+        case = make()
+        got, bits, trace = run_gpu(case, traced=True)
+        want = run_oracle(case)
+        pages = oracle.pages_touched(case.block_tables, case.past_lens, case.subsequence_begins,
+                                     page_size=case.page_size, sliding_window=case.sliding_window)
+        trace_ok = all(np.array_equal(trace[:, g, :], pages) for g in range(case.num_kv_heads))
+        excess = None
+        if case.name in EDGE:
+            excess = float(np.max(np.abs(got - want) - derived_tolerance(case, want)))
+        print(json.dumps({"case": case.name, "bits": bits, "err": max_abs_err(got, want), "excess": excess,
+                          "trace_ok": trace_ok}), flush=True)

@@ -1,0 +1,31 @@
+"""The tensor-memory (tcgen05) partition kernel on every shape it accepts:
+a child process forces it (PA_VERIFY_KERNEL=tc) for 1..64 query rows per KV
+head, head_dim 64 / 128, bf16 / f16, windows and ragged tails, and each case
+is compared with the fp64 oracle (<= 2e-3) and its gather trace bit-exactly."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+from pa_testing import TOL
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def test_forced_tensor_memory_path_matches_oracle():
+    env = dict(os.environ, PA_VERIFY_KERNEL="tc")
+    proc = subprocess.run([sys.executable, os.path.join(HERE, "tc_forced_cases.py")], env=env,
+                          capture_output=True, text=True, timeout=600)
+    assert proc.returncode == 0, proc.stderr[-3000:]
+    rows = [json.loads(line) for line in proc.stdout.splitlines() if line.startswith("{")]
+    assert len(rows) == 7
+    for r in rows:
+        assert r["bits"] == 0, r
+        assert r["trace_ok"], r
+        if r["excess"] is None:
+            assert r["err"] <= TOL, r
+        else:  # short-context edge case: the derived bf16 bound (see pa_testing.derived_tolerance)
+            assert r["excess"] <= 0.0, r
