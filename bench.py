@@ -183,6 +183,15 @@ def whole_job_gbs(bytes_per_rank_step: int, world: int, max_us_per_step: float) 
     return world * bytes_per_rank_step / (max_us_per_step * 1e-6) / 1e9
 
 
+def kernel_name(wl) -> str:
+    p = wl.plan()
+    if p.kernel == 2:
+        return f"pa_partition_tc<D={wl.D}, {wl.kv}> (tcgen05, TMEM accumulators)"
+    if p.kernel == 1:
+        return f"pa_partition_f32<D={wl.D}>"
+    return f"pa_partition_mma<D={wl.D}, {wl.kv}, n-tiles={p.row_tiles}> (mma.sync)"
+
+
 def l2_bytes():
     import torch
     return int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20))
@@ -547,7 +556,7 @@ def run_ours(args, rank, world):
                                   "partition_us": round(pm, 2), "kv_mb": round(w.kv_bytes / 1e6, 2),
                                   "kv_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / hbm_peak, 3),
                                   "ratio_vs_T1": round(u / base, 3), "tflops": round(w.flops / (u * 1e-6) / 1e12, 1),
-                                  "partitions": w.plan().num_partitions})
+                                  "partitions": w.plan().num_partitions, "kernel": kernel_name(w).split(" ")[0]})
                     log(f"[bench] {sweep[-1]}")
                     del w
                     torch.cuda.empty_cache()
@@ -592,7 +601,7 @@ def run_ours(args, rank, world):
                          f" MiB > 2x L2)", "launch": "CUDA graph replay", "trials": len(trials)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": measured_traffic(H["name"]),
-                     "kernel": f"pa_partition_mma<D=128, bf16, n-tiles={wl.plan().row_tiles}>",
+                     "kernel": kernel_name(wl),
                      "kernel_us_mean": part_mean, "kernel_timing": "CUDA graph of back-to-back partition launches",
                      "kernel_us_median": part_med, "algorithmic_bytes_per_launch": wl.kv_bytes,
                      "peak_kind": f"{peak_kind} copy rate (MEASURED_PEAKS.json hbm_gbs)"},

@@ -12,9 +12,14 @@
 //   warp 2      MMA issuer (one thread)
 //   warp 3      TMA producer (block-table lookup + tile loads, as in the mma path)
 // Per 64-key stage s:
-//   S(s)  = Q . K_s^T          tcgen05.mma M=128 (rows 0..63 real), N=64, K=D   -> TMEM
-//   P(s)  = 2^(S*scale*log2e - m)  (softmax warps, bf16/f16, 128-byte-swizzled smem)
-//   O    += P(s) . V_s          tcgen05.mma M=128, N=D, K=64, V as MN-major B     -> TMEM
+//   S(s)  = Q . K_s^T          tcgen05.mma M=128 (rows 0..63 real), N=64, K=D,
+//                              A = Q from TMEM, K as K-major B from smem        -> TMEM
+//   P(s)  = 2^(S*scale*log2e - m)  (softmax warps, bf16/f16, written to TMEM)
+//   O    += P(s) . V_s          tcgen05.mma M=128, N=D, K=64, A = P from TMEM,
+//                              V as MN-major B from shared memory             -> TMEM
+// Q and P live in tensor memory so shared memory holds only the KV ring (six
+// 32 KB stages): a stage is held from its TMA landing until its PV
+// completes, and the ring depth beyond that is what keeps HBM busy.
 // S(s+1) is issued before PV(s) so the tensor cores work while the softmax
 // runs.  The running max is kept lazily: O is rescaled (TMEM load/store) only
 // when a row's max grows by more than 2^8, otherwise weights are taken
@@ -87,6 +92,27 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] . B[smem desc]: A (M rows x 16 K) sits in TMEM, one
+// row per lane, two 16-bit K elements per 32-bit column.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
 // start address, leading / stride byte offsets (16-byte units), version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
@@ -116,19 +142,22 @@ struct TcCfg {
   static constexpr int CH = D / 64;               // 128-byte chunks per key row
   static constexpr int TILE = SK * D * 2;         // one K (or V) stage tile
   static constexpr int STAGE = 2 * TILE;
-  static constexpr int Q_BYTES = CH * M * 128;    // [chunk][row][128 B]
-  static constexpr int P_BYTES = M * 128;         // [row][64 keys x 2 B]
-  static constexpr int FIXED = Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + 256 + 1024;
-  static constexpr int NS = ((220 * 1024 - FIXED) / STAGE) > 8 ? 8 : ((220 * 1024 - FIXED) / STAGE);
-  static constexpr int Q_OFF = NS * STAGE;
-  static constexpr int P_OFF = Q_OFF + Q_BYTES;
-  static constexpr int BLK_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int FIXED = 4 * kMaxPagesPerCta + 512 + 1024;
+  static constexpr int NS_FIT = (226 * 1024 - FIXED) / STAGE;
+  static constexpr int NS = NS_FIT > 16 ? 16 : NS_FIT;
+  static constexpr int BLK_OFF = NS * STAGE;
   static constexpr int BAR_OFF = BLK_OFF + 4 * kMaxPagesPerCta;
-  static constexpr int BYTES = BAR_OFF + 256 + 1024;
-  static constexpr int TMEM_COLS = 256;           // O: D columns, S: 2 x 64 columns
+  static constexpr int BYTES = BAR_OFF + 512 + 1024;
+  // TMEM columns: O [0, D), S buffers [D, D + 2 SK), P buffers (16-bit
+  // pairs) [D + 2 SK, D + 3 SK), Q (16-bit pairs) [D + 3 SK, D + 3 SK + D/2)
+  static constexpr int S_COL = D;
+  static constexpr int P_COL = D + 2 * SK;
+  static constexpr int Q_COL = D + 3 * SK;
+  static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = tc_idesc(M, SK, kBf16, false);
   static constexpr uint32_t IDESC_PV = tc_idesc(M, D, kBf16, true);
-  static_assert(NS >= 2, "pipeline needs two stages");
+  static_assert(NS >= 4, "pipeline needs a few stages");
+  static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory budget");
 };
 
 template <int D, int KV>
@@ -138,8 +167,6 @@ __global__ void __launch_bounds__(128, 1)
   using C = TcCfg<D, KV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qs = smem + C::Q_OFF;
-  uint8_t* ps = smem + C::P_OFF;
   int32_t* blk = reinterpret_cast<int32_t*>(smem + C::BLK_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* full = bars;                 // [NS] TMA landed
@@ -197,30 +224,41 @@ __global__ void __launch_bounds__(128, 1)
     tmem_alloc(&s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
-  // Q rows (query row r = token r/G, head g*G + r%G) into [chunk][row][128 B],
-  // 128-byte swizzled; rows R..127 zero.
-  for (int u = threadIdx.x; u < C::M * C::CH * 8; u += blockDim.x) {
-    const int r = u / (C::CH * 8), rem = u % (C::CH * 8), c = rem >> 3, unit = rem & 7;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < R) {
-      const size_t row = static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G;
-      v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + row * D) + c * 8 + unit);
+  tc_fence_before();
+  __syncthreads();  // the TMEM address is published
+  tc_fence_after();
+  {
+    // Q rows into TMEM (lane = query row r = token r/G, head g*G + r%G; two
+    // 16-bit elements per column); lanes R..127 zero.  Each warp writes its
+    // own lane quarter.
+    const uint32_t base = s_tmem;
+    const int r = warp * 32 + lane;
+    const bool real = r < R;
+    const size_t row = real ? static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + row * D);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      uint32_t v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 x = real ? __ldg(src + 8 * c + u) : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * u] = x.x;
+        v[4 * u + 1] = x.y;
+        v[4 * u + 2] = x.z;
+        v[4 * u + 3] = x.w;
+      }
+      tmem_st32(base + C::Q_COL + 32 * c + (static_cast<uint32_t>(warp * 32) << 16),
+                reinterpret_cast<const float*>(v));
     }
-    *reinterpret_cast<uint4*>(qs + (c * C::M + r) * 128 + swz(unit, r)) = v;
   }
-  // P rows 64..127 are padding: zero them once in both buffers.
-  for (int u = threadIdx.x; u < 2 * (C::M - C::ROWS) * 8; u += blockDim.x) {
-    const int buf = u / ((C::M - C::ROWS) * 8), rem = u % ((C::M - C::ROWS) * 8);
-    *reinterpret_cast<uint4*>(ps + buf * C::P_BYTES + (C::ROWS + (rem >> 3)) * 128 + 16 * (rem & 7)) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-  fence_proxy_async();  // generic smem writes -> visible to the tensor cores
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t tm_o = tmem;                      // O: columns [0, D)
-  const uint32_t tm_s0 = tmem + D;                 // S buffers: [D, D + 64), [D + 64, D + 128)
+  const uint32_t tm_o = tmem;                      // O
+  const uint32_t tm_s0 = tmem + C::S_COL;          // S buffers
+  const uint32_t tm_p0 = tmem + C::P_COL;          // P buffers (16-bit pairs)
+  const uint32_t tm_q = tmem + C::Q_COL;           // Q (16-bit pairs)
 
   if (warp == 3) {
     // =========================== TMA producer ===============================
@@ -270,7 +308,6 @@ __global__ void __launch_bounds__(128, 1)
   } else if (warp == 2) {
     // =========================== MMA issuer =================================
     if (lane == 0) {
-      const uint32_t q_base = smem_u32(qs), p_base = smem_u32(ps);
       bool ok = true;
       auto issue_pv = [&](int s) -> bool {
         const int slot = s % C::NS, pb = s & 1;
@@ -279,9 +316,8 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t v_base = smem_u32(smem + slot * C::STAGE + C::TILE);
 #pragma unroll
         for (int j = 0; j < C::SK / 16; ++j) {
-          const uint64_t ad = sw128_desc(p_base + pb * C::P_BYTES + 32 * j, 16, 1024);
           const uint64_t bd = sw128_desc(v_base + j * 16 * 128, C::SK * 128, 1024);
-          tc_mma(tm_o, ad, bd, C::IDESC_PV, (s > 0 || j > 0) ? 1u : 0u);
+          tc_mma_ta(tm_o, tm_p0 + pb * (C::SK / 2) + 8 * j, bd, C::IDESC_PV, (s > 0 || j > 0) ? 1u : 0u);
         }
         tc_commit(&pv_done[pb]);
         tc_commit(&empty[slot]);
@@ -302,9 +338,8 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int c = kk >> 2, w = kk & 3;
-          const uint64_t ad = sw128_desc(q_base + c * C::M * 128 + 32 * w, 16, 1024);
           const uint64_t bd = sw128_desc(k_base + c * C::SK * 128 + 32 * w, 16, 1024);
-          tc_mma(tm_s0 + sb * C::SK, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          tc_mma_ta(tm_s0 + sb * C::SK, tm_q + 8 * kk, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[sb]);
         if (s >= 1) ok = issue_pv(s - 1);
@@ -390,10 +425,7 @@ __global__ void __launch_bounds__(128, 1)
         ok = false;
         break;
       }
-      uint8_t* prow = ps + sb * C::P_BYTES + r * 128;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(prow + swz(u, r)) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      tmem_st32(tm_p0 + sb * (C::SK / 2) + lane_off, reinterpret_cast<const float*>(pk));
       // V rows of keys outside every row's range may hold garbage (even NaN);
       // their weights are 0 but 0 * NaN is not: clear those rows.
       if (key0 < si.klo || key0 + C::SK - 1 > si.khi) {
@@ -406,6 +438,7 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
       fence_proxy_async();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
     }

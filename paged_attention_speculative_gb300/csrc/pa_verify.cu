@@ -105,11 +105,14 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const long long rows = static_cast<long long>(G) * tmax;
   int kernel = (kv == PA_F32) ? 1 : 0;
   int nt = 0, sk = 64, smem = 0, ctas_per_sm = 4;
-  // 16-bit caches with more than 32 query rows per KV head (e.g. 8 verify
-  // tokens x 8 GQA heads) outgrow warp-level mma: use the tensor-memory path.
+  // 16-bit caches with 8 or more query rows per KV head (T > 1 verify
+  // steps, wide GQA groups) go to the tensor-memory path: its cost per key
+  // does not grow with the row count (measured: T=4 x 4 heads and T=8 x 8
+  // heads cost 1.02-1.07x a single-token step).  Up to 4 rows the warp-level
+  // path is slightly faster.
   const bool tc_ok = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128) && rows <= 64;
   const int choice = env_kernel_choice();
-  if (tc_ok && choice != 1 && (rows > 32 || choice == 2)) {
+  if (tc_ok && choice != 1 && (rows >= 8 || choice == 2)) {
     bool ok = false;
     pa::MmaKernelInfo info = pa::tc_info(D, mma_kind(kv), &ok);
     if (ok) {

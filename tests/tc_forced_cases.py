@@ -27,6 +27,8 @@ CASES = [
                         head_dim=64, page_size=16),
     lambda: W.make_case("tc_window_batch", seed=76, query_lens=[8, 3, 0, 6], past_lens=[1200, 64, 10, 333],
                         num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=16, sliding_window=300),
+    lambda: W.make_case("tc_ps64_rows64", seed=78, query_lens=[8], past_lens=[2000], num_q_heads=64, num_kv_heads=8,
+                        head_dim=128, page_size=64),
     lambda: W.make_case("tc_ps8_long", seed=77, query_lens=[7], past_lens=[9000], num_q_heads=64, num_kv_heads=8,
                         head_dim=128, page_size=8),
 ]

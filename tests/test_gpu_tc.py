@@ -21,7 +21,7 @@ def test_forced_tensor_memory_path_matches_oracle():
                           capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stderr[-3000:]
     rows = [json.loads(line) for line in proc.stdout.splitlines() if line.startswith("{")]
-    assert len(rows) == 7
+    assert len(rows) == 8
     for r in rows:
         assert r["bits"] == 0, r
         assert r["trace_ok"], r

@@ -43,20 +43,26 @@ def dims(**kw):
 
 
 def test_plan_fills_the_sms_once_at_long_context(lib):
-    p = pa.plan(dims(), 32772, 0, pa.PA_BF16, 152)
+    p = pa.plan(dims(total_tokens=1), 32769, 0, pa.PA_BF16, 152)
     assert p.kernel == 0 and p.row_tiles == 1
     assert p.part_tokens % max(p.stage_keys, 16) == 0
-    assert p.num_partitions * p.part_tokens >= 32772
-    assert (p.num_partitions - 1) * p.part_tokens < 32772
+    assert p.num_partitions * p.part_tokens >= 32769
+    assert (p.num_partitions - 1) * p.part_tokens < 32769
     assert 0.8 * 304 <= p.ctas <= 1.1 * 304
+    # 16 rows per KV head: the tensor-memory kernel, one CTA per SM
+    t = pa.plan(dims(), 32772, 0, pa.PA_BF16, 152)
+    assert t.kernel == 2 and t.stage_keys == 64
+    assert 0.8 * 152 <= t.ctas <= 1.1 * 152
 
 
 def test_plan_independent_of_query_count(lib):
     """The split must not collapse when a sequence brings more than one
     query token (the failure both OpenVINO issue 38153 and the
     dual-radeon-vllm article describe)."""
-    ps = [pa.plan(dims(total_tokens=t), 32768 + t, 0, pa.PA_BF16, 152).num_partitions for t in (1, 2, 3, 4)]
+    ps = [pa.plan(dims(total_tokens=t), 32768 + t, 0, pa.PA_BF16, 152).num_partitions for t in (2, 3, 4)]
     assert min(ps) == max(ps) and ps[0] > 16
+    # T=1 (4 rows) takes the warp-level kernel at two CTAs per SM: twice the split
+    assert pa.plan(dims(total_tokens=1), 32769, 0, pa.PA_BF16, 152).num_partitions >= ps[0]
 
 
 def test_plan_window_reads_only_the_window(lib):
