@@ -104,7 +104,8 @@ typedef struct {
   int32_t stage_keys;      /* keys staged per pipeline step                       */
   int32_t row_tiles;       /* n-tiles of 8 query rows per warp (1 or 2)           */
   int32_t kernel;          /* 0 = warp-level mma path (16-bit / u8 KV), 1 = fp32 path,
-                              2 = tensor-memory (tcgen05) path (16-bit KV, D <= 128,
+                              2 = tensor-memory (tcgen05) path (16-bit KV with D <= 128,
+                              or u8 KV with D = 128;
                               8..64 query rows per KV head) */
   int32_t num_sms;         /* SM count the plan was made for                       */
   int32_t ctas;            /* grid size B * Hkv * P                                */

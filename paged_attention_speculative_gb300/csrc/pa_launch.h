@@ -29,7 +29,8 @@ cudaError_t launch_mma_d128(int kv, int nt, const CUtensorMap& k, const CUtensor
 cudaError_t launch_mma_d256(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                             cudaStream_t st);
 
-// Tensor-memory (tcgen05) partition kernel: head_dim 64 / 128, kv KV_BF16 / KV_F16.
+// Tensor-memory (tcgen05) partition kernels: head_dim 64 / 128 with KV_BF16 /
+// KV_F16 caches, head_dim 128 with KV_U8 caches.
 MmaKernelInfo tc_info(int D, int kv, bool* ok);
 cudaError_t launch_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                       cudaStream_t st);

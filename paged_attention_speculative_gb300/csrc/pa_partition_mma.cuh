@@ -176,17 +176,25 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
           atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
       }
       if constexpr (C::kU8) {
+        // per segment [scales(br) | zero-points(br)]; one copy when the
+        // segment is a whole page (the record keeps both arrays adjacent)
         const size_t rec = static_cast<size_t>(a.ps) * (D + 4);
         for (int j = lane; j < nseg; j += 32) {
           const int key = key0 + (j << br_log2);
           const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
           const int id = blk[lp - lp0];
           const size_t roff = (static_cast<size_t>(id) * a.Hkv + g) * rec + static_cast<size_t>(a.ps) * D;
-          uint8_t* dst = st + 2 * C::TILE + 2 * (j << br_log2);
-          bulk_load(dst, a.k_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
-          bulk_load(dst + C::SZ, a.k_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
-          bulk_load(dst + 2 * C::SZ, a.v_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
-          bulk_load(dst + 3 * C::SZ, a.v_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
+          uint8_t* dk = st + 2 * C::TILE + j * 4 * br;
+          uint8_t* dv = dk + 4 * C::SK;
+          if (br == a.ps) {
+            bulk_load(dk, a.k_bytes + roff, 4 * br, &full[slot]);
+            bulk_load(dv, a.v_bytes + roff, 4 * br, &full[slot]);
+          } else {
+            bulk_load(dk, a.k_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
+            bulk_load(dk + 2 * br, a.k_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
+            bulk_load(dv, a.v_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
+            bulk_load(dv + 2 * br, a.v_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
+          }
         }
       }
       issued = s + 1;
@@ -342,9 +350,11 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
               for (int hf = 0; hf < 2; ++hf)
                 kw[kh][dc][hf] = *reinterpret_cast<const uint4*>(
                     st + tile_row_off(kk, dc, a.box_log2, C::CHUNKS) + swz(tig + 4 * hf, kk));
-            const __half* scp = reinterpret_cast<const __half*>(st + 2 * C::TILE);
-            ksc[kh] = __half2float(scp[kk]) * sl2;
-            kzp[kh] = __half2float(scp[C::SK + kk]);
+            const __half* scp = reinterpret_cast<const __half*>(st + 2 * C::TILE + (kk >> a.box_log2) * 4 *
+                                                                (1 << a.box_log2));
+            const int o = kk & ((1 << a.box_log2) - 1);
+            ksc[kh] = __half2float(scp[o]) * sl2;
+            kzp[kh] = __half2float(scp[(1 << a.box_log2) + o]);
           }
 #pragma unroll
           for (int k = 0; k < C::KSTEPS; ++k) {
@@ -421,15 +431,17 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
             pb[nt][1] = movmatrix_t(pack2<kBf>(sc[nt][2], sc[nt][3]));
           }
         } else {
-          const __half* scp = reinterpret_cast<const __half*>(st + 2 * C::TILE + 2 * C::SZ);
           float vsc[2], vzp[2];
 #pragma unroll
           for (int kh = 0; kh < 2; ++kh) {
             const int kk = 16 * c + key_perm(g8 + 8 * kh);
             const int key = kk + key0;
             const bool in_union = key >= si.klo && key <= si.khi;
-            vsc[kh] = in_union ? __half2float(scp[kk]) : 0.f;
-            vzp[kh] = in_union ? __half2float(scp[C::SK + kk]) : 0.f;
+            const __half* scp = reinterpret_cast<const __half*>(st + 2 * C::TILE + 4 * C::SK +
+                                                                (kk >> a.box_log2) * 4 * (1 << a.box_log2));
+            const int o = kk & ((1 << a.box_log2) - 1);
+            vsc[kh] = in_union ? __half2float(scp[o]) : 0.f;
+            vzp[kh] = in_union ? __half2float(scp[(1 << a.box_log2) + o]) : 0.f;
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {

@@ -110,9 +110,11 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   // does not grow with the row count (measured: T=4 x 4 heads and T=8 x 8
   // heads cost 1.02-1.07x a single-token step).  Up to 4 rows the warp-level
   // path is slightly faster.
-  const bool tc_ok = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128) && rows <= 64;
+  const bool tc16 = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128);
+  const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
   const int choice = env_kernel_choice();
-  if (tc_ok && choice != 1 && (rows >= 8 || choice == 2)) {
+  // u8 caches take the tensor-memory kernel only when forced (tuning).
+  if (tc_ok && choice != 1 && ((rows >= 8 && tc16) || choice == 2)) {
     bool ok = false;
     pa::MmaKernelInfo info = pa::tc_info(D, mma_kind(kv), &ok);
     if (ok) {

@@ -29,6 +29,12 @@ CASES = [
                         num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=16, sliding_window=300),
     lambda: W.make_case("tc_ps64_rows64", seed=78, query_lens=[8], past_lens=[2000], num_q_heads=64, num_kv_heads=8,
                         head_dim=128, page_size=64),
+    lambda: W.qwen_u8(1, 1500, seed=79),
+    lambda: W.qwen_u8(3, 2345, seed=80),
+    lambda: W.make_case("tcu8_rows64_f16q", seed=81, query_lens=[8], past_lens=[3100], num_q_heads=64, num_kv_heads=8,
+                        head_dim=128, page_size=16, kv_dtype="u8", q_dtype="f16"),
+    lambda: W.make_case("tcu8_window_ps32", seed=82, query_lens=[4, 2], past_lens=[1500, 700], num_q_heads=32,
+                        num_kv_heads=8, head_dim=128, page_size=32, kv_dtype="u8", sliding_window=500),
     lambda: W.make_case("tc_ps8_long", seed=77, query_lens=[7], past_lens=[9000], num_q_heads=64, num_kv_heads=8,
                         head_dim=128, page_size=8),
 ]

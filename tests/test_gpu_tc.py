@@ -1,6 +1,6 @@
 """The tensor-memory (tcgen05) partition kernel on every shape it accepts:
 a child process forces it (PA_VERIFY_KERNEL=tc) for 1..64 query rows per KV
-head, head_dim 64 / 128, bf16 / f16, windows and ragged tails, and each case
+head, head_dim 64 / 128, bf16 / f16 and u8 caches, windows and ragged tails, and each case
 is compared with the fp64 oracle (<= 2e-3) and its gather trace bit-exactly."""
 import json
 import os
@@ -21,7 +21,7 @@ def test_forced_tensor_memory_path_matches_oracle():
                           capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stderr[-3000:]
     rows = [json.loads(line) for line in proc.stdout.splitlines() if line.startswith("{")]
-    assert len(rows) == 8
+    assert len(rows) == 12
     for r in rows:
         assert r["bits"] == 0, r
         assert r["trace_ok"], r
