@@ -102,11 +102,14 @@ typedef struct {
   int32_t num_partitions;  /* P: KV partitions per (sequence, KV head), grid.x   */
   int32_t part_tokens;     /* keys per partition (multiple of the stage size)     */
   int32_t stage_keys;      /* keys staged per pipeline step                       */
-  int32_t row_tiles;       /* n-tiles of 8 query rows per warp (1 or 2)           */
+  int32_t row_tiles;       /* kernel 0: n-tiles of 8 query rows per warp (1 or 2);
+                              kernel 3: query-row tile N (16, 32 or 64)           */
   int32_t kernel;          /* 0 = warp-level mma path (16-bit / u8 KV), 1 = fp32 path,
-                              2 = tensor-memory (tcgen05) path (16-bit KV with D <= 128,
-                              or u8 KV with D = 128;
-                              8..64 query rows per KV head) */
+                              2 = tensor-memory (tcgen05) path, query rows on the MMA's
+                              M dimension (16-bit KV with D <= 128, or u8 KV with
+                              D = 128; 8..64 query rows per KV head),
+                              3 = tensor-memory path, keys on the MMA's M dimension
+                              (16-bit KV with D <= 128, up to 64 query rows) */
   int32_t num_sms;         /* SM count the plan was made for                       */
   int32_t ctas;            /* grid size B * Hkv * P                                */
   int32_t smem_bytes;      /* dynamic shared memory per partition CTA             */

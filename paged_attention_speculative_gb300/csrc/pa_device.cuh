@@ -65,13 +65,28 @@ struct SeqInfo {
   bool rows_ok;          // t0 / T can be trusted to index output rows
 };
 
+// A global load the compiler issues exactly once: a read-only (__ldg) load
+// may legally be repeated at each use instead of holding the value in a
+// register, and under a saturated memory system every repeat costs a full
+// round trip.
+__device__ __forceinline__ int32_t ld_once(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_once(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ SeqInfo seq_info(const int32_t* begins, const int32_t* past_lens, int b,
                                             int total_tokens, int G, int ps, int max_ctx, int window,
                                             int part_tokens, int row_capacity) {
   SeqInfo s;
-  s.t0 = __ldg(begins + b);
-  const int t1 = __ldg(begins + b + 1);
-  s.L = __ldg(past_lens + b);
+  s.t0 = ld_once(begins + b);
+  const int t1 = ld_once(begins + b + 1);
+  s.L = ld_once(past_lens + b);
   s.T = t1 - s.t0;
   s.err = 0;
   s.rows_ok = (s.t0 >= 0 && t1 >= s.t0 && t1 <= total_tokens);
@@ -179,6 +194,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+
+// 4-byte asynchronous global -> shared copy (completion: cp_async_wait_all).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

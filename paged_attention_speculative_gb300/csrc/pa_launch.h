@@ -35,4 +35,10 @@ MmaKernelInfo tc_info(int D, int kv, bool* ok);
 cudaError_t launch_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                       cudaStream_t st);
 
+// Tensor-memory partition kernels with the keys on the MMA's M dimension:
+// head_dim 64 / 128, KV_BF16 / KV_F16 caches, row tiles n = 16 / 32 / 64.
+MmaKernelInfo tk_info(int D, int kv, int n, bool* ok);
+cudaError_t launch_tk(int D, int kv, int n, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                      cudaStream_t st);
+
 }  // namespace pa

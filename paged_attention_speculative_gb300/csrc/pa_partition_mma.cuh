@@ -250,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     for (int kk = 0; kk < C::KSTEPS; ++kk) {
       if constexpr (!C::kU8) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(a.q) + qoff);
-        qf[kk][nt][0] = rv ? __ldg(src + (16 * kk + 2 * tig) / 2) : 0u;
-        qf[kk][nt][1] = rv ? __ldg(src + (16 * kk + 8 + 2 * tig) / 2) : 0u;
+        qf[kk][nt][0] = rv ? ld_once(src + (16 * kk + 2 * tig) / 2) : 0u;
+        qf[kk][nt][1] = rv ? ld_once(src + (16 * kk + 8 + 2 * tig) / 2) : 0u;
       } else {
         const int dc = kk >> 3, half = (kk >> 2) & 1, sub = kk & 3;
         const int d0 = 128 * dc + 16 * (tig + 4 * half) + 4 * sub;

@@ -2,19 +2,20 @@
 // caches with per-token fp16 scale / zero-point (OpenVINO issue 38153,
 // reproduction step 1: u8 KV cache precision), head_dim 128.
 //
-// The u8 codes are exact in f16, so the tensor cores take the codes
-// themselves and the dequantisation folds into two per-key terms:
-//   q . K_j      = scale^K_j (q . code^K_j - zp^K_j * sum(q))
-//   sum_j p_j V_j = sum_j (p_j scale^V_j) code^V_j - sum_j (p_j scale^V_j) zp^V_j
+// Converter warps dequantise every landed u8 stage once, value by value, to
+// f16 ((code - zp) * scale, two f16 operations per pair of codes) in the
+// 128-byte-swizzled tile layout of the 16-bit path; from there on the stage
+// is processed exactly like an f16 cache (S = Q.K^T and O += P.V on the tensor
+// cores, softmax one row per thread).  Keeping the per-key scale and
+// zero-point out of the softmax matters: read there, every key costs two
+// dependent shared-memory loads on the softmax's critical path.
 // Warp roles (256 threads):
-//   warps 0, 1    softmax: thread r owns query row r (TMEM lane r); applies the
-//                 per-key K terms, forms P'_j = p_j scale^V_j (f16, into TMEM)
-//                 and accumulates the zero-point term of its row
-//   warp 2        MMA issuer (one thread): S = Q . code^K^T, O += P' . code^V
+//   warps 0, 1    softmax: thread r owns query row r (TMEM lane r)
+//   warp 2        MMA issuer (one thread)
 //   warp 3        TMA producer: u8 code tiles + per-page scale / zero-point
-//   warps 6, 7    converters: each landed u8 stage -> 128-byte-swizzled f16
-//                 code tiles and fp32 per-key scale / zero-point arrays, once
-//                 per stage (not once per query-row group)
+//   warps 6, 7    converters: u8 stage -> f16 K / V tiles (value rows of keys
+//                 outside every query row's range are zeroed: their scales
+//                 may be garbage, and 0 * NaN is not 0)
 //   warps 4, 5    idle (they wait at the final barrier): warp w issues on
 //                 scheduler w % 4, and converters polling next to the
 //                 softmax warps would take the issue slots of the softmax
@@ -37,8 +38,7 @@ struct TcU8Cfg {
   static constexpr int U8_SIDE = 8 * SK;                  // [seg][scale|zp] for K, then V
   static constexpr int U8_STAGE = (2 * U8_TILE + U8_SIDE + 1023) / 1024 * 1024;
   static constexpr int F_TILE = SK * D * 2;               // f16 codes of K (or V), [chunk][key][128 B]
-  static constexpr int F_SIDE = 4 * SK * 4;               // fp32 k_scale*log2e*softmax_scale, k_zp, v_scale, v_zp
-  static constexpr int F_STAGE = (2 * F_TILE + F_SIDE + 1023) / 1024 * 1024;
+  static constexpr int F_STAGE = 2 * F_TILE;
   static constexpr int NB = 3;                            // f16 buffers
   static constexpr int FIXED = NB * F_STAGE + 4 * kMaxPagesPerCta + 512 + 1024;
   static constexpr int NSU_FIT = (226 * 1024 - FIXED) / U8_STAGE;
@@ -133,8 +133,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tm_o = tmem, tm_s0 = tmem + C::S_COL, tm_p0 = tmem + C::P_COL, tm_q = tmem + C::Q_COL;
 
   // Q rows -> f16 in TMEM (lanes 0..63; softmax warps), zeros in lanes 64..127
-  // (warps 2, 3); each softmax thread keeps the sum of its row's f16 query.
-  float qsum = 0.f;
+  // (warps 2, 3).
   if (warp < 4) {
     const int r = warp * 32 + lane;
     const bool real = r < R;
@@ -156,8 +155,6 @@ __global__ void __launch_bounds__(256, 1)
             f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
           }
           const __half2 h = __floats2half2_rn(f.x, f.y);
-          const float2 hr = __half22float2(h);
-          qsum += hr.x + hr.y;
           v[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h);
         }
       }
@@ -228,44 +225,48 @@ __global__ void __launch_bounds__(256, 1)
     // =========================== converters =================================
     const int ct = threadIdx.x - 192;  // 0..63
     const int br_log2 = a.box_log2, br = 1 << br_log2;
-    const float sl2 = a.scale_log2;
     for (int s = 0; s < n_stages; ++s) {
       const int slot = s % C::NSU, cb = s % C::NB;
       if (!mbar_wait(&full[slot], (s / C::NSU) & 1)) break;
       if (s >= C::NB && !mbar_wait(&cfree[cb], ((s / C::NB) - 1) & 1)) break;
       const uint8_t* st = smem + slot * C::U8_STAGE;
       uint8_t* fb = fbuf + cb * C::F_STAGE;
+      const int key0 = kstart + s * C::SK;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {  // K codes, then V codes
+      for (int half = 0; half < 2; ++half) {  // K, then V
         const uint8_t* src = st + half * C::U8_TILE;
+        const __half* side = reinterpret_cast<const __half*>(st + 2 * C::U8_TILE + half * 4 * C::SK);
         uint8_t* dst = fb + half * C::F_TILE;
 #pragma unroll 4
         for (int i = 0; i < (C::SK * 8) / 64; ++i) {
           const int u = ct + 64 * i;                // 16-byte unit of codes
           const int key = u >> 3, us = u & 7;       // d = 16 us .. 16 us + 15
+          const int seg = key >> br_log2, o = key & (br - 1);
+          const __half sc = side[seg * 2 * br + o], zp = side[seg * 2 * br + br + o];
+          // value = code * scale - zp * scale in one rounding; code enters f16
+          // exactly (1024 + code, less 1024).  zp * scale is about the size of
+          // the values themselves, so its f16 rounding stays relative.
+          const __half2 sc2 = __half2half2(sc);
+          const __half2 nzs2 = __half2half2(__float2half_rn(-__half2float(zp) * __half2float(sc)));
+          const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+          const bool keep = half == 0 || (key0 + key >= si.klo && key0 + key <= si.khi);
           const uint4 w = *reinterpret_cast<const uint4*>(src + key * 128 + swz(us, key));
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
           uint32_t h[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            h[2 * e] = u8pair_to_f16x2(ws[e], 0x4140u);
-            h[2 * e + 1] = u8pair_to_f16x2(ws[e], 0x4342u);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t b = __byte_perm(ws[e], 0x64646464u, q ? 0x4342u : 0x4140u);
+              const __half2 v = __hfma2(__hsub2(*reinterpret_cast<__half2*>(&b), k1024), sc2, nzs2);
+              h[2 * e + q] = keep ? *reinterpret_cast<const uint32_t*>(&v) : 0u;
+            }
           }
           const int c = us >> 2, du = 2 * (us & 3);
           uint8_t* rowp = dst + (c * C::SK + key) * 128;
           *reinterpret_cast<uint4*>(rowp + swz(du, key)) = make_uint4(h[0], h[1], h[2], h[3]);
           *reinterpret_cast<uint4*>(rowp + swz(du + 1, key)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
-      }
-      if (ct < C::SK) {
-        const int k = ct, seg = k >> br_log2, o = k & (br - 1);
-        const __half* ks = reinterpret_cast<const __half*>(st + 2 * C::U8_TILE + seg * 4 * br);
-        const __half* vs = reinterpret_cast<const __half*>(st + 2 * C::U8_TILE + 4 * C::SK + seg * 4 * br);
-        float* side = reinterpret_cast<float*>(fb + 2 * C::F_TILE);
-        side[k] = __half2float(ks[o]) * sl2;
-        side[C::SK + k] = __half2float(ks[br + o]);
-        side[2 * C::SK + k] = __half2float(vs[o]);
-        side[3 * C::SK + k] = __half2float(vs[br + o]);
       }
       fence_proxy_async();  // f16 tiles are read by the tensor cores
       __syncwarp();
@@ -329,10 +330,11 @@ __global__ void __launch_bounds__(256, 1)
     const int hi = si.L + rc / a.G;
     const int lo = a.window > 0 ? hi - a.window + 1 : INT_MIN;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f, zc = 0.f;
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int s = 0; s < n_stages; ++s) {
-      const int sb = s & 1, cb = s % C::NB;
+      const int sb = s & 1;
       if (!mbar_wait(&s_full[sb], (s >> 1) & 1)) {
         ok = false;
         break;
@@ -345,26 +347,18 @@ __global__ void __launch_bounds__(256, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
 
-      const float* side = reinterpret_cast<const float*>(fbuf + cb * C::F_STAGE + 2 * C::F_TILE);
       const int key0 = kstart + s * C::SK;
       const bool clean = key0 >= lo && key0 + C::SK - 1 <= hi;
       float mt = -INFINITY;
 #pragma unroll
-      for (int j4 = 0; j4 < C::SK; j4 += 4) {
-        const float4 ksc = *reinterpret_cast<const float4*>(side + j4);
-        const float4 kzp = *reinterpret_cast<const float4*>(side + C::SK + j4);
-        const float sc4[4] = {ksc.x, ksc.y, ksc.z, ksc.w}, zp4[4] = {kzp.x, kzp.y, kzp.z, kzp.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = j4 + e;
-          float v = (x[j] - zp4[e] * qsum) * sc4[e];
-          if (!clean) {
-            const int key = key0 + j;
-            v = (key >= lo && key <= hi) ? v : -INFINITY;
-          }
-          x[j] = v;
-          mt = fmaxf(mt, v);
+      for (int j = 0; j < C::SK; ++j) {
+        float v = x[j] * sl2;
+        if (!clean) {
+          const int key = key0 + j;
+          v = (key >= lo && key <= hi) ? v : -INFINITY;
         }
+        x[j] = v;
+        mt = fmaxf(mt, v);
       }
       const bool need = (mt > m_ref + 8.f) || (m_ref == -INFINITY && mt != -INFINITY);
       const float m_new = need ? mt : m_ref;
@@ -386,35 +380,14 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
       }
       l *= alpha;
-      zc *= alpha;
       m_ref = m_new;
       const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-      const bool all_in = key0 >= si.klo && key0 + C::SK - 1 <= si.khi;
       uint32_t pk[C::SK / 2];
 #pragma unroll
-      for (int j4 = 0; j4 < C::SK; j4 += 4) {
-        const float4 vsc = *reinterpret_cast<const float4*>(side + 2 * C::SK + j4);
-        const float4 vzp = *reinterpret_cast<const float4*>(side + 3 * C::SK + j4);
-        const float sc4[4] = {vsc.x, vsc.y, vsc.z, vsc.w}, zp4[4] = {vzp.x, vzp.y, vzp.z, vzp.w};
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int j = j4 + e;
-          float s0 = sc4[e], s1 = sc4[e + 1], z0 = zp4[e], z1 = zp4[e + 1];
-          if (!all_in) {  // scales of keys outside every row's range may be NaN
-            const bool in0 = key0 + j >= si.klo && key0 + j <= si.khi;
-            const bool in1 = key0 + j + 1 >= si.klo && key0 + j + 1 <= si.khi;
-            s0 = in0 ? s0 : 0.f;
-            z0 = in0 ? z0 : 0.f;
-            s1 = in1 ? s1 : 0.f;
-            z1 = in1 ? z1 : 0.f;
-          }
-          const float p0 = ex2(x[j] - mu), p1 = ex2(x[j + 1] - mu);
-          l += p0 + p1;
-          const __half2 h = __floats2half2_rn(p0 * s0, p1 * s1);
-          const float2 hr = __half22float2(h);
-          zc += hr.x * z0 + hr.y * z1;
-          pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
-        }
+      for (int j = 0; j < C::SK; j += 2) {
+        const float p0 = ex2(x[j] - mu), p1 = ex2(x[j + 1] - mu);
+        l += p0 + p1;
+        pk[j / 2] = pack2<false>(p0, p1);
       }
       if (s >= 2 && !mbar_wait(&pv_done[sb], ((s >> 1) - 1) & 1)) {
         ok = false;
@@ -442,12 +415,11 @@ __global__ void __launch_bounds__(256, 1)
         if (si.nparts == 1) {
           const float inv = (poisoned || !(l > 0.f)) ? 0.f : 1.f / l;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, (o[e] - zc) * inv);
+          for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, o[e] * inv);
         } else {
           float4* dst = reinterpret_cast<float4*>(a.po + (row * a.num_parts + p) * D + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(o[4 * e] - zc, o[4 * e + 1] - zc, o[4 * e + 2] - zc, o[4 * e + 3] - zc);
+          for (int e = 0; e < 8; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
       }
     }

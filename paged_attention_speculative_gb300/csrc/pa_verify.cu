@@ -52,6 +52,7 @@ int env_kernel_choice() {
     if (s == nullptr) return 0;
     if (std::strcmp(s, "tc") == 0) return 2;
     if (std::strcmp(s, "mma") == 0) return 1;
+    if (std::strcmp(s, "tk") == 0) return 3;
     return 0;
   }();
   return v;
@@ -114,7 +115,19 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
   const int choice = env_kernel_choice();
   // u8 caches take the tensor-memory kernel only when forced (tuning).
-  if (tc_ok && choice != 1 && ((rows >= 8 && tc16) || choice == 2)) {
+  if (tc16 && rows <= 64 && choice == 3) {
+    const int n = rows <= 16 ? 16 : (rows <= 32 ? 32 : 64);
+    bool ok = false;
+    pa::MmaKernelInfo info = pa::tk_info(D, mma_kind(kv), n, &ok);
+    if (ok) {
+      kernel = 3;
+      nt = n;
+      sk = info.stage_keys;
+      smem = info.smem_bytes;
+      ctas_per_sm = info.ctas_per_sm;
+    }
+  }
+  if (kernel == 0 && tc_ok && choice != 1 && ((rows >= 8 && tc16) || choice == 2)) {
     bool ok = false;
     pa::MmaKernelInfo info = pa::tc_info(D, mma_kind(kv), &ok);
     if (ok) {
@@ -289,14 +302,23 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.num_parts = plan.num_partitions;
   const int box_rows = std::min(d->page_size, plan.stage_keys);
   a.box_log2 = ilog2(box_rows);
-  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (plan.kernel == 2 ? 64 : (1 << 30));
+  a.row_cap = plan.kernel == 0   ? pa::kConsumerWarps * 8 * plan.row_tiles
+              : plan.kernel == 2 ? 64
+              : plan.kernel == 3 ? plan.row_tiles
+                                 : (1 << 30);
   a.q_dtype = d->q_dtype;
   a.out_dtype = d->out_dtype;
   a.scale_log2 = c.scale * 1.4426950408889634f;
   const dim3 grid(plan.num_partitions, d->num_kv_heads, d->num_seqs);
 
   cudaError_t e;
-  if (plan.kernel == 2) {
+  if (plan.kernel == 3) {
+    CUtensorMap mk, mv;
+    int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
+    if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
+    if (rc != PA_OK) return rc;
+    e = pa::launch_tk(d->head_dim, mma_kind(c.kv), plan.row_tiles, mk, mv, a, grid, c.stream);
+  } else if (plan.kernel == 2) {
     CUtensorMap mk, mv;
     int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
     if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
@@ -341,7 +363,10 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.window = c.window;
   a.part_tokens = plan.part_tokens;
   a.num_parts = plan.num_partitions;
-  a.row_cap = plan.kernel == 0 ? pa::kConsumerWarps * 8 * plan.row_tiles : (plan.kernel == 2 ? 64 : (1 << 30));
+  a.row_cap = plan.kernel == 0   ? pa::kConsumerWarps * 8 * plan.row_tiles
+              : plan.kernel == 2 ? 64
+              : plan.kernel == 3 ? plan.row_tiles
+                                 : (1 << 30);
   a.out_dtype = d->out_dtype;
   const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
   cudaLaunchConfig_t cfg = {};

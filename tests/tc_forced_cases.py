@@ -1,6 +1,7 @@
-"""Run in a child process with PA_VERIFY_KERNEL=tc: every case below goes
-through the tensor-memory partition kernel; prints one JSON line per case
-with the max abs error against the oracle and the gather-trace check."""
+"""Run in a child process with PA_VERIFY_KERNEL=tc (or tk): every case below
+that the forced kernel accepts goes through that tensor-memory partition
+kernel; prints one JSON line per case with the plan's kernel, the max abs
+error against the oracle and the gather-trace check."""
 import json
 import os
 import sys
@@ -13,7 +14,8 @@ import numpy as np  # noqa: E402
 
 import oracle  # noqa: E402
 from paged_attention_speculative_gb300 import workloads as W  # noqa: E402
-from pa_testing import derived_tolerance, max_abs_err, run_gpu, run_oracle  # noqa: E402
+import paged_attention_speculative_gb300 as pa  # noqa: E402
+from pa_testing import KV_CODE, derived_tolerance, dims, max_abs_err, run_gpu, run_oracle, to_device  # noqa: E402
 
 EDGE = {"tc_window_batch"}  # short contexts (O(1) outputs): derived bf16 bound
 
@@ -40,9 +42,13 @@ CASES = [
 ]
 
 if __name__ == "__main__":
-    assert os.environ.get("PA_VERIFY_KERNEL") == "tc"
+    assert os.environ.get("PA_VERIFY_KERNEL") in ("tc", "tk")
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for make in CASES:
         case = make()
+        plan = pa.plan(dims(case, to_device(case)), case.max_context_len, case.sliding_window, KV_CODE[case.kv_dtype],
+                       sms)
         got, bits, trace = run_gpu(case, traced=True)
         want = run_oracle(case)
         pages = oracle.pages_touched(case.block_tables, case.past_lens, case.subsequence_begins,
@@ -51,5 +57,5 @@ if __name__ == "__main__":
         excess = None
         if case.name in EDGE:
             excess = float(np.max(np.abs(got - want) - derived_tolerance(case, want)))
-        print(json.dumps({"case": case.name, "bits": bits, "err": max_abs_err(got, want), "excess": excess,
+        print(json.dumps({"case": case.name, "kernel": plan.kernel, "bits": bits, "err": max_abs_err(got, want), "excess": excess,
                           "trace_ok": trace_ok}), flush=True)

@@ -1,7 +1,8 @@
-"""The tensor-memory (tcgen05) partition kernel on every shape it accepts:
-a child process forces it (PA_VERIFY_KERNEL=tc) for 1..64 query rows per KV
-head, head_dim 64 / 128, bf16 / f16 and u8 caches, windows and ragged tails, and each case
-is compared with the fp64 oracle (<= 2e-3) and its gather trace bit-exactly."""
+"""The tensor-memory (tcgen05) partition kernels on every shape they accept:
+a child process forces one of them (PA_VERIFY_KERNEL=tc: rows on the MMA's
+M dimension; tk: keys on M) for 1..64 query rows per KV head, head_dim 64 /
+128, bf16 / f16 and u8 caches, windows and ragged tails, and each case is
+compared with the fp64 oracle (<= 2e-3) and its gather trace bit-exactly."""
 import json
 import os
 import subprocess
@@ -15,8 +16,9 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def test_forced_tensor_memory_path_matches_oracle():
-    env = dict(os.environ, PA_VERIFY_KERNEL="tc")
+@pytest.mark.parametrize("kernel", ["tc", "tk"])
+def test_forced_tensor_memory_path_matches_oracle(kernel):
+    env = dict(os.environ, PA_VERIFY_KERNEL=kernel)
     proc = subprocess.run([sys.executable, os.path.join(HERE, "tc_forced_cases.py")], env=env,
                           capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stderr[-3000:]
