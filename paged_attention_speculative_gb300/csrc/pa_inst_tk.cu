@@ -1,6 +1,7 @@
 // Tensor-memory partition kernels with the keys on the MMA's M dimension.
 #include "pa_launch.h"
 #include "pa_partition_tk.cuh"
+#include "pa_partition_tku8.cuh"
 
 namespace pa {
 
@@ -30,7 +31,36 @@ cudaError_t launch_tk_n(int n, const CUtensorMap& k, const CUtensorMap& v, const
   if (n == 64) return launch_tk_t<D, KV, 64>(k, v, a, grid, st);
   return cudaErrorInvalidValue;
 }
+template <int N>
+cudaError_t launch_tku8_t(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid, cudaStream_t st) {
+  auto kern = pa_partition_tku8<N>;
+  const int smem = TkU8Cfg<N>::BYTES;
+  static int configured_for[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !__atomic_load_n(&configured_for[dev], __ATOMIC_ACQUIRE)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
+  }
+  kern<<<grid, 320, smem, st>>>(k, v, a);
+  return cudaGetLastError();
+}
 }  // namespace
+
+MmaKernelInfo tku8_info(int n, bool* ok) {
+  *ok = (n == 16 || n == 32);
+  if (!*ok) return MmaKernelInfo{0, 0, 0};
+  return MmaKernelInfo{TkU8Cfg<16>::HK, n == 16 ? TkU8Cfg<16>::BYTES : TkU8Cfg<32>::BYTES, 1};
+}
+
+cudaError_t launch_tku8(int n, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                        cudaStream_t st) {
+  if (n == 16) return launch_tku8_t<16>(k, v, a, grid, st);
+  if (n == 32) return launch_tku8_t<32>(k, v, a, grid, st);
+  return cudaErrorInvalidValue;
+}
 
 MmaKernelInfo tk_info(int D, int kv, int n, bool* ok) {
   *ok = (D == 64 || D == 128) && (kv == KV_BF16 || kv == KV_F16) && (n == 16 || n == 32 || n == 64);

@@ -40,5 +40,10 @@ cudaError_t launch_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v,
 MmaKernelInfo tk_info(int D, int kv, int n, bool* ok);
 cudaError_t launch_tk(int D, int kv, int n, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                       cudaStream_t st);
+// The same for u8 caches, head_dim 128, row tiles n = 16 / 32 (stage_keys =
+// the u8 half stage, 64 keys).
+MmaKernelInfo tku8_info(int n, bool* ok);
+cudaError_t launch_tku8(int n, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                        cudaStream_t st);
 
 }  // namespace pa

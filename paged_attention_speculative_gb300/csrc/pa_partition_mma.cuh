@@ -129,6 +129,10 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
 
   // =========================== producer warp ===============================
   if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
     // Stage this partition's block ids in one coalesced pass and validate
     // them.  A bad id is reported, clamped to page 0 (so every copy stays in
     // bounds) and the partition's result is discarded after the loop.
@@ -164,37 +168,41 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
       uint8_t* st = smem + slot * C::STAGE;
       if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
       __syncwarp();
-      for (int j = lane; j < nseg * C::CHUNKS; j += 32) {
-        const int seg = j / C::CHUNKS, c = j % C::CHUNKS;
-        const int key = key0 + (seg << br_log2);
-        const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
-        const int id = blk[lp - lp0];
-        const uint32_t off = static_cast<uint32_t>(((seg * C::CHUNKS + c) << br_log2) * 128);
-        tma_load_4d(st + off, &tmK, c * C::ELEMS_128, slot0, g, id, &full[slot]);
-        tma_load_4d(st + C::TILE + off, &tmV, c * C::ELEMS_128, slot0, g, id, &full[slot]);
-        if (a.trace != nullptr && c == 0 && slot0 == 0)
-          atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
-      }
-      if constexpr (C::kU8) {
-        // per segment [scales(br) | zero-points(br)]; one copy when the
-        // segment is a whole page (the record keeps both arrays adjacent)
-        const size_t rec = static_cast<size_t>(a.ps) * (D + 4);
-        for (int j = lane; j < nseg; j += 32) {
-          const int key = key0 + (j << br_log2);
+      // one copy per lane: a copy instruction costs its thread hundreds of
+      // cycles, so copies issued by one lane in a row would pace the stream
+      const int nt = nseg * C::CHUNKS;
+      int ncopy = 2 * nt;
+      if constexpr (C::kU8) ncopy += nseg * (br == a.ps ? 2 : 4);
+      for (int c = lane; c < ncopy; c += 32) {
+        if (c < 2 * nt) {
+          const bool is_v = c >= nt;
+          const int j = is_v ? c - nt : c;
+          const int seg = j / C::CHUNKS, ch = j % C::CHUNKS;
+          const int key = key0 + (seg << br_log2);
+          const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+          const int id = blk[lp - lp0];
+          const uint32_t off = static_cast<uint32_t>(((seg * C::CHUNKS + ch) << br_log2) * 128);
+          tma_load_4d(st + (is_v ? C::TILE : 0) + off, is_v ? &tmV : &tmK, ch * C::ELEMS_128, slot0, g, id, &full[slot]);
+          if (!is_v && a.trace != nullptr && ch == 0 && slot0 == 0)
+            atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
+        } else if constexpr (C::kU8) {
+          // per segment [scales(br) | zero-points(br)]; one copy per cache
+          // when the segment is a whole page (the record keeps both arrays
+          // adjacent), else scales and zero-points separately
+          const size_t rec = static_cast<size_t>(a.ps) * (D + 4);
+          const int idx = c - 2 * nt;
+          const bool whole = (br == a.ps);
+          const int seg = whole ? idx >> 1 : idx >> 2;
+          const bool is_v = whole ? (idx & 1) != 0 : (idx & 2) != 0;
+          const int part = whole ? 0 : (idx & 1);  // 0: scales, 1: zero-points
+          const int key = key0 + (seg << br_log2);
           const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
           const int id = blk[lp - lp0];
           const size_t roff = (static_cast<size_t>(id) * a.Hkv + g) * rec + static_cast<size_t>(a.ps) * D;
-          uint8_t* dk = st + 2 * C::TILE + j * 4 * br;
-          uint8_t* dv = dk + 4 * C::SK;
-          if (br == a.ps) {
-            bulk_load(dk, a.k_bytes + roff, 4 * br, &full[slot]);
-            bulk_load(dv, a.v_bytes + roff, 4 * br, &full[slot]);
-          } else {
-            bulk_load(dk, a.k_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
-            bulk_load(dk + 2 * br, a.k_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
-            bulk_load(dv, a.v_bytes + roff + 2 * slot0, 2 * br, &full[slot]);
-            bulk_load(dv + 2 * br, a.v_bytes + roff + 2 * a.ps + 2 * slot0, 2 * br, &full[slot]);
-          }
+          uint8_t* dst = st + 2 * C::TILE + seg * 4 * br + (is_v ? 4 * C::SK : 0);
+          const uint8_t* src = (is_v ? a.v_bytes : a.k_bytes) + roff;
+          if (whole) bulk_load(dst, src, 4 * br, &full[slot]);
+          else bulk_load(dst + 2 * br * part, src + 2 * a.ps * part + 2 * slot0, 2 * br, &full[slot]);
         }
       }
       issued = s + 1;

@@ -262,6 +262,10 @@ __global__ void __launch_bounds__(128, 1)
 
   if (warp == 3) {
     // =========================== TMA producer ===============================
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
     int bad = 0;
     for (int j = lane; j < npages; j += 32) {
       int id = __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);

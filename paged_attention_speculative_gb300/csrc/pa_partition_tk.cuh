@@ -226,6 +226,10 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 5) {
     // =========================== TMA producer ===============================
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
     int bad = 0;
     if (prefetch) {
       cp_async_wait_all();

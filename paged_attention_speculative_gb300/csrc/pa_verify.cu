@@ -115,6 +115,18 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
   const int choice = env_kernel_choice();
   // u8 caches take the tensor-memory kernel only when forced (tuning).
+  if (kv == PA_U8 && D == 128 && rows <= 32 && choice == 3) {
+    const int n = rows <= 16 ? 16 : 32;
+    bool ok = false;
+    pa::MmaKernelInfo info = pa::tku8_info(n, &ok);
+    if (ok) {
+      kernel = 4;
+      nt = n;
+      sk = info.stage_keys;
+      smem = info.smem_bytes;
+      ctas_per_sm = info.ctas_per_sm;
+    }
+  }
   if (tc16 && rows <= 64 && choice == 3) {
     const int n = rows <= 16 ? 16 : (rows <= 32 ? 32 : 64);
     bool ok = false;
@@ -304,7 +316,7 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.box_log2 = ilog2(box_rows);
   a.row_cap = plan.kernel == 0   ? pa::kConsumerWarps * 8 * plan.row_tiles
               : plan.kernel == 2 ? 64
-              : plan.kernel == 3 ? plan.row_tiles
+              : (plan.kernel == 3 || plan.kernel == 4) ? plan.row_tiles
                                  : (1 << 30);
   a.q_dtype = d->q_dtype;
   a.out_dtype = d->out_dtype;
@@ -312,12 +324,13 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   const dim3 grid(plan.num_partitions, d->num_kv_heads, d->num_seqs);
 
   cudaError_t e;
-  if (plan.kernel == 3) {
+  if (plan.kernel == 3 || plan.kernel == 4) {
     CUtensorMap mk, mv;
     int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
     if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
     if (rc != PA_OK) return rc;
-    e = pa::launch_tk(d->head_dim, mma_kind(c.kv), plan.row_tiles, mk, mv, a, grid, c.stream);
+    e = plan.kernel == 3 ? pa::launch_tk(d->head_dim, mma_kind(c.kv), plan.row_tiles, mk, mv, a, grid, c.stream)
+                         : pa::launch_tku8(plan.row_tiles, mk, mv, a, grid, c.stream);
   } else if (plan.kernel == 2) {
     CUtensorMap mk, mv;
     int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
@@ -365,7 +378,7 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.num_parts = plan.num_partitions;
   a.row_cap = plan.kernel == 0   ? pa::kConsumerWarps * 8 * plan.row_tiles
               : plan.kernel == 2 ? 64
-              : plan.kernel == 3 ? plan.row_tiles
+              : (plan.kernel == 3 || plan.kernel == 4) ? plan.row_tiles
                                  : (1 << 30);
   a.out_dtype = d->out_dtype;
   const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
