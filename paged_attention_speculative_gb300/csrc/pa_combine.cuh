@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine(const CombineAr
   const SeqInfo si = seq_info(a.begins, a.past_lens, lo, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
                               a.part_tokens, a.row_cap);
   pdl_wait_primary();
+  pdl_launch_dependents();  // the next step's partition kernel may start its launch
   if (si.err || si.T <= 0 || t < si.t0 || t >= si.t0 + si.T) {
     // malformed metadata: the partition kernel reported it; leave zeros
     for (int d = threadIdx.x; d < D; d += blockDim.x) store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + d, 0.f);

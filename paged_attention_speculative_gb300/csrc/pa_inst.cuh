@@ -26,8 +26,7 @@ cudaError_t launch_mma_t(const CUtensorMap& k, const CUtensorMap& v, const PartA
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  kern<<<grid, kThreads, smem, st>>>(k, v, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(kThreads), smem, st, k, v, a);
 }
 
 }  // namespace pa

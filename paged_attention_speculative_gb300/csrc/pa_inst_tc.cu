@@ -19,8 +19,7 @@ cudaError_t launch_tc_t(const CUtensorMap& k, const CUtensorMap& v, const PartAr
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  kern<<<grid, 128, smem, st>>>(k, v, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(128), smem, st, k, v, a);
 }
 cudaError_t launch_tcu8_128(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                             cudaStream_t st) {
@@ -35,8 +34,7 @@ cudaError_t launch_tcu8_128(const CUtensorMap& k, const CUtensorMap& v, const Pa
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  kern<<<grid, 256, smem, st>>>(k, v, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(256), smem, st, k, v, a);
 }
 }  // namespace
 

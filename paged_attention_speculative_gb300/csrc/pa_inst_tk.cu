@@ -19,8 +19,7 @@ cudaError_t launch_tk_t(const CUtensorMap& k, const CUtensorMap& v, const PartAr
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  kern<<<grid, 192, smem, st>>>(k, v, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(192), smem, st, k, v, a);
 }
 
 template <int D, int KV>
@@ -44,8 +43,7 @@ cudaError_t launch_tku8_t(const CUtensorMap& k, const CUtensorMap& v, const Part
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  kern<<<grid, 320, smem, st>>>(k, v, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(320), smem, st, k, v, a);
 }
 }  // namespace
 

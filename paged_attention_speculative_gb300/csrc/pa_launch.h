@@ -9,6 +9,26 @@
 
 namespace pa {
 
+// Launch with programmatic dependent launch: the grid may start while the
+// stream's previous kernel is finishing.  Every partition kernel executes
+// griddepcontrol.wait before it touches global memory, so only its launch
+// and set-up overlap the previous kernel.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Static facts about one tensor-core partition kernel instantiation.
 struct MmaKernelInfo {
   int stage_keys;   // keys per pipeline stage

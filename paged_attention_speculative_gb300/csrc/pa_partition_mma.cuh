@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
 
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
                               a.part_tokens, a.row_cap);
   pdl_launch_dependents();

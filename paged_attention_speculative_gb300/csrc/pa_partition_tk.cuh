@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(192, 1)
 
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so the producer starts fetching its
   // block-table slice before the sequence's bounds are known.

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(320, 1)
 
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   const bool prefetch = (warp == 9 && a.window == 0);
   if (prefetch) {
     const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;

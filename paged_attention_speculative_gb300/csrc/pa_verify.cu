@@ -347,10 +347,9 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
     else if (d->head_dim == 128) e = pa::launch_mma_d128(kind, plan.row_tiles, mk, mv, a, grid, c.stream);
     else e = pa::launch_mma_d256(kind, plan.row_tiles, mk, mv, a, grid, c.stream);
   } else {
-    if (d->head_dim == 64) pa::pa_partition_f32<64><<<grid, 128, 0, c.stream>>>(a);
-    else if (d->head_dim == 128) pa::pa_partition_f32<128><<<grid, 128, 0, c.stream>>>(a);
-    else pa::pa_partition_f32<256><<<grid, 128, 0, c.stream>>>(a);
-    e = cudaGetLastError();
+    if (d->head_dim == 64) e = pa::launch_dependent(pa::pa_partition_f32<64>, grid, dim3(128), 0, c.stream, a);
+    else if (d->head_dim == 128) e = pa::launch_dependent(pa::pa_partition_f32<128>, grid, dim3(128), 0, c.stream, a);
+    else e = pa::launch_dependent(pa::pa_partition_f32<256>, grid, dim3(128), 0, c.stream, a);
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
