@@ -92,9 +92,23 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
+  // Without a window a partition's first page is p * part_tokens / page_size
+  // whatever the sequence's length, so the producer starts fetching its
+  // block-table slice before the sequence's bounds are known.
+  const bool prefetch = (warp == kConsumerWarps && a.window == 0);
+  if (prefetch) {
+    const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
+    const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
+                                       max(0LL, static_cast<long long>(a.max_blocks) - lpg)));
+    const int32_t* src = a.block_tables + static_cast<size_t>(b) * a.max_blocks + lpg;
+    for (int j = lane; j < n; j += 32) cp_async4(blk + j, src + j);
+  }
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
                               a.part_tokens, a.row_cap);
   pdl_launch_dependents();
+  if (si.err || si.T <= 0 || p >= si.nparts) {
+    if (prefetch) cp_async_wait_all();  // no copy into shared memory outlives the CTA
+  }
 
   if (si.err) {
     if (p == 0 && threadIdx.x == 0) atomicOr(a.status, si.err);
@@ -138,8 +152,12 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     // them.  A bad id is reported, clamped to page 0 (so every copy stays in
     // bounds) and the partition's result is discarded after the loop.
     int bad = 0;
+    if (prefetch) {
+      cp_async_wait_all();
+      __syncwarp();
+    }
     for (int j = lane; j < npages; j += 32) {
-      int id = __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+      int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
       if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
         bad = 1;
         id = 0;

@@ -181,9 +181,23 @@ __global__ void __launch_bounds__(128, 1)
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
+  // Without a window a partition's first page is p * part_tokens / page_size
+  // whatever the sequence's length, so the producer starts fetching its
+  // block-table slice before the sequence's bounds are known.
+  const bool prefetch = (warp == 3 && a.window == 0);
+  if (prefetch) {
+    const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
+    const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
+                                       max(0LL, static_cast<long long>(a.max_blocks) - lpg)));
+    const int32_t* src = a.block_tables + static_cast<size_t>(b) * a.max_blocks + lpg;
+    for (int j = lane; j < n; j += 32) cp_async4(blk + j, src + j);
+  }
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
                               a.part_tokens, a.row_cap);
   pdl_launch_dependents();
+  if (si.err || si.T <= 0 || p >= si.nparts) {
+    if (prefetch) cp_async_wait_all();  // no copy into shared memory outlives the CTA
+  }
   if (si.err) {
     if (p == 0 && threadIdx.x == 0) atomicOr(a.status, si.err);
     if (p == 0 && si.rows_ok) {
@@ -205,8 +219,9 @@ __global__ void __launch_bounds__(128, 1)
   const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
   const int R = si.T * a.G;
 
-  // ---- set-up: barriers, tensor memory, Q tile, zero padding of P ----
-  if (threadIdx.x == 0) {
+  // ---- set-up: barriers; then the producer starts while warps 0-2
+  // allocate tensor memory and stage Q ----
+  if (threadIdx.x == 96) {
     s_bad = 0;
     s_timeout = 0;
     for (int s = 0; s < C::NS; ++s) {
@@ -221,41 +236,44 @@ __global__ void __launch_bounds__(128, 1)
     }
     fence_barrier_init();
   }
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();  // the TMEM address is published
-  tc_fence_after();
-  {
-    // Q rows into TMEM (lane = query row r = token r/G, head g*G + r%G; two
-    // 16-bit elements per column); lanes R..127 zero.  Each warp writes its
-    // own lane quarter.
-    const uint32_t base = s_tmem;
-    const int r = warp * 32 + lane;
-    const bool real = r < R;
-    const size_t row = real ? static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
-    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + row * D);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      uint32_t v[32];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 x = real ? __ldg(src + 8 * c + u) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * u] = x.x;
-        v[4 * u + 1] = x.y;
-        v[4 * u + 2] = x.z;
-        v[4 * u + 3] = x.w;
-      }
-      tmem_st32(base + C::Q_COL + 32 * c + (static_cast<uint32_t>(warp * 32) << 16),
-                reinterpret_cast<const float*>(v));
-    }
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
+  uint32_t tmem = 0;
+  if (warp < 3) {
+    if (warp == 0) {
+      tmem_alloc(&s_tmem, C::TMEM_COLS);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    bar_sync_n(2, 96);  // the TMEM address is published
+    tc_fence_after();
+    tmem = s_tmem;
+    if (warp < 2) {
+      // Q rows into TMEM (lane = query row r = token r/G, head g*G + r%G; two
+      // 16-bit elements per column), lanes R..63 zero.  Lanes 64..127 are
+      // left as they are: they only feed S, P and O rows nobody reads.
+      const int r = warp * 32 + lane;
+      const bool real = r < R;
+      const size_t row = real ? static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + row * D);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = real ? __ldg(src + 8 * c + u) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * u] = x.x;
+          v[4 * u + 1] = x.y;
+          v[4 * u + 2] = x.z;
+          v[4 * u + 3] = x.w;
+        }
+        tmem_st32(tmem + C::Q_COL + 32 * c + (static_cast<uint32_t>(warp * 32) << 16),
+                  reinterpret_cast<const float*>(v));
+      }
+    }
+    tc_fence_before();
+    bar_sync_n(2, 96);  // Q is in place for the MMA warp
+    tc_fence_after();
+  }
   const uint32_t tm_o = tmem;                      // O
   const uint32_t tm_s0 = tmem + C::S_COL;          // S buffers
   const uint32_t tm_p0 = tmem + C::P_COL;          // P buffers (16-bit pairs)
@@ -268,8 +286,12 @@ __global__ void __launch_bounds__(128, 1)
       prefetch_tensormap(&tmV);
     }
     int bad = 0;
+    if (prefetch) {
+      cp_async_wait_all();
+      __syncwarp();
+    }
     for (int j = lane; j < npages; j += 32) {
-      int id = __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+      int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
       if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
         bad = 1;
         id = 0;

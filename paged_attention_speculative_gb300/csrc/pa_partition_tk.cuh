@@ -36,22 +36,6 @@
 
 namespace pa {
 
-// Barrier-reduction over the `n` threads of named barrier `id`: true when the
-// predicate holds on any of them (all of them wait for each other).
-__device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void bar_sync_n(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(
