@@ -176,6 +176,23 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   part = std::min(part, round_up(span, quantum));
   const long long page_cap = (static_cast<long long>(pa::kMaxPagesPerCta - 1) * ps / quantum) * quantum;
   part = std::min(part, std::max(page_cap, quantum));
+  if (env_part_tokens() <= 0) {
+    // Rounding can leave a last wave of CTAs that is mostly empty; a larger
+    // partition that needs fewer waves is then cheaper.  Cost = waves x keys
+    // per CTA, the serial work of the busiest CTA slot.
+    const long long cap = std::min(round_up(span, quantum), std::max(page_cap, quantum));
+    auto cost = [&](long long pt) { return ceil_div(ceil_div(span, pt) * units, target) * pt; };
+    long long best = part, best_cost = cost(part);
+    for (long long cand = part + quantum; cand <= cap && ceil_div(ceil_div(span, best) * units, target) > 1;
+         cand += quantum) {
+      const long long c = cost(cand);
+      if (c < best_cost) {
+        best = cand;
+        best_cost = c;
+      }
+    }
+    part = best;
+  }
   const long long P = ceil_div(span, part);
   if (P > 65535 || P * units > (1LL << 31)) return PA_ERR_UNSUPPORTED;
 
