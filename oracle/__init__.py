@@ -4,8 +4,10 @@ Only the test suite, the package smoke test and the benchmark's CPU-baseline
 leg may import this package.  The product library never imports it, and it
 imports nothing from the product: it restates the storage layouts itself.
 
-`pa_oracle.c` holds the definition (plain C, fp64, one output row per work
-item, OpenMP over rows).  This module compiles it with gcc on first use into
+`pa_oracle.c` holds the definitions: the verify attention (plain C, fp64,
+one output row per work item, OpenMP over rows) and the cache update that
+precedes it (writing the new tokens' K/V into their pages; u8 caches get a
+per-token binary32 min/max quantisation).  This module compiles it with gcc on first use into
 ``oracle/_build/`` and calls it through ctypes.
 
 Parity status: every function here is pinned by the CPU tests in
@@ -56,6 +58,8 @@ def _load():
             lib.pa_oracle_forward.restype = ci
             lib.pa_oracle_pages_touched.argtypes = [i32p, i32p, i32p, ci, ci, ci, ci, i32p]
             lib.pa_oracle_pages_touched.restype = ci
+            lib.pa_oracle_cache_update.argtypes = [vp, vp, ci, vp, vp, ci, i32p, i32p, i32p, ci, ci, ci, ci, ci, ci]
+            lib.pa_oracle_cache_update.restype = ci
             lib.pa_oracle_max_threads.argtypes = []
             lib.pa_oracle_max_threads.restype = ci
             _lib = lib
@@ -121,3 +125,27 @@ def pages_touched(block_tables, past_lens, subsequence_begins, *, page_size: int
     if rc != 0:
         raise ValueError("oracle: key range runs past the block table")
     return out
+
+
+def cache_update(k_new_raw: np.ndarray, v_new_raw: np.ndarray, src_dtype: str, k_cache_raw: np.ndarray,
+                 v_cache_raw: np.ndarray, kv_dtype: str, block_tables, past_lens, subsequence_begins, *,
+                 num_kv_heads: int, head_dim: int, page_size: int, num_blocks: int):
+    """The cache-update definition (pa_oracle.c): returns new copies of the two
+    caches with the new tokens written.  Arrays hold stored bits, as in
+    forward(); k_new / v_new are [total_tokens, Hkv, D].  Raises ValueError on
+    inconsistent inputs."""
+    lib = _load()
+    k_new_raw = np.ascontiguousarray(k_new_raw)
+    v_new_raw = np.ascontiguousarray(v_new_raw)
+    kc = np.array(k_cache_raw, copy=True, order="C")
+    vc = np.array(v_cache_raw, copy=True, order="C")
+    bt = _i32(block_tables)
+    pl = _i32(past_lens)
+    sb = _i32(subsequence_begins)
+    rc = lib.pa_oracle_cache_update(k_new_raw.ctypes.data, v_new_raw.ctypes.data, DTYPE_CODES[src_dtype],
+                                    kc.ctypes.data, vc.ctypes.data, DTYPE_CODES[kv_dtype], _ptr_i32(bt),
+                                    _ptr_i32(pl), _ptr_i32(sb), pl.shape[0], num_kv_heads, head_dim, page_size,
+                                    num_blocks, bt.shape[1])
+    if rc != 0:
+        raise ValueError("oracle: inconsistent cache-update inputs")
+    return kc, vc

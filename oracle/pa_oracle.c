@@ -234,6 +234,159 @@ int pa_oracle_pages_touched(const int32_t* block_tables, const int32_t* past_len
   return 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * The cache update: the step just before the verify (the OpenVINO
+ * paged-attention op writes the new tokens' K/V into the cache itself, issue
+ * 38153 "Step-by-step reproduction" step 3; u8 KV cache precision, step 1).
+ *
+ * Token i of sequence b goes to position p = past_len_b + i: page
+ * block_tables[b][p / ps], slot p % ps, for every KV head, K and V alike.
+ *  - float caches: the value rounded to nearest-even in the cache dtype;
+ *  - u8 caches, per token and KV head over its D values x (binary32, every
+ *    operation rounded to nearest-even):
+ *        mn = min x, mx = max x
+ *        scale = fp16(  (mx - mn) / 255  )        1.0 if that is 0 or not finite
+ *        zp    = fp16(  -mn / scale  )            (any fp16 value)
+ *        code  = clamp(rint(  x / scale + zp  ), 0, 255)
+ *    and the value is read back as (code - zp) * scale.
+ * Only the written slots change.
+ * ------------------------------------------------------------------------- */
+
+/* binary32 -> binary16 bits, round to nearest-even (overflow to inf). */
+static uint16_t float_to_half_rn(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  const uint32_t expo = (u >> 23) & 0xffu;
+  uint32_t mant = u & 0x7fffffu;
+  if (expo == 0xffu) return (uint16_t)(sign | 0x7c00u | (mant ? 0x200u : 0u));
+  /* the value is (1.mant) * 2^(expo-127); binary16 keeps 10 fraction bits */
+  const int e = (int)expo - 127;
+  if (e > 15) return (uint16_t)(sign | 0x7c00u);
+  if (e >= -14) {
+    /* normal: drop 13 bits with round-to-nearest-even */
+    uint32_t m = mant >> 13, rest = mant & 0x1fffu;
+    uint32_t h = ((uint32_t)(e + 15) << 10) | m;
+    if (rest > 0x1000u || (rest == 0x1000u && (m & 1u))) ++h; /* may carry into the exponent: still correct */
+    return (uint16_t)(sign | h);
+  }
+  /* subnormal (or zero): value = m * 2^-24 with m = (1.mant) * 2^(e+24) */
+  if (e < -25) return sign;
+  if (expo == 0) return sign; /* binary32 subnormals are far below 2^-25 */
+  mant |= 0x800000u;                        /* 24-bit significand, value = mant * 2^(e-23) */
+  const int shift = -e - 1;                 /* mant * 2^(e-23) / 2^-24 = mant >> (-1 - e) */
+  uint32_t m = mant >> shift;
+  uint32_t rest = mant & ((1u << shift) - 1u), half = 1u << (shift - 1);
+  if (rest > half || (rest == half && (m & 1u))) ++m;
+  return (uint16_t)(sign | m);
+}
+
+/* binary32 -> bfloat16 bits, round to nearest-even (NaN kept quiet). */
+static uint16_t float_to_bf16_rn(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x7fffffu)) return (uint16_t)((u >> 16) | 0x40u);
+  const uint32_t rest = u & 0xffffu, keep = u >> 16;
+  uint32_t r = keep;
+  if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) ++r;
+  return (uint16_t)r;
+}
+
+static float load_src(const void* base, int dtype, size_t idx) {
+  return (float)load_float(base, dtype, idx); /* f32 / f16 / bf16 values are binary32-exact */
+}
+
+static void store_float(void* base, int dtype, size_t idx, float v) {
+  if (dtype == OR_F32) {
+    memcpy((char*)base + idx * 4, &v, 4);
+  } else {
+    const uint16_t h = dtype == OR_F16 ? float_to_half_rn(v) : float_to_bf16_rn(v);
+    memcpy((char*)base + idx * 2, &h, 2);
+  }
+}
+
+/* One token's D values of one KV head into slot `slot` of record `rec`. */
+static void quantize_u8_slot(const float* x, int D, int ps, int slot, unsigned char* rec) {
+  float mn = x[0], mx = x[0];
+  for (int d = 1; d < D; ++d) {
+    if (x[d] < mn) mn = x[d];
+    if (x[d] > mx) mx = x[d];
+  }
+  const float range = mx - mn;
+  const float s32 = range / 255.0f;
+  uint16_t s16 = float_to_half_rn(s32);
+  float sf = (float)half_to_double(s16);
+  if (!(sf > 0.0f) || isinf(sf)) {
+    s16 = 0x3c00u; /* 1.0 */
+    sf = 1.0f;
+  }
+  const float zq = -mn / sf;
+  const uint16_t z16 = float_to_half_rn(zq);
+  const float zf = (float)half_to_double(z16);
+  for (int d = 0; d < D; ++d) {
+    const float t = x[d] / sf;
+    const float u = t + zf;
+    float c = rintf(u);
+    if (!(c >= 0.0f)) c = 0.0f; /* also NaN */
+    if (c > 255.0f) c = 255.0f;
+    rec[(size_t)slot * D + d] = (unsigned char)c;
+  }
+  memcpy(rec + (size_t)ps * D + 2 * (size_t)slot, &s16, 2);
+  memcpy(rec + (size_t)ps * D + 2 * (size_t)ps + 2 * (size_t)slot, &z16, 2);
+}
+
+/*
+ * pa_oracle_cache_update: the definition above.  k_new / v_new are
+ * [total_tokens, Hkv, D] in src_dtype (0 f32, 1 f16, 2 bf16); the caches use
+ * the layouts of pa_oracle_forward.  Returns 0, or -1 on inconsistent inputs
+ * (bad begins, a position beyond the block table, a block id outside
+ * [0, num_blocks)); nothing is written then.
+ */
+int pa_oracle_cache_update(const void* k_new, const void* v_new, int src_dtype, void* k_cache, void* v_cache,
+                           int kv_dtype, const int32_t* block_tables, const int32_t* past_lens,
+                           const int32_t* subsequence_begins, int num_seqs, int Hkv, int D, int ps,
+                           int num_blocks, int max_blocks_per_seq) {
+  /* validate everything first so that a rejected call writes nothing */
+  for (int b = 0; b < num_seqs; ++b) {
+    const int t0 = subsequence_begins[b], t1 = subsequence_begins[b + 1];
+    if (t0 < 0 || t1 < t0 || past_lens[b] < 0) return -1;
+    for (int i = 0; i < t1 - t0; ++i) {
+      const long p = (long)past_lens[b] + i;
+      if (p / ps >= max_blocks_per_seq) return -1;
+      const int blk = block_tables[(size_t)b * max_blocks_per_seq + p / ps];
+      if (blk < 0 || blk >= num_blocks) return -1;
+    }
+  }
+  float* x = (float*)malloc(sizeof(float) * (size_t)D);
+  if (!x) return -1;
+  for (int b = 0; b < num_seqs; ++b) {
+    const int t0 = subsequence_begins[b], t1 = subsequence_begins[b + 1];
+    for (int i = 0; i < t1 - t0; ++i) {
+      const long p = (long)past_lens[b] + i;
+      const int blk = block_tables[(size_t)b * max_blocks_per_seq + p / ps];
+      const int slot = (int)(p % ps);
+      const size_t t = (size_t)(t0 + i);
+      for (int g = 0; g < Hkv; ++g) {
+        for (int which = 0; which < 2; ++which) {
+          const void* src = which ? v_new : k_new;
+          void* cache = which ? v_cache : k_cache;
+          const size_t sbase = (t * Hkv + g) * (size_t)D;
+          if (kv_dtype != OR_U8) {
+            const size_t cbase = (((size_t)blk * Hkv + g) * ps + slot) * (size_t)D;
+            for (int d = 0; d < D; ++d) store_float(cache, kv_dtype, cbase + d, load_src(src, src_dtype, sbase + d));
+          } else {
+            for (int d = 0; d < D; ++d) x[d] = load_src(src, src_dtype, sbase + d);
+            unsigned char* rec = (unsigned char*)cache + ((size_t)blk * Hkv + g) * (size_t)ps * (D + 4);
+            quantize_u8_slot(x, D, ps, slot, rec);
+          }
+        }
+      }
+    }
+  }
+  free(x);
+  return 0;
+}
+
 int pa_oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

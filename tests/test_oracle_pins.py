@@ -390,3 +390,153 @@ def test_workload_families_have_stated_shapes():
     assert a.num_seqs == 8 and a.sliding_window == 1024
     assert ((a.query_lens >= 1) & (a.query_lens <= 4)).all()
     assert ((a.past_lens >= 2000) & (a.past_lens <= 4000)).all()
+
+
+# ---------------------------------------------------------------------------
+# Cache update (the step before the verify: the new tokens' K/V written into
+# their pages, with per-token u8 quantisation for u8 caches).
+# ---------------------------------------------------------------------------
+def _cu_layout(D=4, ps=4, num_blocks=1):
+    return dict(num_kv_heads=1, head_dim=D, page_size=ps, num_blocks=num_blocks)
+
+
+def _cu_one_token(oracle, x, kv_dtype, D=4, ps=4):
+    """Write one f32 token x (K = V = x) at slot 1 of the only page."""
+    kn = np.asarray(x, dtype=np.float32).reshape(1, 1, D)
+    if kv_dtype == "u8":
+        cache = np.zeros((1, 1, ps * (D + 4)), dtype=np.uint8)
+    elif kv_dtype == "f32":
+        cache = np.zeros((1, 1, ps, D), dtype=np.float32)
+    else:
+        cache = np.zeros((1, 1, ps, D), dtype=np.uint16)
+    kc, vc = oracle.cache_update(kn, kn, "f32", cache, cache, kv_dtype, [[0]], [1], [0, 1], **_cu_layout(D, ps))
+    assert np.array_equal(kc, vc)
+    return kc
+
+
+def _u8_slot(rec, slot, D, ps):
+    rec = rec.reshape(-1)
+    codes = rec[slot * D:(slot + 1) * D]
+    scale = rec[ps * D + 2 * slot: ps * D + 2 * slot + 2].view(np.uint16)[0]
+    zp = rec[ps * D + 2 * ps + 2 * slot: ps * D + 2 * ps + 2 * slot + 2].view(np.uint16)[0]
+    return codes, int(scale), int(zp)
+
+
+def test_cache_update_u8_hand_worked(oracle_mod):
+    g = json.load(open(os.path.join(os.path.dirname(GOLDEN), "cache_update.json")))
+    for case in g["u8"]:
+        rec = _cu_one_token(oracle_mod, case["x"], "u8")
+        codes, s, z = _u8_slot(rec, 1, 4, 4)
+        assert s == case["scale_bits"] and z == case["zp_bits"], case["name"]
+        assert codes.tolist() == case["codes"], case["name"]
+        # the other slots are untouched
+        assert not rec.reshape(-1)[:4].any() and not rec.reshape(-1)[8:16].any()
+
+
+def test_cache_update_float_rounding_hand_worked(oracle_mod):
+    g = json.load(open(os.path.join(os.path.dirname(GOLDEN), "cache_update.json")))
+    for kv in ("f16", "bf16"):
+        for case in g[kv]:
+            x = np.array([case["x_f32_bits"]] * 4, dtype=np.uint32).view(np.float32)
+            c = _cu_one_token(oracle_mod, x, kv)
+            assert c[0, 0, 1].tolist() == [case["bits"]] * 4, (kv, case)
+    x = np.array([0.1, -2.5, 3e-30, 7.0], dtype=np.float32)
+    assert np.array_equal(_cu_one_token(oracle_mod, x, "f32")[0, 0, 1], x)  # f32 caches store the value itself
+
+
+def test_cache_update_u8_properties(oracle_mod):
+    """Round trip within half a code (plus the fp16 zero-point's rounding),
+    order preserved, and the extremes at codes 0 and 255."""
+    rng = np.random.default_rng(11)
+    D, ps = 128, 16
+    for trial in range(200):
+        # offsets relative to the spread, so -min / scale stays inside fp16
+        sigma = rng.choice([0.01, 1.0, 30.0])
+        shift = rng.choice([0.0, -5.0, 5.0, 40.0]) * sigma
+        x = (rng.standard_normal(D) * sigma + shift).astype(np.float32)
+        rec = _cu_one_token(oracle_mod, x, "u8", D=D, ps=ps)
+        codes, s, z = _u8_slot(rec, 1, D, ps)
+        sf = float(np.array([s], dtype=np.uint16).view(np.float16)[0])
+        zf = float(np.array([z], dtype=np.uint16).view(np.float16)[0])
+        back = (codes.astype(np.float64) - zf) * sf
+        zp_ulp = float(np.spacing(np.float16(abs(zf)))) if zf != 0 else 0.0
+        bound = (0.5 + zp_ulp / 2 + 1e-3) * sf
+        assert np.max(np.abs(back - x)) <= bound, trial
+        order = np.argsort(x, kind="stable")
+        assert np.all(np.diff(codes[order].astype(int)) >= 0), trial
+        # the extremes sit at codes 0 and 255, give or take the zero-point's
+        # fp16 rounding (at most half its spacing in code units)
+        slack = int(zp_ulp / 2 + 0.5)
+        assert codes[np.argmin(x)] <= slack and codes[np.argmax(x)] >= 255 - slack, trial
+
+
+def test_cache_update_places_tokens_where_the_verify_reads_them(oracle_mod):
+    """f32 cache full of NaN; the update writes T tokens per sequence; the
+    (pinned) attention definition over the updated cache must equal a dense
+    numpy attention over the same keys -- any misplaced token shows as NaN or
+    a wrong value."""
+    rng = np.random.default_rng(12)
+    Hq, Hkv, D, ps = 4, 2, 8, 4
+    past = [5, 0, 9]
+    Ts = [3, 2, 4]
+    begins = np.concatenate([[0], np.cumsum(Ts)]).astype(np.int32)
+    mb = 4
+    nb = 1 + len(past) * mb
+    perm = rng.permutation(nb - 1) + 1
+    bt = perm[: len(past) * mb].reshape(len(past), mb).astype(np.int32)
+    k_dense = [rng.standard_normal((past[b] + Ts[b], Hkv, D)).astype(np.float32) for b in range(len(past))]
+    v_dense = [rng.standard_normal((past[b] + Ts[b], Hkv, D)).astype(np.float32) for b in range(len(past))]
+    kc = np.full((nb, Hkv, ps, D), np.nan, dtype=np.float32)
+    vc = kc.copy()
+    for b in range(len(past)):  # the past keys, placed by hand
+        for j in range(past[b]):
+            kc[bt[b, j // ps], :, j % ps] = k_dense[b][j]
+            vc[bt[b, j // ps], :, j % ps] = v_dense[b][j]
+    k_new = np.concatenate([k_dense[b][past[b]:] for b in range(len(past))])
+    v_new = np.concatenate([v_dense[b][past[b]:] for b in range(len(past))])
+    kc2, vc2 = oracle_mod.cache_update(k_new, v_new, "f32", kc, vc, "f32", bt, past, begins, num_kv_heads=Hkv,
+                                   head_dim=D, page_size=ps, num_blocks=nb)
+    q = rng.standard_normal((int(begins[-1]), Hq, D)).astype(np.float32)
+    got = oracle_mod.forward(q, "f32", kc2, vc2, "f32", bt, past, begins, num_q_heads=Hq, num_kv_heads=Hkv,
+                         head_dim=D, page_size=ps, num_blocks=nb, scale=0.35)
+    G = Hq // Hkv
+    for b in range(len(past)):
+        for i in range(Ts[b]):
+            t = begins[b] + i
+            for h in range(Hq):
+                keys = k_dense[b][: past[b] + i + 1, h // G].astype(np.float64)
+                vals = v_dense[b][: past[b] + i + 1, h // G].astype(np.float64)
+                s = 0.35 * keys @ q[t, h].astype(np.float64)
+                w = np.exp(s - s.max())
+                assert np.allclose(got[t, h], w @ vals / w.sum(), rtol=0, atol=1e-12)
+    # nothing outside the new tokens' slots changed
+    touched = np.zeros(kc.shape[:3], dtype=bool)
+    for b in range(len(past)):
+        for i in range(Ts[b]):
+            j = past[b] + i
+            touched[bt[b, j // ps], :, j % ps] = True
+    assert np.array_equal(np.isnan(kc2[~touched]), np.isnan(kc[~touched]))
+    assert np.array_equal(kc2[~touched & ~np.isnan(kc).any(-1)], kc[~touched & ~np.isnan(kc).any(-1)])
+
+
+def test_cache_update_rejects_inconsistent_inputs(oracle_mod):
+    kn = np.zeros((1, 1, 4), dtype=np.float32)
+    cache = np.zeros((2, 1, 4, 4), dtype=np.float32)
+    with pytest.raises(ValueError):  # block id out of range
+        oracle_mod.cache_update(kn, kn, "f32", cache, cache, "f32", [[5]], [0], [0, 1], num_kv_heads=1, head_dim=4,
+                            page_size=4, num_blocks=2)
+    with pytest.raises(ValueError):  # position beyond the block table
+        oracle_mod.cache_update(kn, kn, "f32", cache, cache, "f32", [[0]], [4], [0, 1], num_kv_heads=1, head_dim=4,
+                            page_size=4, num_blocks=2)
+
+
+def test_cache_update_u8_zero_point_overflow_is_visible(oracle_mod):
+    """A token clustered far from zero (|min| above ~257 x its range) needs a
+    zero-point beyond fp16: it rounds to -inf and the slot reads back
+    non-finite instead of silently wrong."""
+    x = np.float32(40.0) + np.linspace(-0.01, 0.01, 8, dtype=np.float32)
+    rec = _cu_one_token(oracle_mod, x, "u8", D=8, ps=4)
+    codes, s, z = _u8_slot(rec, 1, 8, 4)
+    assert z == 0xFC00 and not codes.any()
+    sf = float(np.array([s], dtype=np.uint16).view(np.float16)[0])
+    assert not np.isfinite((codes.astype(np.float64) - (-np.inf)) * sf).any()
