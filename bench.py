@@ -122,6 +122,12 @@ class DeviceWorkload:
                 vis += p - lo + 1
         self.flops = 4 * D * G * Hkv * vis
         self.total_device_bytes = sum(t.numel() * t.element_size() for t in (self.k, self.v))
+        # the new tokens' K / V for the cache update (bf16, like a projection's output)
+        self.k_new = torch.randn((self.T_total, Hkv, D), generator=gd, device="cuda").to(torch.bfloat16)
+        self.v_new = torch.randn((self.T_total, Hkv, D), generator=gd, device="cuda").to(torch.bfloat16)
+        # bytes one update moves: both new-token tensors read, their slots written
+        slot_bytes = D + 4 if kv == "u8" else D * eb
+        self.update_bytes = 2 * self.T_total * Hkv * (D * 2 + slot_bytes)
 
     def _u8_pool(self, nb, gd):
         import torch
@@ -149,6 +155,11 @@ class DeviceWorkload:
         import paged_attention_speculative_gb300 as pa
         pa.partition(self.q, self.k, self.v, self.block_tables[r], self.past_lens, self.begins, self.max_ctx,
                      self.scale, self.window, self.kv_code, self.out, self.dims, self.ws, stream=stream)
+
+    def cache_update(self, r, stream=None):
+        import paged_attention_speculative_gb300 as pa
+        pa.cache_update(self.k_new, self.v_new, self.k, self.v, self.block_tables[r], self.past_lens, self.begins,
+                        self.dims, stream=stream)
 
     def combine(self, stream=None):
         import paged_attention_speculative_gb300 as pa
@@ -238,6 +249,31 @@ def time_graph(wl, steps, warmup, stream, min_seconds=0.0):
             if time.time() - t_start >= min_seconds and len(trials) >= 3:
                 break
     return statistics.median(trials), exact, trials
+
+
+def time_calls(fn, replicas, stream, reps=64, trials=20):
+    """Median device time (µs) of one fn(r) call: a CUDA graph of `reps`
+    back-to-back calls rotating r over the replicas, replayed between two
+    events on the launching stream."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for r in range(min(replicas, reps)):
+            fn(r)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                fn(r % replicas)
+        res = []
+        for _ in range(trials):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            res.append(e0.elapsed_time(e1) * 1e3 / reps)
+    return statistics.median(res)
 
 
 def time_partition_kernel(wl, steps, stream):
@@ -578,6 +614,27 @@ def run_ours(args, rank, world):
         if len(mix) == 2:
             mix[0]["ratio_vs_T1"] = round(mix[0]["us_per_step"] / mix[1]["us_per_step"], 3)
 
+    # The cache update (the step before the verify: the new tokens' K/V into
+    # their pages) alone, and followed by the verify step.
+    cache_update = []
+    if not args.no_sweep and rank == 0:
+        cfgs = [("qwen_gqa_T4_L32768", 32, 8, 128, 16, "bf16", [4], [32768]),
+                ("qwen_u8_T3_L32768", 32, 8, 128, 16, "u8", [3], [32768]),
+                ("batch64_T4_L4096_bf16", 32, 8, 128, 16, "bf16", [4] * 64, [4096] * 64),
+                ("batch64_T4_L4096_u8", 32, 8, 128, 16, "u8", [4] * 64, [4096] * 64)]
+        for name, hq, hkv, d, ps, kvd, qs, ls in cfgs:
+            w = DeviceWorkload(hq, hkv, d, ps, kvd, qs, ls, 0, min_bytes=2 * L2, seed=9)
+            u_upd = time_calls(lambda r: w.cache_update(r, stream), w.replicas, stream)
+            u_step = time_calls(lambda r: (w.cache_update(r, stream), w.forward(r, stream)), w.replicas, stream)
+            u_fwd = time_calls(lambda r: w.forward(r, stream), w.replicas, stream)
+            cache_update.append({"workload": name, "update_us": round(u_upd, 2), "update_bytes": w.update_bytes,
+                                 "update_gbs": round(w.update_bytes / (u_upd * 1e-6) / 1e9, 1),
+                                 "update_frac_of_measured_hbm": round(w.update_bytes / (u_upd * 1e-6) / 1e9 / hbm_peak, 4),
+                                 "update_then_verify_us": round(u_step, 2), "verify_us": round(u_fwd, 2)})
+            log(f"[bench] cache update {cache_update[-1]}")
+            del w
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, per, n, cores = time_oracle(H["q_lens"][0], H["past"][0], args.cpu_seconds)
@@ -613,6 +670,7 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "gpu_launches": exact * wl.launches_per_step(),
         "sweep": sweep,
+        "cache_update": cache_update,
     }
     print(json.dumps(line), flush=True)
 

@@ -211,6 +211,48 @@ int pa_verify_forward_no_alloc(const void* q, const void* k_cache, const void* v
                                float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out,
                                const pa_dims* dims, void* cuda_stream);
 
+/*
+ * pa_cache_update — the step just before the verify: write the new tokens'
+ * K and V into their pages (the OpenVINO paged-attention op stores the new
+ * tokens itself, issue 38153 "Step-by-step reproduction" step 3; u8 KV cache
+ * precision, step 1).  After it, pa_verify_forward with the same past_lens /
+ * subsequence_begins / block tables reads these tokens as keys
+ * past_len_b .. past_len_b + T_b - 1.
+ *
+ *  k_new, v_new   [total_tokens, Hkv, head_dim] in src_dtype (F32, F16, BF16),
+ *                 rows ordered by subsequence_begins.
+ *  k_cache, v_cache  the caches, in kv_dtype, layouts as above; only the new
+ *                 tokens' slots are written (for u8 also their scale and
+ *                 zero-point entries).
+ *  block_tables, past_lens, subsequence_begins  as for pa_verify_forward:
+ *                 token i of sequence b goes to position p = past_lens[b] + i,
+ *                 page block_tables[b][p / page_size], slot p % page_size.
+ *  dims           num_seqs, total_tokens, num_kv_heads, head_dim (64/128/256;
+ *                 u8: 128/256), page_size, num_blocks, max_blocks_per_seq are
+ *                 used; num_q_heads, q_dtype and out_dtype are ignored.
+ *  status         optional device uint32 (NULL: none).  A token whose slot
+ *                 cannot be addressed (malformed begins, negative past_len, a
+ *                 position beyond the block table, a block id outside
+ *                 [0, num_blocks)) is skipped and sets PA_STATUS_BEGINS /
+ *                 PA_STATUS_PAST_LEN / PA_STATUS_CONTEXT / PA_STATUS_BLOCK_ID.
+ *
+ * Float caches store each value rounded to nearest-even in kv_dtype.  u8
+ * caches store, per token and KV head (separately for K and V), with every
+ * binary32 operation rounded to nearest-even:
+ *     scale = fp16((max - min) / 255)   (1.0 when that is 0 or not finite)
+ *     zp    = fp16((0 - min) / scale)
+ *     code  = clamp(rint(x / scale + zp), 0, 255)
+ * so that (code - zp) * scale is within about half a code of x.  A token
+ * whose values cluster far from zero (|min| above ~257 x (max - min))
+ * overflows the fp16 zero-point and reads back non-finite.  Inputs are
+ * expected finite.  The pages name the u8 precision only; this encoding is
+ * the library's.  Asynchronous on cuda_stream (launched with programmatic
+ * dependent launch); pointers 16-byte aligned (int32 arrays and status: 4). */
+int pa_cache_update(const void* k_new, const void* v_new, pa_dtype src_dtype, void* k_cache, void* v_cache,
+                    pa_dtype kv_dtype, const int32_t* block_tables, const int32_t* past_lens,
+                    const int32_t* subsequence_begins, const pa_dims* dims, uint32_t* status,
+                    void* cuda_stream);
+
 /* Synchronises cuda_stream, then reads and clears the workspace's status word
  * into *bits (PA_STATUS_* flags, 0 = clean). */
 int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits);

@@ -246,7 +246,7 @@ int pa_oracle_pages_touched(const int32_t* block_tables, const int32_t* past_len
  *    operation rounded to nearest-even):
  *        mn = min x, mx = max x
  *        scale = fp16(  (mx - mn) / 255  )        1.0 if that is 0 or not finite
- *        zp    = fp16(  -mn / scale  )            (any fp16 value)
+ *        zp    = fp16(  (0 - mn) / scale  )       (any fp16 value)
  *        code  = clamp(rint(  x / scale + zp  ), 0, 255)
  *    and the value is read back as (code - zp) * scale.
  * Only the written slots change.
@@ -320,7 +320,7 @@ static void quantize_u8_slot(const float* x, int D, int ps, int slot, unsigned c
     s16 = 0x3c00u; /* 1.0 */
     sf = 1.0f;
   }
-  const float zq = -mn / sf;
+  const float zq = (0.0f - mn) / sf; /* 0 - mn: a -0 minimum gives +0, whatever order found it */
   const uint16_t z16 = float_to_half_rn(zq);
   const float zf = (float)half_to_double(z16);
   for (int d = 0; d < D; ++d) {

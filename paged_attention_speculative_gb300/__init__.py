@@ -8,7 +8,8 @@ fallback: if the library is missing, loading raises.
 
 Entry points mirror the C ABI:
   forward / forward_traced / partition / combine / workspace_size / plan /
-  device_status / status_string
+  device_status / status_string, and cache_update (the step before the
+  verify: the new tokens' K/V written into their pages)
 Tensors are torch CUDA tensors (torch supplies device memory and streams).
 """
 from __future__ import annotations
@@ -19,7 +20,7 @@ import threading
 
 __all__ = ["PA_F32", "PA_F16", "PA_BF16", "PA_U8", "PaDims", "PaPlan", "load_library", "library_path",
            "forward", "forward_traced", "partition", "combine", "workspace_size", "plan", "device_status",
-           "status_string", "dims_for", "PaVerifyError"]
+           "status_string", "dims_for", "cache_update", "PaVerifyError"]
 
 PA_F32, PA_F16, PA_BF16, PA_U8 = 0, 1, 2, 3
 PA_MAX_QUERY_LEN = 8
@@ -27,7 +28,7 @@ STATUS_BITS = {0x1: "QUERY_LEN", 0x2: "CONTEXT", 0x4: "BLOCK_ID", 0x8: "BEGINS",
                0x20: "ROWS", 0x40: "TIMEOUT"}
 EXPORTED = ["pa_verify_workspace_size", "pa_verify_plan", "pa_verify_forward", "pa_verify_forward_traced",
             "pa_verify_partition", "pa_verify_combine", "pa_verify_get_device_status", "pa_verify_status_string",
-            "pa_verify_forward_no_alloc"]
+            "pa_verify_forward_no_alloc", "pa_cache_update"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -91,6 +92,9 @@ def load_library():
         lib.pa_verify_get_device_status.restype = ctypes.c_int
         lib.pa_verify_forward_no_alloc.argtypes = fwd[:12] + [vp]
         lib.pa_verify_forward_no_alloc.restype = ctypes.c_int
+        lib.pa_cache_update.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, vp, dp,
+                                        vp, vp]
+        lib.pa_cache_update.restype = ctypes.c_int
         lib.pa_verify_status_string.argtypes = [ctypes.c_int]
         lib.pa_verify_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -218,3 +222,16 @@ def device_status(workspace, stream=None) -> int:
     _check(load_library().pa_verify_get_device_status(_ptr(workspace), _stream_ptr(stream), ctypes.byref(bits)),
            "pa_verify_get_device_status")
     return int(bits.value)
+
+
+def cache_update(k_new, v_new, k_cache, v_cache, block_tables, past_lens, subsequence_begins, dims: PaDims,
+                 status=None, stream=None):
+    """pa_cache_update: write the new tokens' K / V ([total_tokens, Hkv, D],
+    f32 / f16 / bf16) into their pages of k_cache / v_cache (float caches, or
+    uint8 page records); asynchronous on `stream`.  `status` is an optional
+    int32 / uint32 device tensor of one element that collects PA_STATUS_* bits."""
+    kv = _torch_dtype_code(k_cache.dtype)
+    _check(load_library().pa_cache_update(_ptr(k_new), _ptr(v_new), _torch_dtype_code(k_new.dtype), _ptr(k_cache),
+                                          _ptr(v_cache), int(kv), _ptr(block_tables), _ptr(past_lens),
+                                          _ptr(subsequence_begins), ctypes.byref(dims), _ptr(status),
+                                          _stream_ptr(stream)), "pa_cache_update")

@@ -292,3 +292,33 @@ def long_ctx_b(L: int, T: int = 8, seed: int = 0, **kw) -> Case:
     """Batch 1, T=8, 64 q / 8 KV heads, D=128, page 16, bf16 (128k-185k context)."""
     return make_case(f"long_T{T}_L{L}", seed=seed, query_lens=[T], past_lens=[L], num_q_heads=64,
                      num_kv_heads=8, head_dim=128, page_size=16, **kw)
+
+
+def new_tokens(case: Case, src_dtype: str = "bf16", seed: int = 0, specials: bool = False):
+    """The new tokens' K and V for a cache-update test: [total_tokens, Hkv, D]
+    ~ N(0, 1), rounded once to src_dtype (stored bits).  With specials, a few
+    (token, head) rows are replaced by shapes the u8 encoding must handle: a
+    constant row, an all-negative row, an all-positive row, and a row with a
+    single outlier."""
+    rng = np.random.default_rng(np.random.PCG64(seed + 7919))
+    T = int(case.subsequence_begins[-1])
+    shape = (T, case.num_kv_heads, case.head_dim)
+    out = []
+    for _ in range(2):
+        x = rng.standard_normal(shape).astype(np.float32)
+        if specials and T > 0:
+            rows = [(t, h) for t in range(T) for h in range(case.num_kv_heads)]
+            picks = rng.permutation(len(rows))[:4]
+            kinds = ["constant", "negative", "positive", "outlier"]
+            for k, i in zip(kinds, picks):
+                t, h = rows[i]
+                if k == "constant":
+                    x[t, h] = np.float32(0.75)
+                elif k == "negative":
+                    x[t, h] = -2.0 - np.abs(x[t, h])
+                elif k == "positive":
+                    x[t, h] = 1.0 + np.abs(x[t, h])
+                else:
+                    x[t, h, rng.integers(case.head_dim)] = np.float32(40.0)
+        out.append(to_storage(x, src_dtype))
+    return out[0], out[1]

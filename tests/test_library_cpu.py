@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "pa_verify.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_verify_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pa_(?:verify|cache)_\w+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
