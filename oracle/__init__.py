@@ -56,6 +56,10 @@ def _load():
                                               ci, ci, ctypes.c_double, ci,
                                               ctypes.POINTER(ctypes.c_double), ci]
             lib.pa_oracle_forward.restype = ci
+            lib.pa_oracle_forward_tree.argtypes = [vp, ci, vp, vp, ci, i32p, i32p, i32p, ci, ci, ci, ci, ci,
+                                                   ci, ci, ctypes.c_double, ci, vp,
+                                                   ctypes.POINTER(ctypes.c_double), ci]
+            lib.pa_oracle_forward_tree.restype = ci
             lib.pa_oracle_pages_touched.argtypes = [i32p, i32p, i32p, ci, ci, ci, ci, i32p]
             lib.pa_oracle_pages_touched.restype = ci
             lib.pa_oracle_cache_update.argtypes = [vp, vp, ci, vp, vp, ci, i32p, i32p, i32p, ci, ci, ci, ci, ci, ci]
@@ -81,8 +85,10 @@ def max_threads() -> int:
 def forward(q_raw: np.ndarray, q_dtype: str, k_cache_raw: np.ndarray, v_cache_raw: np.ndarray,
             kv_dtype: str, block_tables, past_lens, subsequence_begins, *, num_q_heads: int,
             num_kv_heads: int, head_dim: int, page_size: int, num_blocks: int, scale: float,
-            sliding_window: int = 0, nthreads: int = 0) -> np.ndarray:
-    """Exact-definition paged verify attention in fp64.
+            sliding_window: int = 0, nthreads: int = 0, tree_mask=None) -> np.ndarray:
+    """Exact-definition paged verify attention in fp64.  tree_mask (optional,
+    uint8 per token, at most 8 new tokens per sequence): bit k set = the token
+    sees the sequence's new token k; None = the causal chain.
 
     Arrays hold the stored bits (f32 values, or uint16 bit patterns for f16 /
     bf16, or the raw bytes of u8 page records).  Returns [total_tokens, Hq, D]
@@ -100,12 +106,15 @@ def forward(q_raw: np.ndarray, q_dtype: str, k_cache_raw: np.ndarray, v_cache_ra
     assert bt.ndim == 2 and bt.shape[0] == num_seqs and sb.shape[0] == num_seqs + 1
     total_tokens = int(sb[-1])
     out = np.zeros((total_tokens, num_q_heads, head_dim), dtype=np.float64)
-    rc = lib.pa_oracle_forward(q_raw.ctypes.data, DTYPE_CODES[q_dtype], k_cache_raw.ctypes.data,
-                               v_cache_raw.ctypes.data, DTYPE_CODES[kv_dtype], _ptr_i32(bt),
-                               _ptr_i32(pl), _ptr_i32(sb), num_seqs, num_q_heads, num_kv_heads,
-                               head_dim, page_size, num_blocks, bt.shape[1], float(scale),
-                               int(sliding_window),
-                               out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(nthreads))
+    tm = None if tree_mask is None else np.ascontiguousarray(np.asarray(tree_mask, dtype=np.uint8))
+    if tm is not None:
+        assert tm.shape == (total_tokens,)
+    rc = lib.pa_oracle_forward_tree(q_raw.ctypes.data, DTYPE_CODES[q_dtype], k_cache_raw.ctypes.data,
+                                    v_cache_raw.ctypes.data, DTYPE_CODES[kv_dtype], _ptr_i32(bt),
+                                    _ptr_i32(pl), _ptr_i32(sb), num_seqs, num_q_heads, num_kv_heads,
+                                    head_dim, page_size, num_blocks, bt.shape[1], float(scale),
+                                    int(sliding_window), None if tm is None else tm.ctypes.data,
+                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(nthreads))
     if rc != 0:
         raise ValueError("oracle: inconsistent inputs (block id or position out of range)")
     return out

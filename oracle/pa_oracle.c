@@ -22,6 +22,12 @@
  *     out[t, h, :] = sum_j exp(s_j - max s) V_j / sum_j exp(s_j - max s)
  *   with t = subsequence_begins[b] + i.
  *
+ *   Tree-mask verify (pa_oracle_forward_tree): the draft tokens form a tree
+ *   (DDTree; OpenVINO issue 34644, cited by the OpenVINO issue 38153 page):
+ *   token i sees every past key j < past_len_b inside its window as above, and
+ *   the new token k (key past_len_b + k) only if bit k of tree_mask[t] is set.
+ *   The causal chain (bits 0..i) gives back the definition above exactly.
+ *
  * Sources (web pages on paged attention for speculative verification):
  *  - OpenVINO issue 38153, "Performance issue description" and "Cause":
  *    a verify step sends k+1 query tokens of one sequence against a long
@@ -123,12 +129,12 @@ static double cache_value(const void* cache, int kv_dtype, int Hkv, int ps, int 
  * [0, num_blocks), a key position beyond the block table, bad begins).
  * out is [total_tokens, Hq, D] doubles.  nthreads <= 0 uses the OpenMP default.
  */
-int pa_oracle_forward(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
-                      int kv_dtype, const int32_t* block_tables, const int32_t* past_lens,
-                      const int32_t* subsequence_begins, int num_seqs, int num_q_heads,
-                      int num_kv_heads, int head_dim, int page_size, int num_blocks,
-                      int max_blocks_per_seq, double scale, int sliding_window, double* out,
-                      int nthreads) {
+int pa_oracle_forward_tree(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                           int kv_dtype, const int32_t* block_tables, const int32_t* past_lens,
+                           const int32_t* subsequence_begins, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int page_size, int num_blocks,
+                           int max_blocks_per_seq, double scale, int sliding_window,
+                           const uint8_t* tree_mask, double* out, int nthreads) {
   const int Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, ps = page_size;
   if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || ps <= 0 || num_seqs < 0) return -1;
   const int G = Hq / Hkv;
@@ -138,7 +144,8 @@ int pa_oracle_forward(const void* q, int q_dtype, const void* k_cache, const voi
   int* row_seq = (int*)malloc(sizeof(int) * (size_t)(total_tokens > 0 ? total_tokens : 1));
   if (!row_seq) return -1;
   for (int b = 0; b < num_seqs; ++b) {
-    if (subsequence_begins[b] > subsequence_begins[b + 1] || past_lens[b] < 0) {
+    if (subsequence_begins[b] > subsequence_begins[b + 1] || past_lens[b] < 0 ||
+        (tree_mask && subsequence_begins[b + 1] - subsequence_begins[b] > 8)) {
       free(row_seq);
       return -1;
     }
@@ -155,26 +162,37 @@ int pa_oracle_forward(const void* q, int q_dtype, const void* k_cache, const voi
     const int t = (int)(item / Hq), h = (int)(item % Hq);
     const int b = row_seq[t];
     const int i = t - subsequence_begins[b];
+    const int T = subsequence_begins[b + 1] - subsequence_begins[b];
     const int g = h / G;
-    const long p = (long)past_lens[b] + i;
+    const long L = past_lens[b];
+    const long p = L + i;
     const long lo = sliding_window > 0 ? (p - sliding_window + 1 > 0 ? p - sliding_window + 1 : 0) : 0;
-    const long n = p - lo + 1;
+    /* the new tokens this one attends: its tree mask, or the causal chain 0..i */
+    const unsigned m = tree_mask ? (unsigned)tree_mask[t] : ((2u << i) - 1u);
+    const long last = L + T - 1; /* the last key any row of the sequence may see */
     double* o = out + ((size_t)t * Hq + h) * D;
     for (int d = 0; d < D; ++d) o[d] = 0.0;
-    if (p / ps >= max_blocks_per_seq) {
+    if (last / ps >= max_blocks_per_seq) {
       bad = 1;
       continue;
     }
-    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    const long n = last - lo + 1;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     if (!s) {
       bad = 1;
       continue;
     }
-    /* scores s_j = scale * q . K_j */
+    /* scores s_j = scale * q . K_j over the visible keys: j >= lo, and either
+       a past key (j < L) or a new token whose bit is set */
     const size_t qoff = ((size_t)t * Hq + h) * D;
     double smax = -INFINITY;
-    int row_bad = 0;
-    for (long j = lo; j <= p; ++j) {
+    int row_bad = 0, seen = 0;
+    for (long j = lo; j <= last; ++j) {
+      const int vis = j < L || ((m >> (j - L)) & 1u);
+      if (!vis) {
+        s[j - lo] = -INFINITY;
+        continue;
+      }
       const int blk = block_tables[(size_t)b * max_blocks_per_seq + j / ps];
       if (blk < 0 || blk >= num_blocks) {
         row_bad = 1;
@@ -186,26 +204,42 @@ int pa_oracle_forward(const void* q, int q_dtype, const void* k_cache, const voi
                cache_value(k_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d);
       s[j - lo] = scale * acc;
       if (s[j - lo] > smax) smax = s[j - lo];
+      seen = 1;
     }
     if (row_bad) {
       free(s);
       bad = 1;
       continue;
     }
-    /* softmax weights and the weighted sum of V */
-    double denom = 0.0;
-    for (long j = lo; j <= p; ++j) {
-      const double w = exp(s[j - lo] - smax);
-      denom += w;
-      const int blk = block_tables[(size_t)b * max_blocks_per_seq + j / ps];
-      for (int d = 0; d < D; ++d)
-        o[d] += w * cache_value(v_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d);
+    if (seen) {
+      /* softmax weights and the weighted sum of V */
+      double denom = 0.0;
+      for (long j = lo; j <= last; ++j) {
+        if (s[j - lo] == -INFINITY) continue;
+        const double w = exp(s[j - lo] - smax);
+        denom += w;
+        const int blk = block_tables[(size_t)b * max_blocks_per_seq + j / ps];
+        for (int d = 0; d < D; ++d)
+          o[d] += w * cache_value(v_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d);
+      }
+      for (int d = 0; d < D; ++d) o[d] /= denom;
     }
-    for (int d = 0; d < D; ++d) o[d] /= denom;
     free(s);
   }
   free(row_seq);
   return bad ? -1 : 0;
+}
+
+int pa_oracle_forward(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                      int kv_dtype, const int32_t* block_tables, const int32_t* past_lens,
+                      const int32_t* subsequence_begins, int num_seqs, int num_q_heads,
+                      int num_kv_heads, int head_dim, int page_size, int num_blocks,
+                      int max_blocks_per_seq, double scale, int sliding_window, double* out,
+                      int nthreads) {
+  return pa_oracle_forward_tree(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, past_lens,
+                                subsequence_begins, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                page_size, num_blocks, max_blocks_per_seq, scale, sliding_window, NULL,
+                                out, nthreads);
 }
 
 /*

@@ -540,3 +540,93 @@ def test_cache_update_u8_zero_point_overflow_is_visible(oracle_mod):
     assert z == 0xFC00 and not codes.any()
     sf = float(np.array([s], dtype=np.uint16).view(np.float16)[0])
     assert not np.isfinite((codes.astype(np.float64) - (-np.inf)) * sf).any()
+
+
+# ---------------------------------------------------------------------------
+# Tree-mask verify: the draft tokens form a tree; a token sees the past keys
+# and the new tokens its mask names (itself and its ancestors).
+# ---------------------------------------------------------------------------
+def _chain_mask(case):
+    m = np.zeros(case.total_tokens, dtype=np.uint8)
+    for b in range(case.num_seqs):
+        t0 = int(case.subsequence_begins[b])
+        for i in range(int(case.query_lens[b])):
+            m[t0 + i] = (2 << i) - 1
+    return m
+
+
+def _random_tree_masks(case, rng):
+    """A random tree per sequence: node i's parent is a random earlier node
+    (node 0 hangs off the past); the mask of i is i plus its ancestors."""
+    m = np.zeros(case.total_tokens, dtype=np.uint8)
+    for b in range(case.num_seqs):
+        t0 = int(case.subsequence_begins[b])
+        for i in range(int(case.query_lens[b])):
+            parent = -1 if i == 0 else int(rng.integers(-1, i))
+            m[t0 + i] = (1 << i) | (m[t0 + parent] if parent >= 0 else 0)
+    return m
+
+
+def test_tree_chain_mask_is_the_causal_definition(oracle_mod):
+    for case in small_cases():
+        want = run_oracle(oracle_mod, case)
+        got = run_oracle(oracle_mod, case, tree_mask=_chain_mask(case))
+        assert np.array_equal(got, want), case.name
+
+
+def test_tree_mask_against_dense_brute_force(oracle_mod):
+    rng = np.random.default_rng(21)
+    for case in small_cases():
+        m = _random_tree_masks(case, rng)
+        got = run_oracle(oracle_mod, case, tree_mask=m)
+        kc, vc = _decode_cache(case)
+        q = W.storage_to_f64(case.q, case.q_dtype).reshape(case.total_tokens, case.num_q_heads, case.head_dim)
+        G = case.num_q_heads // case.num_kv_heads
+        for b in range(case.num_seqs):
+            L, t0, T = int(case.past_lens[b]), int(case.subsequence_begins[b]), int(case.query_lens[b])
+            for i in range(T):
+                p = L + i
+                lo = max(0, p - case.sliding_window + 1) if case.sliding_window > 0 else 0
+                keys = [j for j in range(lo, L + T) if j < L or (m[t0 + i] >> (j - L)) & 1]
+                blk = case.block_tables[b][np.array(keys) // case.page_size]
+                slot = np.array(keys) % case.page_size
+                for h in range(case.num_q_heads):
+                    K = kc[blk, h // G, slot]
+                    V = vc[blk, h // G, slot]
+                    s = case.scale * (K @ q[t0 + i, h])
+                    w = np.exp(s - s.max())
+                    assert np.allclose(got[t0 + i, h], w @ V / w.sum(), rtol=0, atol=1e-12), case.name
+
+
+def test_tree_node_equals_a_decode_over_its_path(oracle_mod):
+    """The tree semantics: node i's output is a single-token decode whose
+    cache holds the past followed by i's ancestors (in order) and i itself."""
+    rng = np.random.default_rng(22)
+    case = W.make_case("tree", seed=23, query_lens=[7], past_lens=[37], num_q_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=8, q_dtype="f32", kv_dtype="f32")
+    m = _random_tree_masks(case, rng)
+    got = run_oracle(oracle_mod, case, tree_mask=m)
+    kc, vc = _decode_cache(case)
+    L, ps, Hkv, D = 37, 8, 2, 16
+    for i in range(7):
+        path = [k for k in range(7) if (m[i] >> k) & 1]
+        n = L + len(path)
+        nb = (n + ps - 1) // ps
+        k_lin = np.full((nb, Hkv, ps, D), np.nan, dtype=np.float32)
+        v_lin = k_lin.copy()
+        for j in range(n):
+            src = j if j < L else L + path[j - L]
+            blk, slot = case.block_tables[0][src // ps], src % ps
+            k_lin[j // ps, :, j % ps] = kc[blk, :, slot]
+            v_lin[j // ps, :, j % ps] = vc[blk, :, slot]
+        one = oracle_mod.forward(case.q[i:i + 1], "f32", k_lin, v_lin, "f32", [list(range(nb))], [n - 1], [0, 1],
+                                 num_q_heads=4, num_kv_heads=Hkv, head_dim=D, page_size=ps, num_blocks=nb,
+                                 scale=case.scale)
+        assert np.array_equal(got[i], one[0]), i
+
+
+def test_tree_mask_with_no_visible_key_gives_zero(oracle_mod):
+    case = W.make_case("tree_empty", seed=24, query_lens=[2], past_lens=[0], num_q_heads=2, num_kv_heads=1,
+                       head_dim=8, page_size=8, q_dtype="f32", kv_dtype="f32")
+    got = run_oracle(oracle_mod, case, tree_mask=np.array([0, 3], dtype=np.uint8))
+    assert not got[0].any() and np.isfinite(got[1]).all() and got[1].any()
