@@ -156,6 +156,12 @@ class DeviceWorkload:
         pa.partition(self.q, self.k, self.v, self.block_tables[r], self.past_lens, self.begins, self.max_ctx,
                      self.scale, self.window, self.kv_code, self.out, self.dims, self.ws, stream=stream)
 
+    def forward_tree(self, r, tree_mask, stream=None):
+        import paged_attention_speculative_gb300 as pa
+        pa.forward_tree(self.q, self.k, self.v, self.block_tables[r], self.past_lens, self.begins, self.max_ctx,
+                        self.scale, self.window, self.kv_code, self.out, self.dims, self.ws, tree_mask,
+                        stream=stream)
+
     def cache_update(self, r, stream=None):
         import paged_attention_speculative_gb300 as pa
         pa.cache_update(self.k_new, self.v_new, self.k, self.v, self.block_tables[r], self.past_lens, self.begins,
@@ -635,6 +641,30 @@ def run_ours(args, rank, world):
             del w
             torch.cuda.empty_cache()
 
+    # Tree-mask verify: a random 8-node draft tree per sequence against the
+    # causal chain of 8 tokens on the same cache.
+    tree_verify = []
+    if not args.no_sweep and rank == 0:
+        import random
+        for name, hq, hkv, d, ps, kvd, T, L in (("qwen_gqa_T8_L32768", 32, 8, 128, 16, "bf16", 8, 32768),
+                                                  ("long_T8_L131072", 64, 8, 128, 16, "bf16", 8, 131072),
+                                                  ("qwen_u8_T8_L32768", 32, 8, 128, 16, "u8", 8, 32768)):
+            w = DeviceWorkload(hq, hkv, d, ps, kvd, [T], [L], 0, min_bytes=2 * L2, seed=11)
+            rr = random.Random(7)
+            m = []
+            for i in range(T):
+                parent = -1 if i == 0 else rr.randint(-1, i - 1)
+                m.append((1 << i) | (m[parent] if parent >= 0 else 0))
+            tm = torch.tensor(m, dtype=torch.uint8, device="cuda")
+            u_tree = time_calls(lambda r: w.forward_tree(r, tm, stream), w.replicas, stream)
+            u_chain = time_calls(lambda r: w.forward(r, stream), w.replicas, stream)
+            tree_verify.append({"workload": name, "tree_masks": m, "tree_us": round(u_tree, 2),
+                                "chain_us": round(u_chain, 2), "ratio": round(u_tree / u_chain, 3),
+                                "kv_gbs_tree": round(w.kv_bytes / (u_tree * 1e-6) / 1e9, 1)})
+            log(f"[bench] tree verify {tree_verify[-1]}")
+            del w
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, per, n, cores = time_oracle(H["q_lens"][0], H["past"][0], args.cpu_seconds)
@@ -671,6 +701,7 @@ def run_ours(args, rank, world):
         "gpu_launches": exact * wl.launches_per_step(),
         "sweep": sweep,
         "cache_update": cache_update,
+        "tree_verify": tree_verify,
     }
     print(json.dumps(line), flush=True)
 

@@ -253,6 +253,28 @@ int pa_cache_update(const void* k_new, const void* v_new, pa_dtype src_dtype, vo
                     const int32_t* subsequence_begins, const pa_dims* dims, uint32_t* status,
                     void* cuda_stream);
 
+/*
+ * pa_verify_forward_tree — the verify step for a tree of draft tokens
+ * (DDTree, OpenVINO issue 34644, both cited on the OpenVINO issue 38153
+ * page): the same as pa_verify_forward except that the new tokens of a
+ * sequence see each other through tree_mask instead of the causal chain.
+ *
+ *  tree_mask  device uint8 [total_tokens]: bit k of tree_mask[t] set = token
+ *             t sees the new token k of its own sequence (key past_len_b + k);
+ *             normally t's ancestors and t itself.  Past keys (j < past_len_b)
+ *             are seen as in pa_verify_forward, the window counted from
+ *             past_len_b + i.  A mask of bits 0..i for every token i gives
+ *             exactly pa_verify_forward's result.  A row that sees no key
+ *             at all is left zero.
+ *
+ * Other arguments, errors and the workspace as for pa_verify_forward
+ * (pa_verify_workspace_size applies unchanged).  Tree masks run on the
+ * library's default kernels; PA_ERR_NULL if tree_mask is NULL. */
+int pa_verify_forward_tree(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                           const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                           float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                           void* workspace, size_t workspace_bytes, const uint8_t* tree_mask, void* cuda_stream);
+
 /* Synchronises cuda_stream, then reads and clears the workspace's status word
  * into *bits (PA_STATUS_* flags, 0 = clean). */
 int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits);

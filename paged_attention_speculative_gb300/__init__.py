@@ -7,7 +7,7 @@ the verify path runs in the library's CUDA kernels.  There is no CPU
 fallback: if the library is missing, loading raises.
 
 Entry points mirror the C ABI:
-  forward / forward_traced / partition / combine / workspace_size / plan /
+  forward / forward_traced / forward_tree / partition / combine / workspace_size / plan /
   device_status / status_string, and cache_update (the step before the
   verify: the new tokens' K/V written into their pages)
 Tensors are torch CUDA tensors (torch supplies device memory and streams).
@@ -20,7 +20,7 @@ import threading
 
 __all__ = ["PA_F32", "PA_F16", "PA_BF16", "PA_U8", "PaDims", "PaPlan", "load_library", "library_path",
            "forward", "forward_traced", "partition", "combine", "workspace_size", "plan", "device_status",
-           "status_string", "dims_for", "cache_update", "PaVerifyError"]
+           "status_string", "dims_for", "cache_update", "forward_tree", "PaVerifyError"]
 
 PA_F32, PA_F16, PA_BF16, PA_U8 = 0, 1, 2, 3
 PA_MAX_QUERY_LEN = 8
@@ -28,7 +28,7 @@ STATUS_BITS = {0x1: "QUERY_LEN", 0x2: "CONTEXT", 0x4: "BLOCK_ID", 0x8: "BEGINS",
                0x20: "ROWS", 0x40: "TIMEOUT"}
 EXPORTED = ["pa_verify_workspace_size", "pa_verify_plan", "pa_verify_forward", "pa_verify_forward_traced",
             "pa_verify_partition", "pa_verify_combine", "pa_verify_get_device_status", "pa_verify_status_string",
-            "pa_verify_forward_no_alloc", "pa_cache_update"]
+            "pa_verify_forward_no_alloc", "pa_cache_update", "pa_verify_forward_tree"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -92,6 +92,8 @@ def load_library():
         lib.pa_verify_get_device_status.restype = ctypes.c_int
         lib.pa_verify_forward_no_alloc.argtypes = fwd[:12] + [vp]
         lib.pa_verify_forward_no_alloc.restype = ctypes.c_int
+        lib.pa_verify_forward_tree.argtypes = fwd[:14] + [vp, vp]
+        lib.pa_verify_forward_tree.restype = ctypes.c_int
         lib.pa_cache_update.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, vp, dp,
                                         vp, vp]
         lib.pa_cache_update.restype = ctypes.c_int
@@ -197,6 +199,17 @@ def forward_traced(q, k_cache, v_cache, block_tables, past_lens, subsequence_beg
                                                               subsequence_begins, max_context_len, scale,
                                                               sliding_window, kv_dtype, out, dims, workspace,
                                                               stream), _ptr(trace)), "pa_verify_forward_traced")
+    return out
+
+
+def forward_tree(q, k_cache, v_cache, block_tables, past_lens, subsequence_begins, max_context_len, scale,
+                 sliding_window, kv_dtype, out, dims: PaDims, workspace, tree_mask, stream=None):
+    """pa_verify_forward_tree: like forward, with the new tokens seeing each
+    other through tree_mask (uint8 device tensor [total_tokens], bit k = sees
+    its sequence's new token k)."""
+    args = _fwd_args(q, k_cache, v_cache, block_tables, past_lens, subsequence_begins, max_context_len, scale,
+                     sliding_window, kv_dtype, out, dims, workspace, stream)
+    _check(load_library().pa_verify_forward_tree(*args[:14], _ptr(tree_mask), args[14]), "pa_verify_forward_tree")
     return out
 
 

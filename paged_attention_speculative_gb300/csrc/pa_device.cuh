@@ -36,6 +36,7 @@ struct PartArgs {
   float* pl;                    // [total_tokens, Hq, P] softmax denominators (-1 = poisoned)
   uint32_t* status;
   int32_t* trace;               // optional gather trace
+  const uint8_t* tree_mask;     // optional: per token, bit k = sees new token k of its sequence
   int num_seqs, total_tokens, Hq, Hkv, G, D, ps, ps_log2, num_blocks, max_blocks;
   int max_ctx, window, part_tokens, num_parts, box_log2, row_cap;
   int q_dtype, out_dtype;
@@ -73,6 +74,16 @@ __device__ __forceinline__ int32_t ld_once(const int32_t* p) {
   int32_t v;
   asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
+}
+__device__ __forceinline__ uint32_t ld_once_u8(const uint8_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+// The new tokens token i of a sequence sees: its tree mask, or the causal
+// chain 0..i when there is none.
+__device__ __forceinline__ uint32_t row_new_token_mask(const uint8_t* tree_mask, int t, int i) {
+  return tree_mask != nullptr ? ld_once_u8(tree_mask + t) : ((2u << i) - 1u);
 }
 __device__ __forceinline__ uint32_t ld_once(const uint32_t* p) {
   uint32_t v;

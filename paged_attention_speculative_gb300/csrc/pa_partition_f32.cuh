@@ -56,12 +56,15 @@ __global__ void __launch_bounds__(128) pa_partition_f32(const PartArgs a) {
       qv[e] = load_q_elem(a.q, a.q_dtype, row * D + lane + 32 * e);
       o[e] = 0.f;
     }
-    const int hi = si.L + i;
-    const int lo = a.window > 0 ? max(0, hi - a.window + 1) : 0;
+    const int p_i = si.L + i;
+    const int lo = a.window > 0 ? max(0, p_i - a.window + 1) : 0;
+    const uint32_t tm = row_new_token_mask(a.tree_mask, si.t0 + i, i);
+    const int hi = a.tree_mask != nullptr ? si.L + si.T - 1 : p_i;
     const int k0 = max(kstart, lo), k1 = min(kend - 1, hi);
     float m = -INFINITY, l = 0.f;
     bool bad = false;
     for (int key = k0; key <= k1; ++key) {
+      if (key >= si.L && !((tm >> (key - si.L)) & 1u)) continue;  // a new token outside the row's tree path
       const int id = __ldg(bt + (key >> a.ps_log2));
       if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
         bad = true;

@@ -250,17 +250,23 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
 
   // Key limits of the rows this thread's accumulator columns hold (rows past
   // R borrow the last valid row's limits so they mask like it).
+  // With a tree mask a row may see any new token its mask names: hi covers
+  // them all and the mask decides; without one the mask is all ones and hi
+  // is the row's own position (the causal chain).
+  const bool tree = a.tree_mask != nullptr;
   int rlo[NT][2], rhi[NT][2];
+  uint32_t rmask[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int r = min(row_base + nt * 8 + 2 * tig + j, R - 1);
-      rhi[nt][j] = L + r / a.G;
-      rlo[nt][j] = a.window > 0 ? rhi[nt][j] - a.window + 1 : INT_MIN;
+      rhi[nt][j] = tree ? L + si.T - 1 : L + r / a.G;
+      rlo[nt][j] = a.window > 0 ? L + r / a.G - a.window + 1 : INT_MIN;
+      rmask[nt][j] = tree ? row_new_token_mask(a.tree_mask, si.t0 + r / a.G, r / a.G) : 0xffffffffu;
     }
   const int last_row = row_base + max(nvalid, 1) - 1;
-  const int wmin_hi = L + min(row_base, R - 1) / a.G;
+  const int wmin_hi = tree ? L - 1 : L + min(row_base, R - 1) / a.G;
   const int wmax_lo = a.window > 0 ? L + min(last_row, R - 1) / a.G - a.window + 1 : INT_MIN;
 
   // Q^T fragments (B operand), loaded once.
@@ -412,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
             else v = acc * sl2;
             if (!clean) {
               const int key = (e >> 1) ? kg1 : kg0;
-              const bool okk = key >= rlo[nt][e & 1] && key <= rhi[nt][e & 1];
+              const bool okk = key >= rlo[nt][e & 1] && key <= rhi[nt][e & 1] &&
+                               (key < L || ((rmask[nt][e & 1] >> (key - L)) & 1u));
               v = okk ? v : -INFINITY;
             }
             sc[nt][e] = v;

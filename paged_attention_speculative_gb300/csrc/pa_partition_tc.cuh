@@ -382,8 +382,13 @@ __global__ void __launch_bounds__(128, 1)
     // =========================== softmax warps (rows) =======================
     const int r = warp * 32 + lane;                          // TMEM lane / query row
     const int rc = min(r, R - 1);                            // padding rows mask like the last row
-    const int hi = si.L + rc / a.G;
-    const int lo = a.window > 0 ? hi - a.window + 1 : INT_MIN;
+    // with a tree mask the row sees the new tokens its mask names (hi covers
+    // them all); without one, the causal chain up to its own position
+    const bool tree = a.tree_mask != nullptr;
+    const int hi = tree ? si.L + si.T - 1 : si.L + rc / a.G;
+    const int clean_hi = tree ? si.L - 1 : hi;
+    const uint32_t tmask = tree ? row_new_token_mask(a.tree_mask, si.t0 + rc / a.G, rc / a.G) : 0xffffffffu;
+    const int lo = a.window > 0 ? si.L + rc / a.G - a.window + 1 : INT_MIN;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
@@ -403,14 +408,14 @@ __global__ void __launch_bounds__(128, 1)
       if (lane == 0) mbar_arrive(&s_free[sb]);
 
       const int key0 = kstart + s * C::SK;
-      const bool clean = key0 >= lo && key0 + C::SK - 1 <= hi;
+      const bool clean = key0 >= lo && key0 + C::SK - 1 <= clean_hi;
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < C::SK; ++j) {
         float v = x[j] * sl2;
         if (!clean) {
           const int key = key0 + j;
-          v = (key >= lo && key <= hi) ? v : -INFINITY;
+          v = (key >= lo && key <= hi && (key < si.L || ((tmask >> (key - si.L)) & 1u))) ? v : -INFINITY;
         }
         x[j] = v;
         mt = fmaxf(mt, v);

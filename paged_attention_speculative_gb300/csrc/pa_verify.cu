@@ -78,7 +78,8 @@ pa::MmaKernelInfo mma_info(int D, int kind, int nt, bool* ok) {
 }
 
 // Argument checks shared by every entry point; fills the plan.
-int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, int32_t num_sms, pa_plan* plan) {
+int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, int32_t num_sms, pa_plan* plan,
+              bool tree = false) {
   if (d == nullptr || plan == nullptr) return PA_ERR_NULL;
   std::memset(plan, 0, sizeof(*plan));
   if (d->num_seqs < 1 || d->num_seqs > 65535 || d->total_tokens < 0 || d->num_q_heads < 1 ||
@@ -113,7 +114,9 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   // path is slightly faster.
   const bool tc16 = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128);
   const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
-  const int choice = env_kernel_choice();
+  // tree masks run on the warp-level, fp32 and rows-on-M tensor-memory
+  // kernels only; a forced keys-on-M or u8 tensor-memory choice falls back
+  const int choice = (tree && (env_kernel_choice() == 3 || kv == PA_U8)) ? 0 : env_kernel_choice();
   // u8 caches take the tensor-memory kernel only when forced (tuning).
   if (kv == PA_U8 && D == 128 && rows <= 32 && choice == 3) {
     const int n = rows <= 16 ? 16 : 32;
@@ -298,6 +301,7 @@ struct Call {
   size_t ws_bytes;
   cudaStream_t stream;
   int32_t* trace;
+  const uint8_t* tree_mask;  // optional (tree-mask verify)
 };
 
 int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
@@ -315,6 +319,7 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.pl = w.pl;
   a.status = w.status;
   a.trace = c.trace;
+  a.tree_mask = c.tree_mask;
   a.num_seqs = d->num_seqs;
   a.total_tokens = d->total_tokens;
   a.Hq = d->num_q_heads;
@@ -430,14 +435,14 @@ int run(const Call& c, bool do_partition, bool do_combine) {
   if (c.d == nullptr) return PA_ERR_NULL;
   int sms = 0;
   pa_plan plan;
-  int rc = make_plan(c.d, c.max_ctx, c.window, c.kv, 1, &plan);  // argument checks first
+  int rc = make_plan(c.d, c.max_ctx, c.window, c.kv, 1, &plan, c.tree_mask != nullptr);  // argument checks first
   if (rc != PA_OK) return rc;
   rc = check_pointers(c, do_partition);
   if (rc != PA_OK) return rc;
   if (c.d->total_tokens == 0) return PA_OK;
   rc = device_sm_count(&sms);
   if (rc != PA_OK) return rc;
-  rc = make_plan(c.d, c.max_ctx, c.window, c.kv, sms, &plan);
+  rc = make_plan(c.d, c.max_ctx, c.window, c.kv, sms, &plan, c.tree_mask != nullptr);
   if (rc != PA_OK) return rc;
   if (c.ws_bytes < workspace_bytes_for(c.d, plan)) return PA_ERR_WORKSPACE;
   const Workspace w = carve(c.ws, c.d, plan);
@@ -500,6 +505,17 @@ int pa_verify_forward(const void* q, const void* k_cache, const void* v_cache, c
   const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
                max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
                static_cast<cudaStream_t>(cuda_stream), nullptr};
+  return run(c, true, true);
+}
+
+int pa_verify_forward_tree(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                           const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                           float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                           void* workspace, size_t workspace_bytes, const uint8_t* tree_mask, void* cuda_stream) {
+  if (tree_mask == nullptr) return PA_ERR_NULL;
+  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+               max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(cuda_stream), nullptr, tree_mask};
   return run(c, true, true);
 }
 
