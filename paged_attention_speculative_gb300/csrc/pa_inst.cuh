@@ -11,10 +11,10 @@ MmaKernelInfo mma_info_t() {
   return MmaKernelInfo{MmaCfg<D, KV>::SK, MmaSmem<D, KV, NT>::BYTES, MmaSmem<D, KV, NT>::CTAS_PER_SM};
 }
 
-template <int D, int KV, int NT>
-cudaError_t launch_mma_t(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
-                         cudaStream_t st) {
-  auto kern = pa_partition_mma<D, KV, NT>;
+template <int D, int KV, int NT, bool TREE>
+cudaError_t launch_mma_tt(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                          cudaStream_t st) {
+  auto kern = pa_partition_mma<D, KV, NT, TREE>;
   const int smem = MmaSmem<D, KV, NT>::BYTES;
   // Raise the dynamic shared-memory limit once per process and device.
   static int configured_for[64] = {0};
@@ -27,6 +27,15 @@ cudaError_t launch_mma_t(const CUtensorMap& k, const CUtensorMap& v, const PartA
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
   return launch_dependent(kern, grid, dim3(kThreads), smem, st, k, v, a);
+}
+
+// Tree-mask verify runs its own instantiation, so the causal kernels keep
+// their code.
+template <int D, int KV, int NT>
+cudaError_t launch_mma_t(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
+                         cudaStream_t st) {
+  return a.tree_mask != nullptr ? launch_mma_tt<D, KV, NT, true>(k, v, a, grid, st)
+                                : launch_mma_tt<D, KV, NT, false>(k, v, a, grid, st);
 }
 
 }  // namespace pa

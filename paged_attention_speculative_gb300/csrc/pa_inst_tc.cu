@@ -6,9 +6,9 @@
 namespace pa {
 
 namespace {
-template <int D, int KV>
-cudaError_t launch_tc_t(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid, cudaStream_t st) {
-  auto kern = pa_partition_tc<D, KV>;
+template <int D, int KV, bool TREE>
+cudaError_t launch_tc_tt(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid, cudaStream_t st) {
+  auto kern = pa_partition_tc<D, KV, TREE>;
   const int smem = TcCfg<D, KV>::BYTES;
   static int configured_for[64] = {0};
   int dev = 0;
@@ -20,6 +20,11 @@ cudaError_t launch_tc_t(const CUtensorMap& k, const CUtensorMap& v, const PartAr
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
   return launch_dependent(kern, grid, dim3(128), smem, st, k, v, a);
+}
+template <int D, int KV>
+cudaError_t launch_tc_t(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid, cudaStream_t st) {
+  return a.tree_mask != nullptr ? launch_tc_tt<D, KV, true>(k, v, a, grid, st)
+                                : launch_tc_tt<D, KV, false>(k, v, a, grid, st);
 }
 cudaError_t launch_tcu8_128(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                             cudaStream_t st) {

@@ -72,7 +72,7 @@ __device__ __forceinline__ int out_dim(int mt, int m) {
   else return 16 * mt + m;
 }
 
-template <int D, int KV, int NT>
+template <int D, int KV, int NT, bool TREE = false>
 __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     pa_partition_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const PartArgs a) {
@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
   // With a tree mask a row may see any new token its mask names: hi covers
   // them all and the mask decides; without one the mask is all ones and hi
   // is the row's own position (the causal chain).
-  const bool tree = a.tree_mask != nullptr;
+  // (TREE: the launcher picks this instantiation when a mask is given)
+  constexpr bool tree = TREE;
   int rlo[NT][2], rhi[NT][2];
   uint32_t rmask[NT][2];
 #pragma unroll
@@ -418,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
             else v = acc * sl2;
             if (!clean) {
               const int key = (e >> 1) ? kg1 : kg0;
-              const bool okk = key >= rlo[nt][e & 1] && key <= rhi[nt][e & 1] &&
-                               (key < L || ((rmask[nt][e & 1] >> (key - L)) & 1u));
+              bool okk = key >= rlo[nt][e & 1] && key <= rhi[nt][e & 1];
+              if constexpr (TREE) okk = okk && (key < L || ((rmask[nt][e & 1] >> (key - L)) & 1u));
               v = okk ? v : -INFINITY;
             }
             sc[nt][e] = v;

@@ -160,7 +160,7 @@ struct TcCfg {
   static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory budget");
 };
 
-template <int D, int KV>
+template <int D, int KV, bool TREE = false>
 __global__ void __launch_bounds__(128, 1)
     pa_partition_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const PartArgs a) {
@@ -384,10 +384,10 @@ __global__ void __launch_bounds__(128, 1)
     const int rc = min(r, R - 1);                            // padding rows mask like the last row
     // with a tree mask the row sees the new tokens its mask names (hi covers
     // them all); without one, the causal chain up to its own position
-    const bool tree = a.tree_mask != nullptr;
-    const int hi = tree ? si.L + si.T - 1 : si.L + rc / a.G;
-    const int clean_hi = tree ? si.L - 1 : hi;
-    const uint32_t tmask = tree ? row_new_token_mask(a.tree_mask, si.t0 + rc / a.G, rc / a.G) : 0xffffffffu;
+    // (TREE: the launcher picks this instantiation when a mask is given)
+    const int hi = TREE ? si.L + si.T - 1 : si.L + rc / a.G;
+    const int clean_hi = TREE ? si.L - 1 : hi;
+    const uint32_t tmask = TREE ? row_new_token_mask(a.tree_mask, si.t0 + rc / a.G, rc / a.G) : 0u;
     const int lo = a.window > 0 ? si.L + rc / a.G - a.window + 1 : INT_MIN;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = a.scale_log2;
@@ -415,7 +415,11 @@ __global__ void __launch_bounds__(128, 1)
         float v = x[j] * sl2;
         if (!clean) {
           const int key = key0 + j;
-          v = (key >= lo && key <= hi && (key < si.L || ((tmask >> (key - si.L)) & 1u))) ? v : -INFINITY;
+          if constexpr (TREE) {
+            v = (key >= lo && key <= hi && (key < si.L || ((tmask >> (key - si.L)) & 1u))) ? v : -INFINITY;
+          } else {
+            v = (key >= lo && key <= hi) ? v : -INFINITY;
+          }
         }
         x[j] = v;
         mt = fmaxf(mt, v);
