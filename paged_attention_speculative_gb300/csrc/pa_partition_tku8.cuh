@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(320, 1)
         const __half* ks = reinterpret_cast<const __half*>(st + 2 * C::U8_TILE + seg * 4 * br);
         const __half* vs = reinterpret_cast<const __half*>(st + 2 * C::U8_TILE + 4 * C::HK + seg * 4 * br);
         const int key = kstart + s * C::SK + ct;
-        const bool in = key >= si.klo && key <= si.khi;
+        const bool in = key >= si.klo && key <= si.khi && key < kend;  // past kend: the next partition's
         side_buf[cb * C::SK + ct] = in ? make_float4(__half2float(ks[o]) * sl2, __half2float(ks[br + o]),
                                                      __half2float(vs[o]), __half2float(vs[br + o]))
                                        : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -457,6 +457,7 @@ __global__ void __launch_bounds__(320, 1)
       const int nlo = dk > 0 ? dk * a.G : 0;
       int nhi = R;
       if (a.window > 0) nhi = min(R, max(0, (dk + a.window) * a.G));
+      if (key >= kend) nhi = 0;  // a half-filled last stage: those keys belong to the next partition
       const bool clean = (nlo == 0 && nhi >= R);
       bool need = false;
 #pragma unroll

@@ -118,7 +118,11 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   // kernels only; a forced keys-on-M or u8 tensor-memory choice falls back
   const int choice = (tree && (env_kernel_choice() == 3 || kv == PA_U8)) ? 0 : env_kernel_choice();
   // u8 caches take the tensor-memory kernel only when forced (tuning).
-  if (kv == PA_U8 && D == 128 && rows <= 32 && choice == 3) {
+  // u8 caches with 17..32 query rows per KV head: the keys-on-M kernel's
+  // cost does not grow with the rows, while the warp-level kernel converts
+  // every chunk once per 8-row group (measured at T = 5..8, G = 4: 41 us vs
+  // 52-57 us at 32k keys).  Up to 16 rows the warp-level kernel is as fast.
+  if (kv == PA_U8 && D == 128 && rows <= 32 && !tree && choice != 1 && (choice == 3 || rows > 16)) {
     const int n = rows <= 16 ? 16 : 32;
     bool ok = false;
     pa::MmaKernelInfo info = pa::tku8_info(n, &ok);

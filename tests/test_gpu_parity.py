@@ -47,6 +47,9 @@ SMALL = [
     lambda: W.qwen_gqa(4, 777, seed=4),
     lambda: W.qwen_u8(1, 1500, seed=5),
     lambda: W.qwen_u8(3, 1234, seed=6),
+    lambda: W.qwen_u8(6, 2345, seed=15),   # 24 rows: the u8 keys-on-M kernel by default
+    lambda: W.make_case("u8_batch_t8", seed=16, query_lens=[8, 5, 0, 7], past_lens=[1900, 700, 20, 2500],
+                        num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, kv_dtype="u8"),
     lambda: W.gemma_hybrid(1500, seed=7),
     lambda: W.gemma_hybrid(3000, window=1024, seed=8),
     lambda: W.batched_mix_a(seed=9),
@@ -88,7 +91,7 @@ FULL = [
     lambda: W.tiny(),
     lambda: W.qwen_gqa(1, 8192), lambda: W.qwen_gqa(4, 8192), lambda: W.qwen_gqa(2, 32768),
     lambda: W.qwen_gqa(4, 32768),
-    lambda: W.qwen_u8(1, 32768), lambda: W.qwen_u8(3, 65536),
+    lambda: W.qwen_u8(1, 32768), lambda: W.qwen_u8(3, 65536), lambda: W.qwen_u8(8, 32768),
     lambda: W.gemma_hybrid(32768), lambda: W.gemma_hybrid(51200), lambda: W.gemma_hybrid(32768, window=1024),
     lambda: W.batched_mix_a(),
     lambda: W.long_ctx_b(131072), lambda: W.long_ctx_b(184320),
