@@ -37,7 +37,7 @@ HEADLINE = dict(name="qwen_gqa_T4_L32768", Hq=32, Hkv=8, D=128, ps=16, kv="bf16"
 
 SWEEP = [
     dict(name="qwen_gqa_T{T}_L{L}", Hq=32, Hkv=8, D=128, ps=16, kv="bf16", T=[1, 2, 3, 4], L=[8192, 32768], window=0),
-    dict(name="qwen_u8_T{T}_L{L}", Hq=32, Hkv=8, D=128, ps=16, kv="u8", T=[1, 3], L=[32768, 65536], window=0),
+    dict(name="qwen_u8_T{T}_L{L}", Hq=32, Hkv=8, D=128, ps=16, kv="u8", T=[1, 3, 8], L=[32768, 65536], window=0),
     dict(name="gemma_global_T{T}_L{L}", Hq=32, Hkv=16, D=256, ps=64, kv="bf16", T=[1, 2], L=[32768, 51200], window=0),
     dict(name="gemma_swa1024_T{T}_L{L}", Hq=32, Hkv=16, D=256, ps=64, kv="bf16", T=[1, 2], L=[32768], window=1024),
     dict(name="long_T{T}_L{L}", Hq=64, Hkv=8, D=128, ps=16, kv="bf16", T=[1, 8], L=[131072, 184320], window=0),
@@ -204,6 +204,10 @@ def kernel_name(wl) -> str:
     p = wl.plan()
     if p.kernel == 2:
         return f"pa_partition_tc<D={wl.D}, {wl.kv}> (tcgen05, TMEM accumulators)"
+    if p.kernel == 3:
+        return f"pa_partition_tk<D={wl.D}, {wl.kv}, N={p.row_tiles}> (tcgen05, keys on M)"
+    if p.kernel == 4:
+        return f"pa_partition_tku8<N={p.row_tiles}> (tcgen05, keys on M, u8 codes in TMEM)"
     if p.kernel == 1:
         return f"pa_partition_f32<D={wl.D}>"
     return f"pa_partition_mma<D={wl.D}, {wl.kv}, n-tiles={p.row_tiles}> (mma.sync)"
