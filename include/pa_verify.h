@@ -268,7 +268,7 @@ int pa_cache_update(const void* k_new, const void* v_new, pa_dtype src_dtype, vo
  *             at all is left zero.
  *
  * Other arguments, errors and the workspace as for pa_verify_forward
- * (pa_verify_workspace_size applies unchanged).  Tree masks run on the
+ * (pa_verify_workspace_size covers both entry points).  Tree masks run on the
  * library's default kernels; PA_ERR_NULL if tree_mask is NULL. */
 int pa_verify_forward_tree(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                            const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,

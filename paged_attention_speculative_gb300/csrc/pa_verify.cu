@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -494,7 +495,11 @@ size_t pa_verify_workspace_size(const pa_dims* dims, int32_t max_context_len, in
   if (device_sm_count(&sms) != PA_OK) return 0;
   pa_plan plan;
   if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &plan) != PA_OK) return 0;
-  return workspace_bytes_for(dims, plan);
+  // one size for both entry points: a tree-mask call may run another kernel
+  // (and so another partition count) than the plain verify
+  pa_plan tree_plan;
+  if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &tree_plan, true) != PA_OK) return 0;
+  return std::max(workspace_bytes_for(dims, plan), workspace_bytes_for(dims, tree_plan));
 }
 
 int pa_verify_plan(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window, pa_dtype kv_dtype,

@@ -94,3 +94,26 @@ def test_chain_mask_is_the_plain_verify_bit_for_bit(idx):
     dev = to_device(case)
     run_gpu(case, dev=dev)
     assert torch.equal(raw_tree.view(torch.int16), dev["out"].cpu().view(torch.int16))
+
+
+def test_workspace_size_covers_tree_calls():
+    """u8 at 24 rows per KV head: the plain verify runs the keys-on-M u8
+    kernel (one CTA per SM), a tree-mask call the warp-level kernel (two per
+    SM, so more partitions); pa_verify_workspace_size must cover both."""
+    import torch
+    case = W.qwen_u8(6, 32768, seed=106)
+    dev = to_device(case)
+    d = dims(case, dev)
+    kvc = KV_CODE[case.kv_dtype]
+    ws = pa.alloc_workspace(d, case.max_context_len, 0, kvc)
+    tm = torch.from_numpy(random_tree_masks(case, seed=9)).cuda()
+    pa.forward_tree(dev["q"], dev["k"], dev["v"], dev["bt"], dev["pl"], dev["sb"], case.max_context_len, case.scale,
+                    0, kvc, dev["out"], d, ws, tm)
+    torch.cuda.synchronize()
+    first = dev["out"].clone()
+    big = torch.zeros(ws.numel() * 4, dtype=torch.uint8, device="cuda")
+    pa.forward_tree(dev["q"], dev["k"], dev["v"], dev["bt"], dev["pl"], dev["sb"], case.max_context_len, case.scale,
+                    0, kvc, dev["out"], d, big, tm)
+    torch.cuda.synchronize()
+    assert pa.device_status(ws) == 0
+    assert torch.equal(first.view(torch.int16), dev["out"].view(torch.int16))
