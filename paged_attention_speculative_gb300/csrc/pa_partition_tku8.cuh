@@ -42,7 +42,7 @@ struct TkU8Cfg {
   static constexpr int NB = 3;                         // converted stages in flight
   static constexpr int Q_BYTES = N * D * 2;
   static constexpr int P_BYTES = N * SK * 2;          // P'^T, K-major: [key chunk][row][128 B]
-  static constexpr int MISC = 4096;
+  static constexpr int MISC = 4608;
   static constexpr int FIXED = NB * SIDE + Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + MISC + 1024;
   static constexpr int NSU_FIT = (226 * 1024 - FIXED) / U8_STAGE;
   static constexpr int NSU = NSU_FIT > 12 ? 12 : NSU_FIT;  // u8 half stages in the ring
@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(320, 1)
   long long* rowoff = reinterpret_cast<long long*>(alpha_sm + 64);    // [64]
   float* qsum_sm = reinterpret_cast<float*>(rowoff + 64);             // [64] sum_d of each f16 query row
   float* xch2 = qsum_sm + 64;                                         // [4][64] second exchange
+  uint32_t* tree_rows = reinterpret_cast<uint32_t*>(xch2 + 256);      // [8] rows that see new token k
   __shared__ uint32_t s_tmem;
   __shared__ int s_bad, s_timeout;
 
@@ -200,6 +201,14 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       qsum_sm[n] = sum;
+    }
+    if (threadIdx.x < PA_MAX_QUERY_LEN) {
+      // tree masks: the rows that see new token k (row n = token n / G)
+      const int k = threadIdx.x;
+      uint32_t rows = 0;
+      if (a.tree_mask != nullptr)
+        for (int n = 0; n < R; ++n) rows |= ((ld_once_u8(a.tree_mask + si.t0 + n / a.G) >> k) & 1u) << n;
+      tree_rows[k] = rows;
     }
   }
   if (warp < 9) {
@@ -454,11 +463,19 @@ __global__ void __launch_bounds__(320, 1)
 
       const int key = kstart + s * C::SK + kq;
       const int dk = key - si.L;
-      const int nlo = dk > 0 ? dk * a.G : 0;
+      // rows that see this key, as a bit set: [nlo, nhi) (the causal limit
+      // and the window), or for a tree mask the window and the rows whose
+      // mask names this new token
+      const bool tree = a.tree_mask != nullptr;
+      const int nlo = (dk > 0 && !tree) ? dk * a.G : 0;
       int nhi = R;
       if (a.window > 0) nhi = min(R, max(0, (dk + a.window) * a.G));
       if (key >= kend) nhi = 0;  // a half-filled last stage: those keys belong to the next partition
-      const bool clean = (nlo == 0 && nhi >= R);
+      const uint32_t below_hi = nhi >= 32 ? 0xffffffffu : ((1u << nhi) - 1u);
+      const uint32_t below_lo = nlo >= 32 ? 0xffffffffu : ((1u << nlo) - 1u);
+      uint32_t vrows = below_hi & ~below_lo;
+      if (tree && dk >= 0) vrows &= (dk < PA_MAX_QUERY_LEN) ? tree_rows[dk] : 0u;
+      const bool clean = (nlo == 0 && nhi >= R) && !(tree && dk >= 0);
       bool need = false;
 #pragma unroll
       for (int n4 = 0; n4 < N; n4 += 4) {
@@ -468,7 +485,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int e = 0; e < 4; ++e) {
           const int n = n4 + e;
           float x = fmaf(-sd.y, qs[n], v[n]) * sd.x;
-          if (!clean) x = (n >= nlo && n < nhi) ? x : -INFINITY;
+          if (!clean) x = ((vrows >> n) & 1u) ? x : -INFINITY;
           v[n] = x;
           need |= x > mm[e] + 8.f;
         }

@@ -117,13 +117,26 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
   // tree masks run on the warp-level, fp32 and rows-on-M tensor-memory
   // kernels only; a forced keys-on-M or u8 tensor-memory choice falls back
-  const int choice = (tree && (env_kernel_choice() == 3 || kv == PA_U8)) ? 0 : env_kernel_choice();
+  // tree masks run on every kernel but the 16-bit keys-on-M one and the u8
+  // rows-on-M tensor-memory one: a forced choice of those falls back
+  const int choice = (tree && (env_kernel_choice() == 3 && kv != PA_U8)) ? 0
+                     : (tree && env_kernel_choice() == 2 && kv == PA_U8) ? 0
+                                                                        : env_kernel_choice();
   // u8 caches take the tensor-memory kernel only when forced (tuning).
   // u8 caches with 17..32 query rows per KV head: the keys-on-M kernel's
   // cost does not grow with the rows, while the warp-level kernel converts
   // every chunk once per 8-row group (measured at T = 5..8, G = 4: 41 us vs
   // 52-57 us at 32k keys).  Up to 16 rows the warp-level kernel is as fast.
-  if (kv == PA_U8 && D == 128 && rows <= 32 && !tree && choice != 1 && (choice == 3 || rows > 16)) {
+  //   The choice follows the rows of an average sequence and needs one wave
+  //   of (sequence, KV head) units: with many short units (large batches)
+  //   the warp-level kernel's two CTAs per SM win (measured: batch 64 x T=4,
+  //   4k keys: 223 us vs 323 us).
+  const long long avg_t = std::min<long long>(PA_MAX_QUERY_LEN, (std::max(d->total_tokens, 1) + d->num_seqs - 1) /
+                                                                     d->num_seqs);
+  const long long rows_avg = static_cast<long long>(G) * avg_t;
+  const bool one_wave = static_cast<long long>(d->num_seqs) * d->num_kv_heads <= num_sms;
+  if (kv == PA_U8 && D == 128 && rows <= 32 && choice != 1 &&
+      (choice == 3 || (rows_avg > 16 && one_wave))) {
     const int n = rows <= 16 ? 16 : 32;
     bool ok = false;
     pa::MmaKernelInfo info = pa::tku8_info(n, &ok);

@@ -35,10 +35,8 @@ CASES = [
     (lambda: W.long_ctx_b(3000, seed=103), 2, False),
     (lambda: W.make_case("tree_batch_win", seed=104, query_lens=[5, 0, 8, 3], past_lens=[900, 10, 1300, 40],
                          num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, sliding_window=400), 2, True),
-    # 24 u8 rows: without a mask the plan picks the u8 keys-on-M kernel, a
-    # tree mask runs on the warp-level one (None: pa_verify_plan, which knows
-    # no mask, does not name it)
-    (lambda: W.qwen_u8(6, 2200, seed=105), None, False),
+    (lambda: W.qwen_u8(6, 2200, seed=105), 4, False),   # 24 u8 rows: the u8 keys-on-M kernel
+    (lambda: W.qwen_u8(3, 2200, seed=108), 0, False),
     (lambda: W.make_case("tree_d256", seed=106, query_lens=[4, 6], past_lens=[1500, 700], num_q_heads=32,
                          num_kv_heads=16, head_dim=256, page_size=64), 0, False),
     (lambda: W.tiny(seed=107), 1, True),
@@ -97,9 +95,8 @@ def test_chain_mask_is_the_plain_verify_bit_for_bit(idx):
 
 
 def test_workspace_size_covers_tree_calls():
-    """u8 at 24 rows per KV head: the plain verify runs the keys-on-M u8
-    kernel (one CTA per SM), a tree-mask call the warp-level kernel (two per
-    SM, so more partitions); pa_verify_workspace_size must cover both."""
+    """A tree-mask call with the workspace pa_verify_workspace_size reports
+    (which covers the plain and the tree-mask plans), at 32k keys."""
     import torch
     case = W.qwen_u8(6, 32768, seed=106)
     dev = to_device(case)
