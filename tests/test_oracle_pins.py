@@ -630,3 +630,32 @@ def test_tree_mask_with_no_visible_key_gives_zero(oracle_mod):
                        head_dim=8, page_size=8, q_dtype="f32", kv_dtype="f32")
     got = run_oracle(oracle_mod, case, tree_mask=np.array([0, 3], dtype=np.uint8))
     assert not got[0].any() and np.isfinite(got[1]).all() and got[1].any()
+
+
+def test_page_size_does_not_change_the_result(oracle_mod):
+    """The same logical K/V laid out in 1-token pages (every token its own
+    block, in shuffled order) and in 16-token pages gives bitwise the same
+    output: the page size only changes where a key is stored."""
+    big = W.make_case("ps16", seed=31, query_lens=[3, 2], past_lens=[45, 70], num_q_heads=8, num_kv_heads=2,
+                      head_dim=16, page_size=16, q_dtype="f32", kv_dtype="f32")
+    kc, vc = _decode_cache(big)  # [nb, Hkv, ps, D] dequantised (exact f32 here)
+    rng = np.random.default_rng(32)
+    n_tok = [int(big.past_lens[b]) + int(big.query_lens[b]) for b in range(big.num_seqs)]
+    total = sum(n_tok)
+    perm = rng.permutation(total) + 1
+    k1 = np.full((total + 1, big.num_kv_heads, 1, big.head_dim), np.nan, dtype=np.float32)
+    v1 = k1.copy()
+    bt1 = np.zeros((big.num_seqs, max(n_tok)), dtype=np.int32)
+    cur = 0
+    for b in range(big.num_seqs):
+        for j in range(n_tok[b]):
+            blk16, slot = big.block_tables[b][j // 16], j % 16
+            bt1[b, j] = perm[cur]
+            k1[perm[cur], :, 0] = kc[blk16, :, slot]
+            v1[perm[cur], :, 0] = vc[blk16, :, slot]
+            cur += 1
+    want = run_oracle(oracle_mod, big)
+    got = oracle_mod.forward(big.q, big.q_dtype, k1, v1, "f32", bt1, big.past_lens, big.subsequence_begins,
+                             num_q_heads=big.num_q_heads, num_kv_heads=big.num_kv_heads, head_dim=big.head_dim,
+                             page_size=1, num_blocks=total + 1, scale=big.scale)
+    assert np.array_equal(got, want)
