@@ -83,9 +83,9 @@ class DeviceWorkload:
         cur = 0
         for r in range(self.replicas):
             for b in range(B):
-                for lp in read_pages[b]:
-                    bts[r, b, lp] = perm[cur]
-                    cur += 1
+                n = len(read_pages[b])
+                bts[r, b, read_pages[b][0]: read_pages[b][0] + n] = perm[cur: cur + n].to(torch.int32)
+                cur += n
         self.block_tables = bts.cuda()
         self.block_tables_host = bts.pin_memory()
         gd = torch.Generator(device="cuda").manual_seed(seed + 1)
@@ -182,6 +182,33 @@ class DeviceWorkload:
         return 1 + (1 if self.plan().num_partitions > 1 else 0)
 
 
+def small_page_sweep(stream, hbm_peak, l2):
+    """The same verify step with the cache in 16-token pages and in 1-, 2- or
+    4-token pages (one block-table lookup per key at page size 1)."""
+    import torch
+    rows = []
+    for name, hq, hkv, d, T, L, sizes in (("long_T8_L131072", 64, 8, 128, 8, 131072, (16, 4, 2, 1)),
+                                          ("long_T8_L184320", 64, 8, 128, 8, 184320, (16, 1)),
+                                          ("qwen_gqa_T4_L32768", 32, 8, 128, 4, 32768, (16, 1)),
+                                          ("qwen_gqa_T1_L32768", 32, 8, 128, 1, 32768, (16, 1))):
+        base = None
+        for ps in sizes:
+            w = DeviceWorkload(hq, hkv, d, ps, "bf16", [T], [L], 0, min_bytes=2 * l2, seed=13)
+            u, _, _ = time_graph(w, 200, 3, stream)
+            pm, _ = time_partition_kernel(w, 50, stream)
+            gbs = w.kv_bytes / (u * 1e-6) / 1e9
+            if base is None:
+                base = u
+            rows.append({"workload": name, "page_size": ps, "us_per_step": round(u, 2),
+                         "partition_us": round(pm, 2), "kv_gbs": round(gbs, 1),
+                         "frac_of_measured_hbm": round(gbs / hbm_peak, 3), "ratio_vs_ps16": round(u / base, 3),
+                         "partitions": w.plan().num_partitions, "kernel": kernel_name(w).split(" ")[0]})
+            log(f"[bench] small pages {rows[-1]}")
+            del w
+            torch.cuda.empty_cache()
+    return rows
+
+
 def reduce_max_over_ranks(x: float, device="cpu") -> float:
     """Max of a per-rank float over the process group (identity when not
     distributed): the timed interval of the slowest rank."""
@@ -202,6 +229,8 @@ def whole_job_gbs(bytes_per_rank_step: int, world: int, max_us_per_step: float) 
 
 def kernel_name(wl) -> str:
     p = wl.plan()
+    if p.kernel == 2 and wl.ps < 8:
+        return f"pa_partition_tc<D={wl.D},{wl.kv},gather> (tcgen05, cp.async page gather)"
     if p.kernel == 2:
         return f"pa_partition_tc<D={wl.D}, {wl.kv}> (tcgen05, TMEM accumulators)"
     if p.kernel == 3:
@@ -669,6 +698,8 @@ def run_ours(args, rank, world):
             del w
             torch.cuda.empty_cache()
 
+    small_pages = small_page_sweep(stream, hbm_peak, L2) if (not args.no_sweep and rank == 0) else []
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, per, n, cores = time_oracle(H["q_lens"][0], H["past"][0], args.cpu_seconds)
@@ -706,6 +737,7 @@ def run_ours(args, rank, world):
         "sweep": sweep,
         "cache_update": cache_update,
         "tree_verify": tree_verify,
+        "small_pages": small_pages,
     }
     print(json.dumps(line), flush=True)
 

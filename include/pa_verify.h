@@ -63,7 +63,11 @@ enum {
   PA_ERR_DTYPE = -2,       /* unsupported q / kv / out dtype combination          */
   PA_ERR_SHAPE = -3,       /* non-positive count, Hq % Hkv != 0, bad table width  */
   PA_ERR_HEAD_DIM = -4,    /* head_dim not in {64, 128, 256} (u8: {128, 256})     */
-  PA_ERR_PAGE_SIZE = -5,   /* page_size not a power of two in [8, 256]           */
+  PA_ERR_PAGE_SIZE = -5,   /* page_size not a power of two in [1, 256]; pages of
+                              1, 2 or 4 tokens need an fp32 cache, or a 16-bit
+                              cache with head_dim <= 128 and <= 64 query rows
+                              per KV head (pa_cache_update: any power of two
+                              up to 256)                                      */
   PA_ERR_ALIGN = -6,       /* a pointer misses its alignment                      */
   PA_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than pa_verify_workspace_size */
   PA_ERR_CONTEXT = -8,     /* max_context_len < 1 while tokens are present, or too large */
@@ -109,7 +113,11 @@ typedef struct {
                               M dimension (16-bit KV with D <= 128, or u8 KV with
                               D = 128; 8..64 query rows per KV head),
                               3 = tensor-memory path, keys on the MMA's M dimension
-                              (16-bit KV with D <= 128, up to 64 query rows) */
+                              (16-bit KV with D <= 128, up to 64 query rows),
+                              4 = the same for u8 KV (D = 128, up to 32 rows).
+                              Pages of 1, 2 or 4 tokens with 16-bit KV always
+                              take kernel 2, gathering key rows with 16-byte
+                              cp.async copies instead of TMA boxes            */
   int32_t num_sms;         /* SM count the plan was made for                       */
   int32_t ctas;            /* grid size B * Hkv * P                                */
   int32_t smem_bytes;      /* dynamic shared memory per partition CTA             */

@@ -195,7 +195,7 @@ extern "C" int pa_cache_update(const void* k_new, const void* v_new, pa_dtype sr
     return PA_ERR_SHAPE;
   const int D = d.head_dim;
   if (D != 64 && D != 128 && D != 256) return PA_ERR_HEAD_DIM;
-  if (!pow2(d.page_size) || d.page_size < 8 || d.page_size > 256) return PA_ERR_PAGE_SIZE;
+  if (!pow2(d.page_size) || d.page_size > 256) return PA_ERR_PAGE_SIZE;
   if (src_dtype != PA_F32 && src_dtype != PA_F16 && src_dtype != PA_BF16) return PA_ERR_DTYPE;
   if (kv_dtype != PA_F32 && kv_dtype != PA_F16 && kv_dtype != PA_BF16 && kv_dtype != PA_U8) return PA_ERR_DTYPE;
   if (kv_dtype == PA_U8 && D == 64) return PA_ERR_HEAD_DIM;

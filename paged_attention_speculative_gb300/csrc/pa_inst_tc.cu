@@ -2,29 +2,16 @@
 #include "pa_launch.h"
 #include "pa_partition_tc.cuh"
 #include "pa_partition_tcu8.cuh"
+#include "pa_inst_tc.cuh"
 
 namespace pa {
 
 namespace {
-template <int D, int KV, bool TREE>
-cudaError_t launch_tc_tt(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid, cudaStream_t st) {
-  auto kern = pa_partition_tc<D, KV, TREE>;
-  const int smem = TcCfg<D, KV>::BYTES;
-  static int configured_for[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && !__atomic_load_n(&configured_for[dev], __ATOMIC_ACQUIRE)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
-  }
-  return launch_dependent(kern, grid, dim3(128), smem, st, k, v, a);
-}
 template <int D, int KV>
 cudaError_t launch_tc_t(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid, cudaStream_t st) {
-  return a.tree_mask != nullptr ? launch_tc_tt<D, KV, true>(k, v, a, grid, st)
-                                : launch_tc_tt<D, KV, false>(k, v, a, grid, st);
+  if (a.ps < kGatherBelowPageSize) return launch_tc_gather(D, KV, a, grid, st);
+  return a.tree_mask != nullptr ? launch_tc_tt<D, KV, true, false>(k, v, a, grid, st)
+                                : launch_tc_tt<D, KV, false, false>(k, v, a, grid, st);
 }
 cudaError_t launch_tcu8_128(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                             cudaStream_t st) {

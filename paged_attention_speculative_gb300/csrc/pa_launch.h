@@ -54,6 +54,10 @@ cudaError_t launch_mma_d256(int kv, int nt, const CUtensorMap& k, const CUtensor
 MmaKernelInfo tc_info(int D, int kv, bool* ok);
 cudaError_t launch_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                       cudaStream_t st);
+// Pages smaller than this many tokens take the cp.async-gather producer of
+// the 16-bit tensor-memory kernel (launch_tc forwards them; no tensor maps).
+constexpr int kGatherBelowPageSize = 8;
+cudaError_t launch_tc_gather(int D, int kv, const PartArgs& a, dim3 grid, cudaStream_t st);
 
 // Tensor-memory partition kernels with the keys on the MMA's M dimension:
 // head_dim 64 / 128, KV_BF16 / KV_F16 caches, row tiles n = 16 / 32 / 64.

@@ -160,7 +160,11 @@ struct TcCfg {
   static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory budget");
 };
 
-template <int D, int KV, bool TREE = false>
+// GATHER (pages of 1, 2 or 4 tokens): the producer warp fetches key rows
+// with 16-byte cp.async copies instead of TMA boxes; block ids are looked up
+// per key, one stage ahead.  Everything downstream of the stage ring is the
+// same kernel.
+template <int D, int KV, bool TREE = false, bool GATHER = false>
 __global__ void __launch_bounds__(128, 1)
     pa_partition_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const PartArgs a) {
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(128, 1)
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so the producer starts fetching its
   // block-table slice before the sequence's bounds are known.
-  const bool prefetch = (warp == 3 && a.window == 0);
+  const bool prefetch = (!GATHER && warp == 3 && a.window == 0);
   if (prefetch) {
     const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
     const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
@@ -279,7 +283,96 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tm_p0 = tmem + C::P_COL;          // P buffers (16-bit pairs)
   const uint32_t tm_q = tmem + C::Q_COL;           // Q (16-bit pairs)
 
-  if (warp == 3) {
+  if (GATHER && warp == 3) {
+    // ======================= cp.async gather producer =======================
+    // Lane (h, u): 16-byte unit u of key row h of each group of KPI keys, so
+    // one warp instruction copies KPI whole rows (256 or 128 contiguous bytes
+    // each).  A stage's copies form one group; stage s is published once
+    // group s has landed, DEPTH groups behind the newest, so DEPTH + 1 stages
+    // are in flight.
+    constexpr int UPK = D * 2 / 16;  // 16-byte units per key row
+    constexpr int KPI = 32 / UPK;    // key rows per warp instruction
+    constexpr int DEPTH = 2;
+    static_assert(C::NS >= DEPTH + 2, "the ring must hold the stages in flight plus the one being consumed");
+    const int u = lane % UPK, h = lane / UPK;
+    const int c = u >> 3, w = u & 7;
+    const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
+    const size_t blk_bytes = static_cast<size_t>(a.Hkv) * a.ps * D * 2;
+    const uint8_t* kb = a.k_bytes + static_cast<size_t>(g) * a.ps * D * 2 + 16 * u;
+    const uint8_t* vb = a.v_bytes + static_cast<size_t>(g) * a.ps * D * 2 + 16 * u;
+    int bad = 0;
+    // ids of keys key0 + lane and key0 + 32 + lane; -1 past the partition
+    auto load_ids = [&](int s, int& i0, int& i1) {
+      const int k0 = kstart + s * C::SK + lane, k1 = k0 + 32;
+      i0 = -1;
+      i1 = -1;
+      if (k0 < kend) {
+        i0 = __ldg(bt + (k0 >> a.ps_log2));
+        if (static_cast<unsigned>(i0) >= static_cast<unsigned>(a.num_blocks)) {
+          bad = 1;
+          i0 = 0;
+        }
+      }
+      if (k1 < kend) {
+        i1 = __ldg(bt + (k1 >> a.ps_log2));
+        if (static_cast<unsigned>(i1) >= static_cast<unsigned>(a.num_blocks)) {
+          bad = 1;
+          i1 = 0;
+        }
+      }
+    };
+    int nid0, nid1;
+    load_ids(0, nid0, nid1);
+    int issued = 0;
+    for (int s = 0; s < n_stages; ++s) {
+      const int slot = s % C::NS;
+      if (s >= C::NS && !mbar_wait(&empty[slot], ((s / C::NS) - 1) & 1)) {
+        if (lane == 0) {
+          atomicOr(a.status, PA_STATUS_TIMEOUT);
+          atomicOr(&s_timeout, 1);
+        }
+        break;
+      }
+      const int id0 = nid0, id1 = nid1;
+      if (s + 1 < n_stages) load_ids(s + 1, nid0, nid1);
+      const int key0 = kstart + s * C::SK;
+      uint8_t* st = smem + slot * C::STAGE;
+#pragma unroll
+      for (int i = 0; i < C::SK / KPI; ++i) {
+        const int kl = i * KPI + h;  // key row within the stage
+        const int id = __shfl_sync(0xffffffffu, (i * KPI < 32) ? id0 : id1, kl & 31);
+        const int key = key0 + kl;
+        const size_t src = static_cast<size_t>(id < 0 ? 0 : id) * blk_bytes +
+                           static_cast<size_t>(key & (a.ps - 1)) * (D * 2);
+        // tile layout [chunk][key][128 B], 16-byte units swizzled by key & 7
+        const uint32_t dst = static_cast<uint32_t>((c * C::SK + kl) * 128 + ((w ^ (kl & 7)) << 4));
+        const uint32_t n = id < 0 ? 0u : 16u;  // past the partition: zeros
+        cp_async16(st + dst, kb + src, n);
+        cp_async16(st + C::TILE + dst, vb + src, n);
+        if (a.trace != nullptr && u == 0 && id >= 0 && (key & (a.ps - 1)) == 0)
+          atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + (key >> a.ps_log2), id + 1);
+      }
+      cp_async_commit();
+      issued = s + 1;
+      if (s >= DEPTH) {
+        cp_async_wait_group<DEPTH>();
+        fence_proxy_async();  // the copies, seen by the tensor cores' proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[(s - DEPTH) % C::NS]);
+      }
+    }
+    cp_async_wait_all();
+    fence_proxy_async();
+    // the flag is set before the last stages are published, so the softmax
+    // warps see it once their last PV has completed
+    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+      s_bad = 1;
+      atomicOr(a.status, PA_STATUS_BLOCK_ID);
+    }
+    __syncwarp();
+    if (lane == 0)
+      for (int q = max(0, issued - DEPTH); q < issued; ++q) mbar_arrive(&full[q % C::NS]);
+  } else if (warp == 3) {
     // =========================== TMA producer ===============================
     if (lane == 0) {
       prefetch_tensormap(&tmK);

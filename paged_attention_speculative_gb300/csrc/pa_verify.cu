@@ -91,7 +91,13 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   if (D != 64 && D != 128 && D != 256) return PA_ERR_HEAD_DIM;
   if (kv == PA_U8 && D == 64) return PA_ERR_HEAD_DIM;
   const int ps = d->page_size;
-  if (!pow2(ps) || ps < 8 || ps > 256) return PA_ERR_PAGE_SIZE;
+  if (!pow2(ps) || ps > 256) return PA_ERR_PAGE_SIZE;
+  // Pages of 1, 2 or 4 tokens: fp32 caches (the FFMA kernel looks every key
+  // up anyway) and 16-bit caches with head_dim <= 128 (the tensor-memory
+  // kernel's cp.async-gather producer).  The other kernels stage whole pages
+  // with TMA boxes and take 8 tokens or more.
+  const bool small_pages = ps < pa::kGatherBelowPageSize;
+  if (small_pages && !(kv == PA_F32 || ((kv == PA_BF16 || kv == PA_F16) && D <= 128))) return PA_ERR_PAGE_SIZE;
   const pa_dtype qd = d->q_dtype, od = d->out_dtype;
   if (od != PA_F32 && od != PA_F16 && od != PA_BF16) return PA_ERR_DTYPE;
   bool combo = (kv == PA_F32 && (qd == PA_F32 || qd == PA_F16 || qd == PA_BF16)) ||
@@ -115,13 +121,13 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   // path is slightly faster.
   const bool tc16 = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128);
   const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
-  // tree masks run on the warp-level, fp32 and rows-on-M tensor-memory
-  // kernels only; a forced keys-on-M or u8 tensor-memory choice falls back
   // tree masks run on every kernel but the 16-bit keys-on-M one and the u8
-  // rows-on-M tensor-memory one: a forced choice of those falls back
-  const int choice = (tree && (env_kernel_choice() == 3 && kv != PA_U8)) ? 0
-                     : (tree && env_kernel_choice() == 2 && kv == PA_U8) ? 0
-                                                                        : env_kernel_choice();
+  // rows-on-M tensor-memory one: a forced choice of those falls back.  Small
+  // pages always take the rows-on-M tensor-memory kernel (16-bit caches).
+  const int choice = small_pages                                             ? 2
+                     : (tree && (env_kernel_choice() == 3 && kv != PA_U8)) ? 0
+                     : (tree && env_kernel_choice() == 2 && kv == PA_U8)   ? 0
+                                                                           : env_kernel_choice();
   // u8 caches take the tensor-memory kernel only when forced (tuning).
   // u8 caches with 17..32 query rows per KV head: the keys-on-M kernel's
   // cost does not grow with the rows, while the warp-level kernel converts
@@ -170,6 +176,7 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
       ctas_per_sm = info.ctas_per_sm;
     }
   }
+  if (small_pages && kernel != 1 && kernel != 2) return PA_ERR_PAGE_SIZE;  // more than 64 rows per KV head
   if (kernel == 0) {
     // one 8-row n-tile per warp keeps a warp's accumulators within the
     // register budget of two CTAs per SM; rows beyond 8 go to more warps
@@ -195,7 +202,11 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   if (env_part_tokens() > 0) part = env_part_tokens();
   part = round_up(std::max<long long>(part, 1), quantum);
   part = std::min(part, round_up(span, quantum));
-  const long long page_cap = (static_cast<long long>(pa::kMaxPagesPerCta - 1) * ps / quantum) * quantum;
+  // kernels that stage the partition's block ids in shared memory take at
+  // most kMaxPagesPerCta pages per CTA; the small-page paths look ids up per
+  // stage and have no such cap
+  const long long page_cap = small_pages ? round_up(span, quantum)
+                                         : (static_cast<long long>(pa::kMaxPagesPerCta - 1) * ps / quantum) * quantum;
   part = std::min(part, std::max(page_cap, quantum));
   if (env_part_tokens() <= 0) {
     // Rounding can leave a last wave of CTAs that is mostly empty; a larger
@@ -371,6 +382,8 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
     if (rc != PA_OK) return rc;
     e = plan.kernel == 3 ? pa::launch_tk(d->head_dim, mma_kind(c.kv), plan.row_tiles, mk, mv, a, grid, c.stream)
                          : pa::launch_tku8(plan.row_tiles, mk, mv, a, grid, c.stream);
+  } else if (plan.kernel == 2 && d->page_size < pa::kGatherBelowPageSize) {
+    e = pa::launch_tc_gather(d->head_dim, mma_kind(c.kv), a, grid, c.stream);
   } else if (plan.kernel == 2) {
     CUtensorMap mk, mv;
     int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);

@@ -258,10 +258,14 @@ def tiny(seed: int = 0) -> Case:
                      num_kv_heads=2, head_dim=64, page_size=16, q_dtype="f32", kv_dtype="f32")
 
 
-def qwen_gqa(T: int, L: int, seed: int = 0, **kw) -> Case:
+def _ps_tag(page_size: int) -> str:
+    return "" if page_size == 16 else f"_ps{page_size}"
+
+
+def qwen_gqa(T: int, L: int, seed: int = 0, page_size: int = 16, **kw) -> Case:
     """Qwen-like GQA verify: batch 1, 32 q / 8 KV heads, D=128, page 16, bf16."""
-    return make_case(f"qwen_gqa_T{T}_L{L}", seed=seed, query_lens=[T], past_lens=[L], num_q_heads=32,
-                     num_kv_heads=8, head_dim=128, page_size=16, **kw)
+    return make_case(f"qwen_gqa_T{T}_L{L}{_ps_tag(page_size)}", seed=seed, query_lens=[T], past_lens=[L],
+                     num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=page_size, **kw)
 
 
 def qwen_u8(T: int, L: int, seed: int = 0, **kw) -> Case:
@@ -288,10 +292,43 @@ def batched_mix_a(seed: int = 0, **kw) -> Case:
                      num_kv_heads=16, head_dim=256, page_size=64, sliding_window=1024, **kw)
 
 
-def long_ctx_b(L: int, T: int = 8, seed: int = 0, **kw) -> Case:
-    """Batch 1, T=8, 64 q / 8 KV heads, D=128, page 16, bf16 (128k-185k context)."""
-    return make_case(f"long_T{T}_L{L}", seed=seed, query_lens=[T], past_lens=[L], num_q_heads=64,
-                     num_kv_heads=8, head_dim=128, page_size=16, **kw)
+def long_ctx_b(L: int, T: int = 8, seed: int = 0, page_size: int = 16, **kw) -> Case:
+    """Batch 1, T=8, 64 q / 8 KV heads, D=128, page 16, bf16 (128k-185k context).
+    page_size=1 is the one-token-per-page layout of the long-context stress
+    case (every key its own block-table lookup)."""
+    return make_case(f"long_T{T}_L{L}{_ps_tag(page_size)}", seed=seed, query_lens=[T], past_lens=[L],
+                     num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=page_size, **kw)
+
+
+def relayout(case: Case, page_size: int, seed: int = 0) -> Case:
+    """The same logical K/V (float or 16-bit caches) in pages of `page_size`
+    tokens: a fresh shuffled block table, every unreferenced slot NaN."""
+    assert case.kv_dtype != "u8"
+    ps0, ps = case.page_size, page_size
+    rng = np.random.default_rng(seed)
+    n_tok = (case.past_lens.astype(np.int64) + case.query_lens.astype(np.int64))
+    pages = [int(math.ceil(int(n) / ps)) for n in n_tok]
+    used = int(sum(pages))
+    nb = used + max(2, used // 10)
+    perm = rng.permutation(nb).astype(np.int32)
+    max_blocks = max(pages) + 1
+    bt = np.empty((case.num_seqs, max_blocks), dtype=np.int32)
+    shape = (nb, case.num_kv_heads, ps, case.head_dim)
+    k = to_storage(np.full(shape, np.nan, dtype=np.float32), case.kv_dtype)
+    v = k.copy()
+    cur = 0
+    for b in range(case.num_seqs):
+        bt[b, : pages[b]] = perm[cur: cur + pages[b]]
+        spare = perm[used:]  # unreferenced (all-NaN) blocks fill the table's tail
+        bt[b, pages[b]:] = spare[np.arange(max_blocks - pages[b]) % len(spare)]
+        cur += pages[b]
+        j = np.arange(int(n_tok[b]))
+        src_blk, src_slot = case.block_tables[b][j // ps0], j % ps0
+        dst_blk, dst_slot = bt[b][j // ps], j % ps
+        k[dst_blk, :, dst_slot] = case.k_cache[src_blk, :, src_slot]
+        v[dst_blk, :, dst_slot] = case.v_cache[src_blk, :, src_slot]
+    return dataclasses.replace(case, name=f"{case.name}_as_ps{ps}", k_cache=k, v_cache=v, block_tables=bt,
+                               page_size=ps, num_blocks=nb)
 
 
 def new_tokens(case: Case, src_dtype: str = "bf16", seed: int = 0, specials: bool = False):

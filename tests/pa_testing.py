@@ -116,3 +116,26 @@ def max_abs_err(got, want):
     assert got.shape == want.shape
     assert np.isfinite(got).all(), f"{np.count_nonzero(~np.isfinite(got))} non-finite outputs"
     return float(np.max(np.abs(got - want))) if got.size else 0.0
+
+
+def check_parity(case, out_dtype=None, tol=TOL):
+    """GPU output and gather trace against the oracle.  tol: the flat 2e-3
+    bound for the pages' long-context workloads, or "derived"
+    (derived_tolerance) for short-context edge cases whose outputs are O(1),
+    where one bf16 rounding alone exceeds 2e-3."""
+    got, bits, trace = run_gpu(case, out_dtype=out_dtype, traced=True)
+    assert bits == 0, f"device status {bits:#x}"
+    want = run_oracle(case)
+    err = max_abs_err(got, want)
+    if isinstance(tol, str):
+        bound = derived_tolerance(case, want, out_dtype)
+        worst = float(np.max(np.abs(got - want) - bound))
+        assert worst <= 0.0, f"{case.name}: error exceeds the derived bound by {worst:.3e} (max abs {err:.3e})"
+    else:
+        assert err <= tol, f"{case.name}: max abs err {err:.3e}"
+    import oracle
+    pages = oracle.pages_touched(case.block_tables, case.past_lens, case.subsequence_begins,
+                                 page_size=case.page_size, sliding_window=case.sliding_window)
+    for g in range(case.num_kv_heads):
+        assert np.array_equal(trace[:, g, :], pages), f"{case.name}: gather trace of KV head {g} differs"
+    return err

@@ -10,31 +10,9 @@ import pytest
 
 from paged_attention_speculative_gb300 import workloads as W
 
-from pa_testing import TOL, derived_tolerance, max_abs_err, run_gpu, run_oracle, to_device
+from pa_testing import TOL, check_parity as _check, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
-
-
-def _check(case, out_dtype=None, tol=TOL):
-    """tol: the flat 2e-3 bound for the pages' long-context workloads, or
-    "derived" (see pa_testing.derived_tolerance) for short-context edge cases
-    whose outputs are O(1), where one bf16 rounding alone exceeds 2e-3."""
-    got, bits, trace = run_gpu(case, out_dtype=out_dtype, traced=True)
-    assert bits == 0, f"device status {bits:#x}"
-    want = run_oracle(case)
-    err = max_abs_err(got, want)
-    if isinstance(tol, str):
-        bound = derived_tolerance(case, want, out_dtype)
-        worst = float(np.max(np.abs(got - want) - bound))
-        assert worst <= 0.0, f"{case.name}: error exceeds the derived bound by {worst:.3e} (max abs {err:.3e})"
-    else:
-        assert err <= tol, f"{case.name}: max abs err {err:.3e}"
-    import oracle
-    pages = oracle.pages_touched(case.block_tables, case.past_lens, case.subsequence_begins,
-                                 page_size=case.page_size, sliding_window=case.sliding_window)
-    for g in range(case.num_kv_heads):
-        assert np.array_equal(trace[:, g, :], pages), f"{case.name}: gather trace of KV head {g} differs"
-    return err
 
 
 EDGE = {"batch_edge", "window1", "f32_win_batch"}

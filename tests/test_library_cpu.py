@@ -98,7 +98,12 @@ def test_plan_rejections(lib):
         (dims(head_dim=96), pa.PA_BF16, -4),
         (dims(head_dim=64), pa.PA_U8, -4),
         (dims(page_size=12), pa.PA_BF16, -5),
-        (dims(page_size=4), pa.PA_BF16, -5),
+        (dims(page_size=3), pa.PA_BF16, -5),
+        (dims(page_size=512), pa.PA_BF16, -5),
+        (dims(page_size=4), pa.PA_U8, -5),
+        (dims(page_size=2, head_dim=256), pa.PA_BF16, -5),
+        (dims(page_size=1, num_q_heads=128, num_kv_heads=8, total_tokens=8, max_blocks_per_seq=8192), pa.PA_BF16,
+         -5),
         (dims(num_q_heads=30), pa.PA_BF16, -3),
         (dims(q_dtype=pa.PA_F16), pa.PA_BF16, -2),
         (dims(out_dtype=pa.PA_U8), pa.PA_BF16, -2),
@@ -109,6 +114,26 @@ def test_plan_rejections(lib):
     assert lib.pa_verify_plan(ctypes.byref(dims()), 0, 0, pa.PA_BF16, 152, ctypes.byref(p)) == -8
     assert lib.pa_verify_plan(ctypes.byref(dims()), 2100 * 16 + 1, 0, pa.PA_BF16, 152, ctypes.byref(p)) == -8
     assert lib.pa_verify_plan(None, 4096, 0, pa.PA_BF16, 152, ctypes.byref(p)) == -1
+
+
+def test_plan_small_pages(lib):
+    """Pages of 1, 2 or 4 tokens: 16-bit caches take the tensor-memory kernel
+    (its cp.async-gather producer) whatever the row count, with partitions
+    free of the per-CTA page-list cap; fp32 caches keep the FFMA kernel."""
+    p = pa.PaPlan()
+    for ps in (1, 2, 4):
+        for hq, t in ((32, 1), (32, 4), (64, 8)):
+            d = dims(page_size=ps, num_q_heads=hq, total_tokens=t, max_blocks_per_seq=131072 // ps + 8)
+            assert lib.pa_verify_plan(ctypes.byref(d), 131072 + t, 0, pa.PA_BF16, 152, ctypes.byref(p)) == 0
+            assert p.kernel == 2 and p.part_tokens % 64 == 0
+            assert p.part_tokens > 1024  # more pages per CTA than a staged page list holds
+            assert p.num_partitions * p.part_tokens >= 131072 + t
+        d = dims(page_size=ps, head_dim=64, num_q_heads=8, num_kv_heads=2, total_tokens=3, q_dtype=pa.PA_F16)
+        assert lib.pa_verify_plan(ctypes.byref(d), 600, 0, pa.PA_F16, 152, ctypes.byref(p)) == 0
+        assert p.kernel == 2
+        d = dims(page_size=ps, q_dtype=pa.PA_F32, max_blocks_per_seq=4096)
+        assert lib.pa_verify_plan(ctypes.byref(d), 4000, 0, pa.PA_F32, 152, ctypes.byref(p)) == 0
+        assert p.kernel == 1
 
 
 def test_forward_host_errors_need_no_gpu(lib):
