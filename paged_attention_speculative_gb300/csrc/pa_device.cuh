@@ -20,6 +20,7 @@ enum KvKind : int { KV_BF16 = 0, KV_F16 = 1, KV_U8 = 2 };
 constexpr int kConsumerWarps = 4;            // warps that do the math
 constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one TMA producer warp
 constexpr int kMaxPagesPerCta = 1024;        // block ids staged in shared memory
+constexpr int kGatherWarps = 4;              // cp.async producer warps of the small-page gather
 constexpr uint32_t kWaitLimit = 1u << 22;    // bounded mbarrier polls before giving up
 
 // Arguments common to the partition kernels (plain values, passed by value).

@@ -20,7 +20,7 @@ cudaError_t launch_tc_tt(const CUtensorMap& k, const CUtensorMap& v, const PartA
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  return launch_dependent(kern, grid, dim3(128), smem, st, k, v, a);
+  return launch_dependent(kern, grid, dim3(GATHER ? 128 + 32 * kGatherWarps : 128), smem, st, k, v, a);
 }
 
 }  // namespace pa

@@ -160,12 +160,12 @@ struct TcCfg {
   static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory budget");
 };
 
-// GATHER (pages of 1, 2 or 4 tokens): the producer warp fetches key rows
-// with 16-byte cp.async copies instead of TMA boxes; block ids are looked up
-// per key, one stage ahead.  Everything downstream of the stage ring is the
-// same kernel.
+// GATHER (pages of 1, 2 or 4 tokens): four more warps (4..7, one per SM
+// sub-partition) fetch key rows with 16-byte cp.async copies instead of TMA
+// boxes, block ids looked up per key; warp 3 has no role.  Everything
+// downstream of the stage ring is the same kernel.
 template <int D, int KV, bool TREE = false, bool GATHER = false>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
     pa_partition_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const PartArgs a) {
   using C = TcCfg<D, KV>;
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(128, 1)
     s_bad = 0;
     s_timeout = 0;
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], GATHER ? kGatherWarps : 1);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -283,46 +283,37 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tm_p0 = tmem + C::P_COL;          // P buffers (16-bit pairs)
   const uint32_t tm_q = tmem + C::Q_COL;           // Q (16-bit pairs)
 
-  if (GATHER && warp == 3) {
-    // ======================= cp.async gather producer =======================
-    // Lane (h, u): 16-byte unit u of key row h of each group of KPI keys, so
-    // one warp instruction copies KPI whole rows (256 or 128 contiguous bytes
-    // each).  A stage's copies form one group; stage s is published once
-    // group s has landed, DEPTH groups behind the newest, so DEPTH + 1 stages
-    // are in flight.
+  if (GATHER && warp >= 4) {
+    // ======================= cp.async gather producers ======================
+    // Warp 4 + pw copies key rows [16 pw, 16 pw + 16) of every stage.  Lane
+    // (h, u): 16-byte unit u of key row h of each group of KPI rows, so one
+    // warp instruction copies KPI whole rows (256 or 128 contiguous bytes
+    // each).  A warp's copies of one stage form one group; the warp arrives
+    // on the stage's barrier once that group has landed, DEPTH groups behind
+    // its newest, so DEPTH + 1 stages are in flight and the ring keeps two
+    // more for the consumers (the stage whose PV is pending and the next
+    // one's scores).  Block ids are loaded two stages ahead and checked only
+    // when used, so no load latency sits between two stages' copies.
     constexpr int UPK = D * 2 / 16;  // 16-byte units per key row
     constexpr int KPI = 32 / UPK;    // key rows per warp instruction
-    constexpr int DEPTH = 2;
-    static_assert(C::NS >= DEPTH + 2, "the ring must hold the stages in flight plus the one being consumed");
+    constexpr int ROWS_W = C::SK / kGatherWarps;
+    constexpr int DEPTH = (C::NS - 3) < 5 ? (C::NS - 3) : 5;
+    static_assert(DEPTH >= 2, "the ring must hold the stages in flight plus two being consumed");
+    static_assert(ROWS_W <= 32 && ROWS_W % KPI == 0, "one id per lane covers a warp's rows");
+    const int pw = warp - 4;
     const int u = lane % UPK, h = lane / UPK;
     const int c = u >> 3, w = u & 7;
     const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
-    const size_t blk_bytes = static_cast<size_t>(a.Hkv) * a.ps * D * 2;
+    const uint64_t blk_bytes = static_cast<uint64_t>(a.Hkv) * a.ps * D * 2;
     const uint8_t* kb = a.k_bytes + static_cast<size_t>(g) * a.ps * D * 2 + 16 * u;
     const uint8_t* vb = a.v_bytes + static_cast<size_t>(g) * a.ps * D * 2 + 16 * u;
     int bad = 0;
-    // ids of keys key0 + lane and key0 + 32 + lane; -1 past the partition
-    auto load_ids = [&](int s, int& i0, int& i1) {
-      const int k0 = kstart + s * C::SK + lane, k1 = k0 + 32;
-      i0 = -1;
-      i1 = -1;
-      if (k0 < kend) {
-        i0 = __ldg(bt + (k0 >> a.ps_log2));
-        if (static_cast<unsigned>(i0) >= static_cast<unsigned>(a.num_blocks)) {
-          bad = 1;
-          i0 = 0;
-        }
-      }
-      if (k1 < kend) {
-        i1 = __ldg(bt + (k1 >> a.ps_log2));
-        if (static_cast<unsigned>(i1) >= static_cast<unsigned>(a.num_blocks)) {
-          bad = 1;
-          i1 = 0;
-        }
-      }
+    // raw id of key row `lane` of this warp's slice (0 past the partition)
+    auto load_id = [&](int s) -> int {
+      const int k = kstart + s * C::SK + pw * ROWS_W + lane;
+      return (lane < ROWS_W && k < kend) ? __ldg(bt + (k >> a.ps_log2)) : 0;
     };
-    int nid0, nid1;
-    load_ids(0, nid0, nid1);
+    int na = load_id(0), nb = load_id(1);  // ids of the next stage and of the one after
     int issued = 0;
     for (int s = 0; s < n_stages; ++s) {
       const int slot = s % C::NS;
@@ -333,23 +324,28 @@ __global__ void __launch_bounds__(128, 1)
         }
         break;
       }
-      const int id0 = nid0, id1 = nid1;
-      if (s + 1 < n_stages) load_ids(s + 1, nid0, nid1);
+      int idl = na;
+      na = nb;
+      if (s + 2 < n_stages) nb = load_id(s + 2);
+      if (static_cast<unsigned>(idl) >= static_cast<unsigned>(a.num_blocks)) {
+        bad = 1;
+        idl = 0;
+      }
       const int key0 = kstart + s * C::SK;
       uint8_t* st = smem + slot * C::STAGE;
 #pragma unroll
-      for (int i = 0; i < C::SK / KPI; ++i) {
-        const int kl = i * KPI + h;  // key row within the stage
-        const int id = __shfl_sync(0xffffffffu, (i * KPI < 32) ? id0 : id1, kl & 31);
+      for (int i = 0; i < ROWS_W / KPI; ++i) {
+        const int r = i * KPI + h;        // row within this warp's slice
+        const int kl = pw * ROWS_W + r;   // key row within the stage
+        const int id = __shfl_sync(0xffffffffu, idl, r);
         const int key = key0 + kl;
-        const size_t src = static_cast<size_t>(id < 0 ? 0 : id) * blk_bytes +
-                           static_cast<size_t>(key & (a.ps - 1)) * (D * 2);
+        const uint64_t src = static_cast<uint64_t>(id) * blk_bytes + static_cast<uint32_t>(key & (a.ps - 1)) * (D * 2);
         // tile layout [chunk][key][128 B], 16-byte units swizzled by key & 7
         const uint32_t dst = static_cast<uint32_t>((c * C::SK + kl) * 128 + ((w ^ (kl & 7)) << 4));
-        const uint32_t n = id < 0 ? 0u : 16u;  // past the partition: zeros
+        const uint32_t n = key < kend ? 16u : 0u;  // past the partition: zeros
         cp_async16(st + dst, kb + src, n);
         cp_async16(st + C::TILE + dst, vb + src, n);
-        if (a.trace != nullptr && u == 0 && id >= 0 && (key & (a.ps - 1)) == 0)
+        if (a.trace != nullptr && u == 0 && key < kend && (key & (a.ps - 1)) == 0)
           atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + (key >> a.ps_log2), id + 1);
       }
       cp_async_commit();
@@ -372,6 +368,8 @@ __global__ void __launch_bounds__(128, 1)
     __syncwarp();
     if (lane == 0)
       for (int q = max(0, issued - DEPTH); q < issued; ++q) mbar_arrive(&full[q % C::NS]);
+  } else if (GATHER && warp == 3) {
+    // no role in the gather variant
   } else if (warp == 3) {
     // =========================== TMA producer ===============================
     if (lane == 0) {

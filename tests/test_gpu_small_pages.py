@@ -110,3 +110,27 @@ def test_bad_block_id_in_a_one_token_page_sets_the_status():
     bad = W.Case(**{**case.__dict__, "block_tables": bt})
     got, bits, _ = run_gpu(bad)
     assert bits & 0x4  # PA_STATUS_BLOCK_ID
+
+
+@pytest.mark.parametrize("make", [
+    lambda: W.long_ctx_b(3000, page_size=1, seed=55),
+    lambda: W.make_case("ps2_tree_batch_win", seed=56, query_lens=[5, 0, 8, 3], past_lens=[900, 10, 1300, 40],
+                        num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=2, sliding_window=400),
+])
+def test_tree_mask_on_small_pages(make):
+    import oracle
+    from test_gpu_tree import _gpu_tree, random_tree_masks
+    from pa_testing import derived_tolerance
+    case = make()
+    mask = random_tree_masks(case, seed=3)
+    want = oracle.forward(case.q, case.q_dtype, case.k_cache, case.v_cache, case.kv_dtype, case.block_tables,
+                          case.past_lens, case.subsequence_begins, num_q_heads=case.num_q_heads,
+                          num_kv_heads=case.num_kv_heads, head_dim=case.head_dim, page_size=case.page_size,
+                          num_blocks=case.num_blocks, scale=case.scale, sliding_window=case.sliding_window,
+                          tree_mask=mask)
+    got, bits, k, _ = _gpu_tree(case, mask)
+    assert bits == 0 and k == 2
+    if case.sliding_window:  # short windows: O(1) outputs, the derived bound
+        assert float(np.max(np.abs(got - want) - derived_tolerance(case, want))) <= 0.0
+    else:
+        assert float(np.max(np.abs(got - want))) <= TOL
