@@ -13,6 +13,7 @@
  * result up to rounding order):
  *
  *   For every sequence b, every new token i < T_b and every query head h
+ *   (any T_b: a verify step brings a few tokens, a prefill chunk many)
  *     p   = past_len_b + i                       absolute position of token i
  *     g   = h / (Hq / Hkv)                       KV head shared by the GQA group
  *     lo  = W > 0 ? max(0, p - W + 1) : 0         first visible key
@@ -167,8 +168,8 @@ int pa_oracle_forward_tree(const void* q, int q_dtype, const void* k_cache, cons
     const long L = past_lens[b];
     const long p = L + i;
     const long lo = sliding_window > 0 ? (p - sliding_window + 1 > 0 ? p - sliding_window + 1 : 0) : 0;
-    /* the new tokens this one attends: its tree mask, or the causal chain 0..i */
-    const unsigned m = tree_mask ? (unsigned)tree_mask[t] : ((2u << i) - 1u);
+    /* with a tree mask, the new tokens this one attends are the bits of its mask */
+    const unsigned m = tree_mask ? (unsigned)tree_mask[t] : 0u;
     const long last = L + T - 1; /* the last key any row of the sequence may see */
     double* o = out + ((size_t)t * Hq + h) * D;
     for (int d = 0; d < D; ++d) o[d] = 0.0;
@@ -182,13 +183,15 @@ int pa_oracle_forward_tree(const void* q, int q_dtype, const void* k_cache, cons
       bad = 1;
       continue;
     }
-    /* scores s_j = scale * q . K_j over the visible keys: j >= lo, and either
-       a past key (j < L) or a new token whose bit is set */
+    /* scores s_j = scale * q . K_j over the visible keys: j >= lo, and
+       without a tree mask j <= p (the causal rule, for any number of new
+       tokens); with one, either a past key (j < L) or a new token whose bit
+       is set */
     const size_t qoff = ((size_t)t * Hq + h) * D;
     double smax = -INFINITY;
     int row_bad = 0, seen = 0;
     for (long j = lo; j <= last; ++j) {
-      const int vis = j < L || ((m >> (j - L)) & 1u);
+      const int vis = tree_mask ? (j < L || ((m >> (j - L)) & 1u)) : (j <= p);
       if (!vis) {
         s[j - lo] = -INFINITY;
         continue;

@@ -6,7 +6,10 @@ a library attention routine on the T=1 case, closed forms (W=1, q=0, equal
 keys, a window covering everything), the invariant that a T-token verify
 equals T single-token decodes with key limits past_len+i+1 (OpenVINO issue
 38153, Suggestion paragraph), block-table permutation, causal and window
-perturbation, the convex-hull bound, and u8 == float on the dequantised cache.
+perturbation, the convex-hull bound, and u8 == float on the dequantised cache;
+for prefill chunks and mixed batches, the dense brute force, torch's causal
+attention at past_len 0, single-token decodes beyond 32 new tokens, and the
+independence of a batch's sequences.
 """
 import json
 import math
@@ -659,3 +662,84 @@ def test_page_size_does_not_change_the_result(oracle_mod):
                              num_q_heads=big.num_q_heads, num_kv_heads=big.num_kv_heads, head_dim=big.head_dim,
                              page_size=1, num_blocks=total + 1, scale=big.scale)
     assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# Mixed batches: prefill chunks (many new tokens) beside verify steps.  The
+# causal rule is the same for any number of new tokens: token i of sequence b
+# sees keys lo_i .. past_len_b + i.
+# ---------------------------------------------------------------------------
+
+def prefill_cases():
+    return [
+        W.make_case("prefill_no_past", seed=61, query_lens=[40], past_lens=[0], num_q_heads=4, num_kv_heads=2,
+                    head_dim=16, page_size=8, q_dtype="f32", kv_dtype="f32"),
+        W.make_case("prefill_on_past", seed=62, query_lens=[70], past_lens=[25], num_q_heads=8, num_kv_heads=2,
+                    head_dim=32, page_size=16),
+        W.make_case("prefill_window", seed=63, query_lens=[45], past_lens=[30], num_q_heads=4, num_kv_heads=1,
+                    head_dim=16, page_size=8, q_dtype="f16", kv_dtype="f16", sliding_window=19),
+        W.make_case("mixed_batch", seed=64, query_lens=[1, 3, 45, 0, 33, 8, 9], past_lens=[50, 7, 12, 3, 0, 40, 21],
+                    num_q_heads=6, num_kv_heads=3, head_dim=16, page_size=4),
+        W.make_case("mixed_u8", seed=65, query_lens=[2, 37], past_lens=[64, 17], num_q_heads=4, num_kv_heads=2,
+                    head_dim=16, page_size=8, kv_dtype="u8", q_dtype="f16"),
+    ]
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_prefill_and_mixed_batches_match_dense_brute_force(oracle_mod, idx):
+    case = prefill_cases()[idx]
+    got = run_oracle(oracle_mod, case)
+    want = brute_force(case)
+    assert np.isfinite(got).all(), "oracle read a poisoned slot"
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [0, 9])
+def test_long_t_equals_single_token_decodes(oracle_mod, window):
+    """Beyond 32 new tokens (past any bit-mask width): token i of a 45-token
+    chunk equals a single-token decode with past_len L + i, bit for bit."""
+    T, L = 45, 20
+    case = W.make_case("eq_long", seed=66, query_lens=[T], past_lens=[L], num_q_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=8, sliding_window=window)
+    multi = run_oracle(oracle_mod, case)
+    for i in (0, 1, 30, 31, 32, 33, 44):
+        single = oracle_mod.forward(case.q[i: i + 1], case.q_dtype, case.k_cache, case.v_cache, case.kv_dtype,
+                                    case.block_tables, [L + i], [0, 1], num_q_heads=4, num_kv_heads=2,
+                                    head_dim=16, page_size=8, num_blocks=case.num_blocks, scale=case.scale,
+                                    sliding_window=window)
+        assert np.array_equal(multi[i], single[0])
+
+
+def test_prefill_without_past_matches_torch_causal_sdpa(oracle_mod):
+    """past_len 0: the chunk is plain causal self-attention (library routine)."""
+    torch = pytest.importorskip("torch")
+    T, Hq, Hkv, D, ps = 50, 8, 2, 32, 16
+    case = W.make_case("causal", seed=67, query_lens=[T], past_lens=[0], num_q_heads=Hq, num_kv_heads=Hkv,
+                       head_dim=D, page_size=ps)
+    got = run_oracle(oracle_mod, case)
+    kc, vc = _decode_cache(case)
+    pos = np.arange(T)
+    blocks = case.block_tables[0][pos // ps]
+    K = torch.from_numpy(kc[blocks, :, pos % ps, :].transpose(1, 0, 2).copy()).repeat_interleave(Hq // Hkv, dim=0)
+    V = torch.from_numpy(vc[blocks, :, pos % ps, :].transpose(1, 0, 2).copy()).repeat_interleave(Hq // Hkv, dim=0)
+    q = torch.from_numpy(W.storage_to_f64(case.q, "bf16").reshape(T, Hq, D).transpose(1, 0, 2).copy())
+    ref = torch.nn.functional.scaled_dot_product_attention(q[None], K[None], V[None], is_causal=True,
+                                                           scale=case.scale)[0]
+    np.testing.assert_allclose(got, ref.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)
+
+
+def test_mixed_batch_is_each_sequence_alone(oracle_mod):
+    """Sequences of a mixed batch do not interact: each one's rows equal a
+    call with that sequence alone (bit for bit)."""
+    case = prefill_cases()[3]
+    got = run_oracle(oracle_mod, case)
+    for b in range(case.num_seqs):
+        t0, t1 = int(case.subsequence_begins[b]), int(case.subsequence_begins[b + 1])
+        if t1 == t0:
+            continue
+        alone = oracle_mod.forward(case.q[t0:t1], case.q_dtype, case.k_cache, case.v_cache, case.kv_dtype,
+                                   case.block_tables[b: b + 1], case.past_lens[b: b + 1], [0, t1 - t0],
+                                   num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
+                                   head_dim=case.head_dim, page_size=case.page_size, num_blocks=case.num_blocks,
+                                   scale=case.scale)
+        assert np.array_equal(got[t0:t1], alone)
