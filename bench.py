@@ -162,6 +162,13 @@ class DeviceWorkload:
                         self.scale, self.window, self.kv_code, self.out, self.dims, self.ws, tree_mask,
                         stream=stream)
 
+    def forward_mixed(self, r, stream=None):
+        import paged_attention_speculative_gb300 as pa
+        if not hasattr(self, "ws_mixed"):
+            self.ws_mixed = pa.alloc_mixed_workspace(self.dims, self.max_ctx, self.window, self.kv_code)
+        pa.forward_mixed(self.q, self.k, self.v, self.block_tables[r], self.past_lens, self.begins, self.max_ctx,
+                         self.scale, self.window, self.kv_code, self.out, self.dims, self.ws_mixed, stream=stream)
+
     def cache_update(self, r, stream=None):
         import paged_attention_speculative_gb300 as pa
         pa.cache_update(self.k_new, self.v_new, self.k, self.v, self.block_tables[r], self.past_lens, self.begins,
@@ -180,6 +187,34 @@ class DeviceWorkload:
 
     def launches_per_step(self):
         return 1 + (1 if self.plan().num_partitions > 1 else 0)
+
+
+def mixed_sweep(stream, hbm_peak, l2):
+    """Verify steps and prefill chunks in one pa_forward_mixed call, against
+    each part alone (verify steps: pa_forward_mixed with no chunk, which is
+    the verify path; chunks: pa_forward_mixed with no verify step)."""
+    import torch
+    tc_peak = peaks().get("bf16_tflops", 1900.0)
+    rows = []
+    for name, hq, hkv, d, vq, vl, pq, plen in (
+            ("qwen_4xT4_L32768+T512_L32768", 32, 8, 128, [4] * 4, [32768] * 4, [512], [32768]),
+            ("qwen_4xT4_L32768+T2048_L0", 32, 8, 128, [4] * 4, [32768] * 4, [2048], [0]),
+            ("long_T8_L131072+T256_L131072", 64, 8, 128, [8], [131072], [256], [131072])):
+        us = {}
+        for part, ql, pl in (("mixed", vq + pq, vl + plen), ("verify", vq, vl), ("prefill", pq, plen)):
+            w = DeviceWorkload(hq, hkv, d, 16, "bf16", ql, pl, 0, min_bytes=2 * l2, seed=17)
+            us[part] = time_calls(lambda r: w.forward_mixed(r, stream), w.replicas, stream, reps=16, trials=10)
+            if part == "prefill":
+                pf_flops = w.flops
+            del w
+            torch.cuda.empty_cache()
+        rows.append({"workload": name, "mixed_us": round(us["mixed"], 2), "verify_alone_us": round(us["verify"], 2),
+                     "prefill_alone_us": round(us["prefill"], 2),
+                     "mixed_vs_sum": round(us["mixed"] / (us["verify"] + us["prefill"]), 3),
+                     "prefill_tflops": round(pf_flops / (us["prefill"] * 1e-6) / 1e12, 1),
+                     "prefill_frac_of_measured_bf16": round(pf_flops / (us["prefill"] * 1e-6) / 1e12 / tc_peak, 3)})
+        log(f"[bench] mixed {rows[-1]}")
+    return rows
 
 
 def small_page_sweep(stream, hbm_peak, l2):
@@ -699,6 +734,7 @@ def run_ours(args, rank, world):
             torch.cuda.empty_cache()
 
     small_pages = small_page_sweep(stream, hbm_peak, L2) if (not args.no_sweep and rank == 0) else []
+    mixed = mixed_sweep(stream, hbm_peak, L2) if (not args.no_sweep and rank == 0) else []
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -738,6 +774,7 @@ def run_ours(args, rank, world):
         "cache_update": cache_update,
         "tree_verify": tree_verify,
         "small_pages": small_pages,
+        "mixed": mixed,
     }
     print(json.dumps(line), flush=True)
 

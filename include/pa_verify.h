@@ -285,6 +285,36 @@ int pa_verify_forward_tree(const void* q, const void* k_cache, const void* v_cac
 
 /* Synchronises cuda_stream, then reads and clears the workspace's status word
  * into *bits (PA_STATUS_* flags, 0 = clean). */
+/*
+ * pa_forward_mixed — one call for a batch that mixes verify steps with
+ * prefill chunks (the MIXED stage of the OpenVINO paged-attention op, issue
+ * 38153 "Cause"; vLLM's decode_query_len gate on the dual-radeon-vllm page):
+ * the same attention as pa_verify_forward, token i of sequence b seeing keys
+ * lo_i .. past_len_b + i, but T_b may be any number of new tokens.
+ *
+ *  Sequences with T_b <= 8 (verify steps) run on the split-KV partition
+ *  kernels and the combine, exactly as in pa_verify_forward, their partials
+ *  indexed by slot b * 8 + i.  Sequences with T_b > 8 (prefill chunks) run
+ *  on a prefill kernel: 128 query rows per CTA (128 / G tokens x the G heads
+ *  of a KV head) streaming the tile's keys once on the tensor cores (16-bit
+ *  caches), or the fp32 FFMA kernel (fp32 caches); their rows are written
+ *  directly.  The three launches are ordered on cuda_stream.
+ *
+ *  Arguments as for pa_verify_forward; dims.total_tokens counts both kinds.
+ *  The workspace is pa_mixed_workspace_size bytes (status word + partials
+ *  for 8 token slots per sequence); its status word is shared by all three
+ *  kernels.  Supported: bf16 / f16 caches with head_dim 64 or 128, pages of
+ *  8 tokens or more and Hq / Hkv <= 128, or fp32 caches (any head_dim and
+ *  page size); otherwise PA_ERR_UNSUPPORTED (PA_ERR_PAGE_SIZE for 16-bit
+ *  caches with smaller pages).  Device errors as for pa_verify_forward,
+ *  except that T_b > 8 is not one. */
+size_t pa_mixed_workspace_size(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window,
+                               pa_dtype kv_dtype);
+int pa_forward_mixed(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                     const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                     float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                     void* workspace, size_t workspace_bytes, void* cuda_stream);
+
 int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits);
 
 /* Static description of a PA_OK / PA_ERR_* code. */

@@ -28,7 +28,8 @@ STATUS_BITS = {0x1: "QUERY_LEN", 0x2: "CONTEXT", 0x4: "BLOCK_ID", 0x8: "BEGINS",
                0x20: "ROWS", 0x40: "TIMEOUT"}
 EXPORTED = ["pa_verify_workspace_size", "pa_verify_plan", "pa_verify_forward", "pa_verify_forward_traced",
             "pa_verify_partition", "pa_verify_combine", "pa_verify_get_device_status", "pa_verify_status_string",
-            "pa_verify_forward_no_alloc", "pa_cache_update", "pa_verify_forward_tree"]
+            "pa_verify_forward_no_alloc", "pa_cache_update", "pa_verify_forward_tree", "pa_mixed_workspace_size",
+            "pa_forward_mixed"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -94,6 +95,10 @@ def load_library():
         lib.pa_verify_forward_no_alloc.restype = ctypes.c_int
         lib.pa_verify_forward_tree.argtypes = fwd[:14] + [vp, vp]
         lib.pa_verify_forward_tree.restype = ctypes.c_int
+        lib.pa_mixed_workspace_size.argtypes = [dp, i32, i32, ctypes.c_int]
+        lib.pa_mixed_workspace_size.restype = sz
+        lib.pa_forward_mixed.argtypes = fwd
+        lib.pa_forward_mixed.restype = ctypes.c_int
         lib.pa_cache_update.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, vp, dp,
                                         vp, vp]
         lib.pa_cache_update.restype = ctypes.c_int
@@ -210,6 +215,30 @@ def forward_tree(q, k_cache, v_cache, block_tables, past_lens, subsequence_begin
     args = _fwd_args(q, k_cache, v_cache, block_tables, past_lens, subsequence_begins, max_context_len, scale,
                      sliding_window, kv_dtype, out, dims, workspace, stream)
     _check(load_library().pa_verify_forward_tree(*args[:14], _ptr(tree_mask), args[14]), "pa_verify_forward_tree")
+    return out
+
+
+def mixed_workspace_size(dims: PaDims, max_context_len: int, sliding_window: int, kv_dtype: int) -> int:
+    return int(load_library().pa_mixed_workspace_size(ctypes.byref(dims), int(max_context_len),
+                                                      int(sliding_window), int(kv_dtype)))
+
+
+def alloc_mixed_workspace(dims: PaDims, max_context_len: int, sliding_window: int, kv_dtype: int, device=None):
+    """A zeroed workspace tensor of the size pa_mixed_workspace_size asks for."""
+    import torch
+    n = mixed_workspace_size(dims, max_context_len, sliding_window, kv_dtype)
+    if n == 0:
+        raise PaVerifyError("pa_mixed_workspace_size rejected the arguments")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def forward_mixed(q, k_cache, v_cache, block_tables, past_lens, subsequence_begins, max_context_len, scale,
+                  sliding_window, kv_dtype, out, dims: PaDims, workspace, stream=None):
+    """pa_forward_mixed: verify steps (T_b <= 8) and prefill chunks (T_b > 8)
+    in one call; the workspace from alloc_mixed_workspace."""
+    _check(load_library().pa_forward_mixed(*_fwd_args(q, k_cache, v_cache, block_tables, past_lens,
+                                                      subsequence_begins, max_context_len, scale, sliding_window,
+                                                      kv_dtype, out, dims, workspace, stream)), "pa_forward_mixed")
     return out
 
 

@@ -35,9 +35,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine(const CombineAr
     else hi = mid - 1;
   }
   const SeqInfo si = seq_info(a.begins, a.past_lens, lo, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
-                              a.part_tokens, a.row_cap);
+                              a.part_tokens, a.row_cap, a.role);
   pdl_wait_primary();
   pdl_launch_dependents();  // the next step's partition kernel may start its launch
+  if (si.foreign) return;  // a prefill chunk of a mixed call: the prefill kernel writes it
   if (si.err || si.T <= 0 || t < si.t0 || t >= si.t0 + si.T) {
     // malformed metadata: the partition kernel reported it; leave zeros
     for (int d = threadIdx.x; d < D; d += blockDim.x) store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + d, 0.f);
@@ -45,9 +46,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine(const CombineAr
   }
   const int np = si.nparts;
   if (np <= 1) return;  // written directly by the partition kernel
-  const float* pm = a.pm + static_cast<size_t>(row) * a.num_parts;
-  const float* pl = a.pl + static_cast<size_t>(row) * a.num_parts;
-  const float* po = a.po + static_cast<size_t>(row) * a.num_parts * D + lane * PER;
+  const size_t pr = prow(static_cast<size_t>(row), si, a.Hq);
+  const float* pm = a.pm + pr * a.num_parts;
+  const float* pl = a.pl + pr * a.num_parts;
+  const float* po = a.po + pr * a.num_parts * D + lane * PER;
   // Warp w merges partitions w, w + 8, ... with its own running max; the
   // loads of up to kBatch partitions are issued together (one round trip).
   constexpr int kBatch = 8;

@@ -24,6 +24,13 @@ constexpr int kGatherWarps = 4;              // cp.async producer warps of the s
 constexpr uint32_t kWaitLimit = 1u << 22;    // bounded mbarrier polls before giving up
 
 // Arguments common to the partition kernels (plain values, passed by value).
+// Which sequences a launch serves.  A plain verify call serves all of them
+// (T_b <= 8).  A mixed call runs the split-KV kernels over its verify steps
+// (T_b <= 8; their partials indexed by slot b * 8 + i, so the workspace does
+// not grow with prefill tokens) and the prefill kernel over its prefill
+// chunks (T_b > 8).
+constexpr int kRoleAll = 0, kRoleShort = 1, kRoleLong = 2;
+
 struct PartArgs {
   const void* q;
   const uint8_t* k_bytes;       // cache bases (u8 records need byte addressing)
@@ -32,15 +39,18 @@ struct PartArgs {
   const int32_t* past_lens;
   const int32_t* begins;
   void* out;
-  float* po;                    // [total_tokens, Hq, P, D] unnormalised partial outputs
-  float* pm;                    // [total_tokens, Hq, P] running max (log2 domain)
-  float* pl;                    // [total_tokens, Hq, P] softmax denominators (-1 = poisoned)
+  float* po;                    // [slots, Hq, P, D] unnormalised partial outputs
+  float* pm;                    // [slots, Hq, P] running max (log2 domain)
+  float* pl;                    // [slots, Hq, P] softmax denominators (-1 = poisoned)
+                                // slots: total_tokens (token t), or B * 8 in a
+                                // mixed call's verify part (b * 8 + i)
   uint32_t* status;
   int32_t* trace;               // optional gather trace
   const uint8_t* tree_mask;     // optional: per token, bit k = sees new token k of its sequence
   int num_seqs, total_tokens, Hq, Hkv, G, D, ps, ps_log2, num_blocks, max_blocks;
   int max_ctx, window, part_tokens, num_parts, box_log2, row_cap;
   int q_dtype, out_dtype;
+  int role;                     // kRoleAll / kRoleShort / kRoleLong
   float scale_log2;             // softmax scale * log2(e)
 };
 
@@ -53,6 +63,7 @@ struct CombineArgs {
   const float* pl;
   uint32_t* status;
   int num_seqs, total_tokens, Hq, Hkv, G, ps, max_ctx, window, part_tokens, num_parts, row_cap, out_dtype;
+  int role;
 };
 
 // ---------------------------------------------------------------------------
@@ -63,6 +74,8 @@ struct SeqInfo {
   int klo, khi;          // union of the rows' key ranges [klo, khi]
   int kbase;             // klo rounded down to a page boundary
   int nparts;            // partitions this sequence needs
+  long long pshift;      // partials of token t live at token slot t + pshift (prow)
+  bool foreign;          // another kernel of a mixed call owns this sequence
   uint32_t err;          // PA_STATUS_* bits that make the sequence invalid
   bool rows_ok;          // t0 / T can be trusted to index output rows
 };
@@ -94,24 +107,37 @@ __device__ __forceinline__ uint32_t ld_once(const uint32_t* p) {
 
 __device__ __forceinline__ SeqInfo seq_info(const int32_t* begins, const int32_t* past_lens, int b,
                                             int total_tokens, int G, int ps, int max_ctx, int window,
-                                            int part_tokens, int row_capacity) {
+                                            int part_tokens, int row_capacity, int role) {
   SeqInfo s;
   s.t0 = ld_once(begins + b);
   const int t1 = ld_once(begins + b + 1);
   s.L = ld_once(past_lens + b);
   s.T = t1 - s.t0;
   s.err = 0;
+  s.pshift = role == kRoleShort ? static_cast<long long>(b) * PA_MAX_QUERY_LEN - s.t0 : 0;
+  s.foreign = false;
   s.rows_ok = (s.t0 >= 0 && t1 >= s.t0 && t1 <= total_tokens);
+  // a mixed call splits its sequences by length: verify steps (T <= 8) to
+  // the split-KV kernels, prefill chunks (T > 8) to the prefill kernel
+  if (s.rows_ok && ((role == kRoleShort && s.T > PA_MAX_QUERY_LEN) || (role == kRoleLong && s.T <= PA_MAX_QUERY_LEN))) {
+    s.foreign = true;
+    s.T = 0;
+  }
   if (!s.rows_ok) s.err |= PA_STATUS_BEGINS;
-  if (s.T > PA_MAX_QUERY_LEN) s.err |= PA_STATUS_QUERY_LEN;
+  if (role != kRoleLong && s.T > PA_MAX_QUERY_LEN) s.err |= PA_STATUS_QUERY_LEN;
   if (s.L < 0) s.err |= PA_STATUS_PAST_LEN;
   if ((long long)s.L + s.T > (long long)max_ctx) s.err |= PA_STATUS_CONTEXT;
-  if (s.T * G > row_capacity) s.err |= PA_STATUS_ROWS;
+  if (role != kRoleLong && s.T * G > row_capacity) s.err |= PA_STATUS_ROWS;
   s.khi = s.L + s.T - 1;
   s.klo = window > 0 ? max(0, s.L - window + 1) : 0;
   s.kbase = (s.klo / ps) * ps;
   s.nparts = (s.err || s.T <= 0) ? 0 : (s.khi + 1 - s.kbase + part_tokens - 1) / part_tokens;
   return s;
+}
+
+// Partial-buffer row of output row `row` (= t * Hq + h) of a sequence.
+__device__ __forceinline__ size_t prow(size_t row, const SeqInfo& si, int Hq) {
+  return static_cast<size_t>(static_cast<long long>(row) + si.pshift * Hq);
 }
 
 // ---------------------------------------------------------------------------

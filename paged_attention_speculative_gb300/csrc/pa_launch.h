@@ -59,6 +59,12 @@ cudaError_t launch_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v,
 constexpr int kGatherBelowPageSize = 8;
 cudaError_t launch_tc_gather(int D, int kv, const PartArgs& a, dim3 grid, cudaStream_t st);
 
+// Prefill tiles of a mixed batch (sequences with more than 8 new tokens):
+// 128 query rows per CTA, head_dim 64 / 128, KV_BF16 / KV_F16 caches; grid
+// (row tiles, Hkv), 192 threads.
+cudaError_t launch_prefill_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a,
+                              dim3 grid, cudaStream_t st);
+
 // Tensor-memory partition kernels with the keys on the MMA's M dimension:
 // head_dim 64 / 128, KV_BF16 / KV_F16 caches, row tiles n = 16 / 32 / 64.
 MmaKernelInfo tk_info(int D, int kv, int n, bool* ok);

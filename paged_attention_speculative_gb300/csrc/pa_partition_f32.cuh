@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(128) pa_partition_f32(const PartArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
-                              a.part_tokens, a.row_cap);
+                              a.part_tokens, a.row_cap, a.role);
   pdl_launch_dependents();
   if (si.err) {
     if (p == 0 && threadIdx.x == 0) atomicOr(a.status, si.err);
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(128) pa_partition_f32(const PartArgs a) {
       if (si.nparts == 1) {
         store_out(a.out, a.out_dtype, row * D + d, (bad || !(l > 0.f)) ? 0.f : o[e] / l);
       } else {
-        const size_t pr = row * a.num_parts + p;
+        const size_t pr = prow(row, si, a.Hq) * a.num_parts + p;
         a.po[pr * D + d] = o[e];
         if (d == 0) {
           a.pm[pr] = m;

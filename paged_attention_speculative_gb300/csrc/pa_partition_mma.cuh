@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     for (int j = lane; j < n; j += 32) cp_async4(blk + j, src + j);
   }
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
-                              a.part_tokens, a.row_cap);
+                              a.part_tokens, a.row_cap, a.role);
   pdl_launch_dependents();
   if (si.err || si.T <= 0 || p >= si.nparts) {
     if (prefetch) cp_async_wait_all();  // no copy into shared memory outlives the CTA
@@ -576,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
       if (si.nparts == 1) {
         store_out(a.out, a.out_dtype, row * D + d, 0.f);
       } else if (d == 0) {
-        a.pm[row * a.num_parts + p] = 0.f;
-        a.pl[row * a.num_parts + p] = -1.f;
+        a.pm[prow(row, si, a.Hq) * a.num_parts + p] = 0.f;
+        a.pl[prow(row, si, a.Hq) * a.num_parts + p] = -1.f;
       }
     }
     return;
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     if (si.nparts == 1) {
       store_out(a.out, a.out_dtype, row * D + d, (poisoned || !(lsum > 0.f)) ? 0.f : acc / lsum);
     } else {
-      const size_t pr = row * a.num_parts + p;
+      const size_t pr = prow(row, si, a.Hq) * a.num_parts + p;
       a.po[pr * D + d] = acc;
       if (d == 0) {
         a.pm[pr] = M;

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
     for (int j = lane; j < n; j += 32) cp_async4(blk + j, src + j);
   }
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
-                              a.part_tokens, a.row_cap);
+                              a.part_tokens, a.row_cap, a.role);
   pdl_launch_dependents();
   if (si.err || si.T <= 0 || p >= si.nparts) {
     if (prefetch) cp_async_wait_all();  // no copy into shared memory outlives the CTA
@@ -609,15 +609,15 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, o[e] * inv);
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.po + (row * a.num_parts + p) * D + 32 * c);
+          float4* dst = reinterpret_cast<float4*>(a.po + (prow(row, si, a.Hq) * a.num_parts + p) * D + 32 * c);
 #pragma unroll
           for (int e = 0; e < 8; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
       }
     }
     if (real && si.nparts > 1) {
-      a.pm[row * a.num_parts + p] = m_ref;
-      a.pl[row * a.num_parts + p] = poisoned ? -1.f : l;
+      a.pm[prow(row, si, a.Hq) * a.num_parts + p] = m_ref;
+      a.pl[prow(row, si, a.Hq) * a.num_parts + p] = poisoned ? -1.f : l;
     }
     tc_fence_before();
   }

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int j = lane; j < n; j += 32) cp_async4(blk + j, src + j);
   }
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
-                              a.part_tokens, a.row_cap);
+                              a.part_tokens, a.row_cap, a.role);
   pdl_launch_dependents();
   if (si.err || si.T <= 0 || p >= si.nparts) {
     if (prefetch) cp_async_wait_all();  // no copy into shared memory outlives the CTA
@@ -474,9 +474,9 @@ __global__ void __launch_bounds__(192, 1)
         rowoff[n] = row * D;
         linv[n] = (poisoned || !(lt > 0.f)) ? 0.f : 1.f / lt;
       } else {
-        rowoff[n] = (row * a.num_parts + p) * D;
-        a.pm[row * a.num_parts + p] = m_sm[n];
-        a.pl[row * a.num_parts + p] = poisoned ? -1.f : lt;
+        rowoff[n] = (prow(row, si, a.Hq) * a.num_parts + p) * D;
+        a.pm[prow(row, si, a.Hq) * a.num_parts + p] = m_sm[n];
+        a.pl[prow(row, si, a.Hq) * a.num_parts + p] = poisoned ? -1.f : lt;
       }
     }
     bar_sync_n(1, 128);

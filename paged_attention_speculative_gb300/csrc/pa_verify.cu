@@ -239,8 +239,14 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   return PA_OK;
 }
 
-size_t workspace_bytes_for(const pa_dims* d, const pa_plan& plan) {
-  const size_t rows = static_cast<size_t>(d->total_tokens) * d->num_q_heads * plan.num_partitions;
+// Token slots of the split-KV partials: one per token, or 8 per sequence in
+// a mixed call (its verify steps index partials by b * 8 + i).
+size_t partial_slots(const pa_dims* d, bool mixed) {
+  return mixed ? static_cast<size_t>(d->num_seqs) * PA_MAX_QUERY_LEN : static_cast<size_t>(d->total_tokens);
+}
+
+size_t workspace_bytes_for(const pa_dims* d, const pa_plan& plan, bool mixed = false) {
+  const size_t rows = partial_slots(d, mixed) * d->num_q_heads * plan.num_partitions;
   return kStatusBytes + align256(rows * d->head_dim * 4) + 2 * align256(rows * 4);
 }
 
@@ -251,8 +257,8 @@ struct Workspace {
   float* pl;
 };
 
-Workspace carve(void* ws, const pa_dims* d, const pa_plan& plan) {
-  const size_t rows = static_cast<size_t>(d->total_tokens) * d->num_q_heads * plan.num_partitions;
+Workspace carve(void* ws, const pa_dims* d, const pa_plan& plan, bool mixed = false) {
+  const size_t rows = partial_slots(d, mixed) * d->num_q_heads * plan.num_partitions;
   uint8_t* base = static_cast<uint8_t*>(ws);
   Workspace w;
   w.status = reinterpret_cast<uint32_t*>(base);
@@ -330,10 +336,11 @@ struct Call {
   size_t ws_bytes;
   cudaStream_t stream;
   int32_t* trace;
-  const uint8_t* tree_mask;  // optional (tree-mask verify)
+  const uint8_t* tree_mask = nullptr;  // optional (tree-mask verify)
+  int role = pa::kRoleAll;             // which sequences the launches serve
 };
 
-int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
+PartArgs part_args(const Call& c, const pa_plan& plan, const Workspace& w) {
   const pa_dims* d = c.d;
   PartArgs a;
   a.q = c.q;
@@ -363,8 +370,7 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.window = c.window;
   a.part_tokens = plan.part_tokens;
   a.num_parts = plan.num_partitions;
-  const int box_rows = std::min(d->page_size, plan.stage_keys);
-  a.box_log2 = ilog2(box_rows);
+  a.box_log2 = ilog2(std::min(d->page_size, plan.stage_keys));
   a.row_cap = plan.kernel == 0   ? pa::kConsumerWarps * 8 * plan.row_tiles
               : plan.kernel == 2 ? 64
               : (plan.kernel == 3 || plan.kernel == 4) ? plan.row_tiles
@@ -372,6 +378,14 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.q_dtype = d->q_dtype;
   a.out_dtype = d->out_dtype;
   a.scale_log2 = c.scale * 1.4426950408889634f;
+  a.role = c.role;
+  return a;
+}
+
+int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
+  const pa_dims* d = c.d;
+  const PartArgs a = part_args(c, plan, w);
+  const int box_rows = std::min(d->page_size, plan.stage_keys);
   const dim3 grid(plan.num_partitions, d->num_kv_heads, d->num_seqs);
 
   cudaError_t e;
@@ -433,6 +447,7 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
               : (plan.kernel == 3 || plan.kernel == 4) ? plan.row_tiles
                                  : (1 << 30);
   a.out_dtype = d->out_dtype;
+  a.role = c.role;
   const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(rows));
@@ -485,6 +500,75 @@ int run(const Call& c, bool do_partition, bool do_combine) {
   return rc;
 }
 
+// The prefill chunks (T_b > 8) of a mixed call: 128-row tiles on the
+// tensor cores (16-bit caches), or the FFMA kernel with one partition per
+// sequence (fp32 caches).  Outputs are written directly.
+int launch_prefill(const Call& c, const pa_plan& plan, const Workspace& w) {
+  const pa_dims* d = c.d;
+  PartArgs a = part_args(c, plan, w);
+  a.role = pa::kRoleLong;
+  cudaError_t e;
+  if (c.kv == PA_F32) {
+    a.part_tokens = 1 << 30;  // one partition: the output row directly
+    a.num_parts = 1;
+    const dim3 grid(1, d->num_kv_heads, d->num_seqs);
+    if (d->head_dim == 64) e = pa::launch_dependent(pa::pa_partition_f32<64>, grid, dim3(128), 0, c.stream, a);
+    else if (d->head_dim == 128) e = pa::launch_dependent(pa::pa_partition_f32<128>, grid, dim3(128), 0, c.stream, a);
+    else e = pa::launch_dependent(pa::pa_partition_f32<256>, grid, dim3(128), 0, c.stream, a);
+  } else {
+    // tiles of TQ tokens: at most total / TQ full ones plus one partial one
+    // per prefill sequence (each has at least 9 tokens)
+    const int G = d->num_q_heads / d->num_kv_heads;
+    const long long TQ = 128 / G;
+    const long long tiles = ceil_div(d->total_tokens, TQ) +
+                            std::min<long long>(d->num_seqs, d->total_tokens / (PA_MAX_QUERY_LEN + 1));
+    if (tiles > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (tiles == 0) return PA_OK;
+    const int box_rows = std::min(d->page_size, 64);
+    a.box_log2 = ilog2(box_rows);
+    CUtensorMap mk, mv;
+    int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
+    if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
+    if (rc != PA_OK) return rc;
+    e = pa::launch_prefill_tc(d->head_dim, mma_kind(c.kv), mk, mv, a,
+                              dim3(static_cast<unsigned>(tiles), d->num_kv_heads), c.stream);
+  }
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Argument checks of a mixed call beyond the verify part's plan.
+int mixed_support(const pa_dims* d, pa_dtype kv) {
+  const bool tc16 = (kv == PA_BF16 || kv == PA_F16) && d->head_dim <= 128;
+  if (kv != PA_F32 && !tc16) return PA_ERR_UNSUPPORTED;
+  if (tc16 && d->page_size < pa::kGatherBelowPageSize) return PA_ERR_PAGE_SIZE;
+  if (tc16 && d->num_q_heads / d->num_kv_heads > 128) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+int run_mixed(Call c) {
+  if (c.d == nullptr) return PA_ERR_NULL;
+  pa_plan plan;
+  int rc = make_plan(c.d, c.max_ctx, c.window, c.kv, 1, &plan);
+  if (rc != PA_OK) return rc;
+  rc = mixed_support(c.d, c.kv);
+  if (rc != PA_OK) return rc;
+  rc = check_pointers(c, true);
+  if (rc != PA_OK) return rc;
+  if (c.d->total_tokens == 0) return PA_OK;
+  int sms = 0;
+  rc = device_sm_count(&sms);
+  if (rc != PA_OK) return rc;
+  rc = make_plan(c.d, c.max_ctx, c.window, c.kv, sms, &plan);
+  if (rc != PA_OK) return rc;
+  if (c.ws_bytes < workspace_bytes_for(c.d, plan, true)) return PA_ERR_WORKSPACE;
+  const Workspace w = carve(c.ws, c.d, plan, true);
+  c.role = pa::kRoleShort;  // verify steps: split-KV partitions + combine
+  rc = launch_partition(c, plan, w);
+  if (rc == PA_OK) rc = launch_combine(c, plan, w);
+  if (rc == PA_OK) rc = launch_prefill(c, plan, w);  // prefill chunks, after the combine in stream order
+  return rc;
+}
+
 // ---------------------------------------------------------------------------
 // Scratch for pa_verify_forward_no_alloc: a fixed device array that the
 // library owns, so the caller needs no allocator.  Every GPU that loads the
@@ -526,6 +610,26 @@ size_t pa_verify_workspace_size(const pa_dims* dims, int32_t max_context_len, in
   pa_plan tree_plan;
   if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &tree_plan, true) != PA_OK) return 0;
   return std::max(workspace_bytes_for(dims, plan), workspace_bytes_for(dims, tree_plan));
+}
+
+size_t pa_mixed_workspace_size(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window,
+                               pa_dtype kv_dtype) {
+  int sms = 0;
+  if (device_sm_count(&sms) != PA_OK) return 0;
+  pa_plan plan;
+  if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &plan) != PA_OK) return 0;
+  if (mixed_support(dims, kv_dtype) != PA_OK) return 0;
+  return workspace_bytes_for(dims, plan, true);
+}
+
+int pa_forward_mixed(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                     const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                     float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                     void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+               max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(cuda_stream), nullptr};
+  return run_mixed(c);
 }
 
 int pa_verify_plan(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window, pa_dtype kv_dtype,

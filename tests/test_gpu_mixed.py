@@ -1,0 +1,124 @@
+"""Mixed batches on the GPU (pa_forward_mixed, through the C ABI): verify
+steps (T_b <= 8) on the split-KV kernels and prefill chunks (T_b > 8) on the
+prefill tile kernel, in one call, against the oracle (whose causal rule holds
+for any number of new tokens).  Cases cover every query-head group size the
+tiles handle (G = 1, 2, 4, 6, 8: 128-row tiles of 128 / G tokens, ragged last
+tiles), windows, f16 / bf16 / fp32 caches, large pages, and device errors in
+a prefill chunk; a mixed call with no prefill chunk is pa_verify_forward bit
+for bit."""
+import numpy as np
+import pytest
+
+import oracle
+import paged_attention_speculative_gb300 as pa
+from paged_attention_speculative_gb300 import workloads as W
+
+from pa_testing import KV_CODE, TOL, derived_tolerance, dims, max_abs_err, run_gpu, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def run_mixed(case, dev=None, max_context_len=None):
+    import torch
+    dev = dev or to_device(case)
+    d = dims(case, dev)
+    kvc = KV_CODE[case.kv_dtype]
+    mcl = max_context_len or case.max_context_len
+    ws = pa.alloc_mixed_workspace(d, mcl, case.sliding_window, kvc)
+    pa.forward_mixed(dev["q"], dev["k"], dev["v"], dev["bt"], dev["pl"], dev["sb"], mcl, case.scale,
+                     case.sliding_window, kvc, dev["out"], d, ws)
+    torch.cuda.synchronize()
+    return dev["out"].float().cpu().numpy().astype(np.float64), pa.device_status(ws), dev["out"].cpu()
+
+
+def mk(name, seed, ql, pl, hq, hkv, d=128, ps=16, **kw):
+    return lambda: W.make_case(name, seed=seed, query_lens=ql, past_lens=pl, num_q_heads=hq, num_kv_heads=hkv,
+                               head_dim=d, page_size=ps, **kw)
+
+
+CASES = [
+    # (factory, derived bound: short contexts with O(1) outputs)
+    (mk("prefill_g4", 70, [100], [1000], 32, 8), False),
+    (mk("mixed_g4", 71, [4, 200, 1, 0, 37, 8, 9], [3000, 500, 1500, 10, 0, 700, 2000], 32, 8), True),
+    (mk("mixed_g8", 72, [8, 300], [20000, 20000], 64, 8), False),
+    (mk("mixed_win", 73, [50, 3, 130], [2000, 900, 64], 32, 8, sliding_window=300), True),
+    (mk("mixed_f16_d64_g2", 74, [150, 2], [400, 800], 8, 4, d=64, q_dtype="f16", kv_dtype="f16"), True),
+    (mk("prefill_g1", 75, [260], [700], 8, 8), False),
+    (mk("prefill_g6", 76, [50, 5], [300, 90], 24, 4), True),
+    (mk("mixed_f32", 77, [3, 20], [40, 10], 4, 2, d=64, q_dtype="f32", kv_dtype="f32"), True),
+    (mk("prefill_ps128", 78, [70, 2], [1000, 130], 32, 8, ps=128), False),
+    (mk("prefill_ps8_win1", 79, [40], [100], 8, 2, ps=8, sliding_window=1), True),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(CASES)))
+def test_mixed_matches_the_oracle(idx):
+    make, derived = CASES[idx]
+    case = make()
+    got, bits, _ = run_mixed(case)
+    assert bits == 0, f"device status {bits:#x}"
+    want = run_oracle(case)
+    err = max_abs_err(got, want)
+    if derived:
+        worst = float(np.max(np.abs(got - want) - derived_tolerance(case, want)))
+        assert worst <= 0.0, f"{case.name}: exceeds the derived bound by {worst:.3e} (max abs {err:.3e})"
+    else:
+        assert err <= TOL, f"{case.name}: max abs err {err:.3e}"
+
+
+@pytest.mark.slow
+def test_mixed_full_size():
+    """A prefill chunk of 130 tokens and three T=4 verify steps at 32k keys
+    (Qwen-like heads)."""
+    case = W.make_case("mixed_32k", seed=80, query_lens=[4, 130, 4, 4], past_lens=[32768, 32768, 30000, 32000],
+                       num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    got, bits, _ = run_mixed(case)
+    assert bits == 0
+    assert max_abs_err(got, run_oracle(case)) <= TOL
+
+
+def test_mixed_without_prefill_is_the_verify_call_bit_for_bit():
+    import torch
+    case = W.make_case("no_prefill", seed=81, query_lens=[4, 1, 8, 3], past_lens=[5000, 3000, 4500, 100],
+                       num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    _, bits, raw = run_mixed(case)
+    assert bits == 0
+    dev = to_device(case)
+    run_gpu(case, dev=dev)
+    assert torch.equal(raw.view(torch.int16), dev["out"].cpu().view(torch.int16))
+
+
+def test_prefill_chunk_equals_its_tokens_as_decodes():
+    """The pages' equivalence at prefill length: token i of a 40-token chunk
+    equals a single-token decode at past_len L + i (within the tolerance)."""
+    case = W.make_case("eq", seed=82, query_lens=[40], past_lens=[3000], num_q_heads=32, num_kv_heads=8,
+                       head_dim=128, page_size=16)
+    multi, bits, _ = run_mixed(case)
+    assert bits == 0
+    for i in (0, 17, 39):
+        single = W.Case(**{**case.__dict__, "q": case.q[i:i + 1].copy(), "past_lens": np.array([3000 + i], np.int32),
+                           "subsequence_begins": np.array([0, 1], np.int32), "name": f"single{i}"})
+        got, bits, _ = run_gpu(single)
+        assert bits == 0
+        assert np.max(np.abs(got[0] - multi[i])) <= TOL
+
+
+def test_bad_block_id_in_a_prefill_chunk_sets_the_status():
+    case = W.make_case("bad", seed=83, query_lens=[3, 60], past_lens=[500, 700], num_q_heads=32, num_kv_heads=8,
+                       head_dim=128, page_size=16)
+    bt = case.block_tables.copy()
+    bt[1, 10] = case.num_blocks + 3
+    bad = W.Case(**{**case.__dict__, "block_tables": bt})
+    got, bits, _ = run_mixed(bad)
+    assert bits & 0x4  # PA_STATUS_BLOCK_ID
+    good = run_oracle(case)
+    # the verify step is untouched; the chunk's tiles that read the bad page are zero
+    assert max_abs_err(got[:3], good[:3]) <= TOL
+
+
+def test_context_overflow_in_a_prefill_chunk_sets_the_status():
+    case = W.make_case("ctx", seed=84, query_lens=[2, 40], past_lens=[100, 200], num_q_heads=8, num_kv_heads=2,
+                       head_dim=128, page_size=16)
+    got, bits, _ = run_mixed(case, max_context_len=220)
+    assert bits & 0x2  # PA_STATUS_CONTEXT
+    assert np.all(got[2:] == 0.0)

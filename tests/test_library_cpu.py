@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "pa_verify.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_(?:verify|cache)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pa_(?:verify|cache|mixed|forward)_\w+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -153,6 +153,22 @@ def test_forward_host_errors_need_no_gpu(lib):
     bad = list(args)
     bad[11] = None
     assert lib.pa_verify_forward(*bad) == -1
+
+
+def test_mixed_host_errors_need_no_gpu(lib):
+    """pa_forward_mixed rejects what its prefill kernels do not serve before
+    touching the device: u8 caches, head_dim 256 with 16-bit caches, 16-bit
+    caches with pages under 8 tokens; NULL pointers as pa_verify_forward."""
+    a16 = ctypes.c_void_p(4096)
+    z = ctypes.c_void_p(0)
+
+    def call(d, kv, ptr=a16):
+        return lib.pa_forward_mixed(ptr, a16, a16, a16, a16, a16, 4096, 0.1, 0, kv, a16, ctypes.byref(d), a16,
+                                    1 << 20, z)
+    assert call(dims(q_dtype=pa.PA_BF16), pa.PA_U8) == -10
+    assert call(dims(head_dim=256, num_q_heads=16), pa.PA_BF16) == -10
+    assert call(dims(page_size=4, max_blocks_per_seq=4096), pa.PA_BF16) == -5
+    assert call(dims(), pa.PA_BF16, ptr=z) == -1
 
 
 def test_status_strings(lib):
