@@ -779,10 +779,21 @@ def run_ours(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# Workloads the ncu summaries of the other kernels are taken on: the
+# cp.async page gather (one token per page) and a prefill chunk alone.
+PROFILE_EXTRA = {
+    "long_T8_L131072_ps1": dict(Hq=64, Hkv=8, D=128, ps=1, kv="bf16", q_lens=[8], past=[131072], window=0),
+    "prefill_T512_L32768": dict(Hq=32, Hkv=8, D=128, ps=16, kv="bf16", q_lens=[512], past=[32768], window=0,
+                                mixed=True),
+}
+
+
 def workload_by_name(name):
     """A sweep / headline workload spec by its printed name, e.g. qwen_gqa_T4_L32768."""
     if name == HEADLINE["name"]:
         return dict(HEADLINE)
+    if name in PROFILE_EXTRA:
+        return dict(name=name, **PROFILE_EXTRA[name])
     for fam in SWEEP:
         for L in fam["L"]:
             for T in fam["T"]:
@@ -804,9 +815,10 @@ def run_profile(args):
     wl = DeviceWorkload(spec["Hq"], spec["Hkv"], spec["D"], spec["ps"], spec["kv"], spec["q_lens"], spec["past"],
                         spec["window"], min_bytes=2 * l2_bytes())
     stream = torch.cuda.Stream()
+    step = wl.forward_mixed if spec.get("mixed") else wl.forward
     with torch.cuda.stream(stream):
         for s in range(args.warmup + args.steps):
-            wl.forward(s % wl.replicas, stream)
+            step(s % wl.replicas, stream)
     torch.cuda.synchronize()
     log(f"[profile] {spec['name']}: {args.warmup + args.steps} steps, plan {wl.plan().as_dict()}, "
         f"kv bytes/step {wl.kv_bytes}")

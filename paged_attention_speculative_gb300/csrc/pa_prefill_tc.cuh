@@ -20,8 +20,9 @@
 //   warp 4     MMA issuer (one thread)
 //   warp 5     TMA producer: block ids one stage ahead, one tile load per
 //              page segment and 128-byte chunk
-// Tiles are numbered over the batch's prefill sequences in order; each CTA
-// finds its (sequence, first token) by walking subsequence_begins.
+// Tiles are numbered over the batch's prefill sequences in order, each
+// sequence's tiles last token first; each CTA finds its (sequence, first
+// token) by walking subsequence_begins.
 #pragma once
 
 #include "pa_partition_tc.cuh"
@@ -59,8 +60,10 @@ __global__ void __launch_bounds__(192, 1)
       if (T <= PA_MAX_QUERY_LEN) continue;  // a verify step (or malformed: reported below)
       const long long nt = (T + TQ - 1) / TQ;
       if (tile < nt) {
+        // a chunk's tiles in reverse: the last tokens see the most keys, so
+        // the longest tiles are scheduled first
         b = s;
-        i0 = static_cast<int>(tile) * TQ;
+        i0 = static_cast<int>(nt - 1 - tile) * TQ;
         break;
       }
       tile -= nt;
