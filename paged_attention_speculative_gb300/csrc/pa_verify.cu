@@ -68,6 +68,16 @@ int env_part_tokens() {
   return v;
 }
 
+// Optional tuning override of the warp-level kernel's n-tiles per warp (1 or 2), read once.
+int env_row_tiles() {
+  static const int v = [] {
+    const char* s = std::getenv("PA_VERIFY_ROW_TILES");
+    const int n = s ? std::atoi(s) : 0;
+    return (n == 1 || n == 2) ? n : 0;
+  }();
+  return v;
+}
+
 int mma_kind(pa_dtype kv) { return kv == PA_BF16 ? pa::KV_BF16 : (kv == PA_F16 ? pa::KV_F16 : pa::KV_U8); }
 
 pa::MmaKernelInfo mma_info(int D, int kind, int nt, bool* ok) {
@@ -181,6 +191,7 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
     // one 8-row n-tile per warp keeps a warp's accumulators within the
     // register budget of two CTAs per SM; rows beyond 8 go to more warps
     nt = (D == 256 || rows <= 32) ? 1 : 2;
+    if (env_row_tiles() > 0 && D != 256) nt = env_row_tiles();
     const int cap = pa::kConsumerWarps * 8 * nt;
     if (rows > cap) return PA_ERR_UNSUPPORTED;
     bool ok = false;
