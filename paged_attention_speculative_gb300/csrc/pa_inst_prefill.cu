@@ -8,7 +8,7 @@ namespace {
 template <int D, int KV>
 cudaError_t launch_p(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid, cudaStream_t st) {
   auto kern = pa_prefill_tc<D, KV>;
-  const int smem = TcCfg<D, KV>::BYTES;
+  const int smem = PfCfg<D, KV>::BYTES;
   static int configured_for[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -18,7 +18,7 @@ cudaError_t launch_p(const CUtensorMap& k, const CUtensorMap& v, const PartArgs&
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  return launch_dependent(kern, grid, dim3(192), smem, st, k, v, a);
+  return launch_dependent(kern, grid, dim3(320), smem, st, k, v, a);
 }
 }  // namespace
 

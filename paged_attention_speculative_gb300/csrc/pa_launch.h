@@ -60,8 +60,8 @@ constexpr int kGatherBelowPageSize = 8;
 cudaError_t launch_tc_gather(int D, int kv, const PartArgs& a, dim3 grid, cudaStream_t st);
 
 // Prefill tiles of a mixed batch (sequences with more than 8 new tokens):
-// 128 query rows per CTA, head_dim 64 / 128, KV_BF16 / KV_F16 caches; grid
-// (row tiles, Hkv), 192 threads.
+// up to 256 query rows (two 128-row tiles) per CTA, head_dim 64 / 128,
+// KV_BF16 / KV_F16 caches; grid (row blocks, Hkv), 320 threads.
 cudaError_t launch_prefill_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a,
                               dim3 grid, cudaStream_t st);
 

@@ -3,78 +3,141 @@
 // beside the verify steps of other sequences, the MIXED stage of the OpenVINO
 // paged-attention op that issue 38153 describes).
 //
-// One CTA per (row tile, KV head).  A row tile is 128 query rows: TQ = 128 / G
-// consecutive new tokens of one sequence times the G query heads of the KV
-// head, ordered like the verify kernels' rows (r -> token r / G, head
-// g * G + r % G).  The tile streams its keys [klo, khi] once, klo the window
-// start of its first token and khi = past_len + its last token, through the
-// same pipeline as pa_partition_tc, with every MMA row real:
-//   S(s)  = Q . K_s^T   tcgen05.mma M=128, N=64, K=D   (Q in TMEM, K from smem)
-//   P(s)  = 2^(S*scale*log2e - m) per row, causal / window mask per row
-//   O    += P(s) . V_s  tcgen05.mma M=128, N=D, K=64   (P in TMEM, V from smem)
+// One CTA per (row block, KV head).  A row block is 128 or 256 query rows
+// (the launcher's choice): TQ = rows / G consecutive new tokens of one
+// sequence times the G query heads
+// of the KV head, ordered like the verify kernels' rows (r -> token r / G,
+// head g * G + r % G), split into two 128-row tiles that share every K/V
+// stage.  The CTA streams its keys [klo, khi] once, klo the window start of
+// its first token and khi = past_len + its last token:
+//   S_t(s) = Q_t . K_s^T   tcgen05.mma M=128, N=64, K=D  (Q_t from smem)
+//   P_t(s) = 2^(S*scale*log2e - m) per row, causal / window mask per row
+//   O_t   += P_t(s) . V_s  tcgen05.mma M=128, N=D, K=64  (P_t in TMEM)
 // and writes the normalised rows directly (no split over keys).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r; warp w reads
-//              the lane quarter w)
-//   warp 4     MMA issuer (one thread)
-//   warp 5     TMA producer: block ids one stage ahead, one tile load per
+// With two tiles they ping-pong, one S and one P buffer each: the MMA thread
+// issues S_0(s), PV_1(s-1), S_1(s), PV_0(s), so tile 0's softmax of stage s
+// runs while tile 1's scores are computed, and tile 1's while tile 0's next
+// scores are; each SM sub-partition holds one softmax warp of each tile.
+// With one tile (blocks of 128 rows), tile 0 uses both tiles' S and P
+// columns as two buffers and S(s+1) is issued before PV(s).
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax of tile 0: thread owns row (warp % 4) * 32 + lane (TMEM lane)
+//   warps 4-7  softmax of tile 1 (idle when the block has 128 rows or fewer)
+//   warp 8     MMA issuer (one thread)
+//   warp 9     TMA producer: block ids one stage ahead, one tile load per
 //              page segment and 128-byte chunk
-// Tiles are numbered over the batch's prefill sequences in order, each
-// sequence's tiles last token first; each CTA finds its (sequence, first
-// token) by walking subsequence_begins.
+// Row blocks are numbered over the batch's prefill sequences in order, each
+// sequence's blocks last token first (the longest start first); each CTA
+// finds its (sequence, first token) by walking subsequence_begins.
 #pragma once
 
 #include "pa_partition_tc.cuh"
 
 namespace pa {
 
+// 2^x on the SFU, as a pure function the compiler may schedule freely.
+__device__ __forceinline__ float ex2_free(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Thread i of the warp reads 64 consecutive 32-bit columns of TMEM lane
+// (lane base + i) in one load, waited in the same statement.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, "
+      "%36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, "
+      "%57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
 template <int D, int KV>
-__global__ void __launch_bounds__(192, 1)
+struct PfCfg {
+  static_assert(KV == KV_BF16 || KV == KV_F16, "prefill tiles take 16-bit caches");
+  static_assert(D == 64 || D == 128, "prefill tiles: head_dim 64 or 128");
+  static constexpr bool kBf16 = (KV == KV_BF16);
+  static constexpr int SK = 64;                  // keys per stage
+  static constexpr int CH = D / 64;              // 128-byte chunks per row
+  static constexpr int TILE = SK * D * 2;        // one K (or V) stage tile
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int QT = 128 * D * 2;         // one query tile, [chunk][row][128 B]
+  static constexpr int RING_OFF = 2 * QT;
+  static constexpr int FIXED = 2 * QT + 512 + 1024;
+  static constexpr int NS_FIT = (226 * 1024 - FIXED) / STAGE;
+  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
+  static constexpr int BAR_OFF = RING_OFF + NS * STAGE;
+  static constexpr int BYTES = BAR_OFF + 512 + 1024;
+  // TMEM columns: O_t [t D, t D + D), S_t [2 D + t SK, +SK), P_t (16-bit
+  // pairs) [2 D + 2 SK + t SK / 2, +SK / 2)
+  static constexpr int S_COL = 2 * D;
+  static constexpr int P_COL = 2 * D + 2 * SK;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_S = tc_idesc(128, SK, kBf16, false);
+  static constexpr uint32_t IDESC_PV = tc_idesc(128, D, kBf16, true);
+  static_assert(NS >= 3, "pipeline needs a few stages");
+  static_assert(P_COL + SK <= TMEM_COLS, "tensor-memory budget");
+};
+
+template <int D, int KV>
+__global__ void __launch_bounds__(320, 1)
     pa_prefill_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const PartArgs a) {
-  using C = TcCfg<D, KV>;
+  using C = PfCfg<D, KV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem + C::RING_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* full = bars;                 // [NS] TMA landed
-  uint64_t* empty = full + C::NS;        // [NS] stage consumed (MMA commit after PV)
-  uint64_t* s_full = empty + C::NS;      // [2] S buffer written (MMA commit)
-  uint64_t* s_free = s_full + 2;         // [2] S buffer read (4 softmax warps)
-  uint64_t* p_full = s_free + 2;         // [2] P buffer written (4 softmax warps)
-  uint64_t* pv_done = p_full + 2;        // [2] PV of the stage using that P buffer done (MMA commit)
+  uint64_t* empty = full + C::NS;        // [NS] stage consumed (MMA commit after the last PV)
+  uint64_t* s_full = empty + C::NS;      // [2] S_t written (MMA commit)
+  uint64_t* s_free = s_full + 2;         // [2] S_t read (4 softmax warps of tile t)
+  uint64_t* p_full = s_free + 2;         // [2] P_t written (4 softmax warps of tile t)
+  uint64_t* pv_done = p_full + 2;        // [2] PV_t done (MMA commit)
   __shared__ uint32_t s_tmem;
   __shared__ int s_bad, s_timeout;
 
   const int g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int TQ = 128 / a.G;  // new tokens per row tile
+  const int TQ = a.row_cap / a.G;  // new tokens per row block (a.row_cap = 128 or 256 rows)
   pdl_wait_primary();        // inputs and outputs may belong to the previous kernel
 
-  // ---- which sequence and tokens this tile covers ----
+  // ---- which sequence and tokens this row block covers ----
   int b = -1, i0 = 0;
   {
-    long long tile = blockIdx.x;
+    long long blk = blockIdx.x;
     for (int s = 0; s < a.num_seqs; ++s) {
       const int T = ld_once(a.begins + s + 1) - ld_once(a.begins + s);
       if (T <= PA_MAX_QUERY_LEN) continue;  // a verify step (or malformed: reported below)
-      const long long nt = (T + TQ - 1) / TQ;
-      if (tile < nt) {
-        // a chunk's tiles in reverse: the last tokens see the most keys, so
-        // the longest tiles are scheduled first
+      const long long nb = (T + TQ - 1) / TQ;
+      if (blk < nb) {
         b = s;
-        i0 = static_cast<int>(nt - 1 - tile) * TQ;
+        i0 = static_cast<int>(nb - 1 - blk) * TQ;  // last tokens (most keys) first
         break;
       }
-      tile -= nt;
+      blk -= nb;
     }
   }
   pdl_launch_dependents();
   if (b < 0) return;
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
                               a.part_tokens, a.row_cap, kRoleLong);
-  const int nt = min(TQ, si.T - i0);  // tokens of this tile
-  const int R = nt * a.G;             // real rows
+  const int ntok = min(TQ, si.T - i0);  // tokens of this row block
+  const int R = ntok * a.G;             // real rows (at most 256)
   if (si.err) {
     if (threadIdx.x == 0) atomicOr(a.status, si.err);
     if (si.rows_ok)
@@ -85,72 +148,62 @@ __global__ void __launch_bounds__(192, 1)
       }
     return;
   }
-  if (nt <= 0) return;
+  if (ntok <= 0) return;
+  const bool two = R > 128;  // block-uniform: tile 1 has real rows
 
   const int klo = a.window > 0 ? max(0, si.L + i0 - a.window + 1) : 0;
-  const int khi = si.L + i0 + nt - 1;
+  const int khi = si.L + i0 + ntok - 1;
   const int kstart = (klo >> a.ps_log2) << a.ps_log2;  // page aligned
   const int kend = khi + 1;
   const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
 
-  if (threadIdx.x == 160) {
+  if (threadIdx.x == 288) {
     s_bad = 0;
     s_timeout = 0;
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-      mbar_init(&p_full[i], 4);
-      mbar_init(&pv_done[i], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 4);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&pv_done[t], 1);
     }
     fence_barrier_init();
   }
   __syncthreads();
   uint32_t tmem = 0;
-  if (warp < 5) {
+  if (warp < 9) {
     if (warp == 0) {
       tmem_alloc(&s_tmem, C::TMEM_COLS);
       tmem_relinquish();
     }
-    tc_fence_before();
-    bar_sync_n(2, 160);  // the TMEM address is published
-    tc_fence_after();
-    tmem = s_tmem;
-    if (warp < 4) {
-      // Q rows into TMEM lanes 0..127 (two 16-bit elements per column);
-      // rows past the tile's tokens are zero
-      const int r = warp * 32 + lane;
+    if (warp < 8) {
+      // Q rows into shared memory, 128B-swizzled K-major tiles (the layout a
+      // TMA load would give): unit u of row rr of tile t at
+      // t QT + (c 128 + rr) 128 + (u ^ (rr & 7)) 16; rows past the block's
+      // tokens are zero
+      const int r = warp * 32 + lane, t = r >> 7, rr = r & 127;
       const bool real = r < R;
       const size_t row = real ? static_cast<size_t>(si.t0 + i0 + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + row * D);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
+      for (int c = 0; c < C::CH; ++c)
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const uint4 x = real ? __ldg(src + 8 * c + u) : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * u] = x.x;
-          v[4 * u + 1] = x.y;
-          v[4 * u + 2] = x.z;
-          v[4 * u + 3] = x.w;
+          *reinterpret_cast<uint4*>(smem + t * C::QT + (c * 128 + rr) * 128 + ((u ^ (rr & 7)) << 4)) = x;
         }
-        tmem_st32(tmem + C::Q_COL + 32 * c + (static_cast<uint32_t>(warp * 32) << 16),
-                  reinterpret_cast<const float*>(v));
-      }
+      fence_proxy_async();  // Q, seen by the tensor cores' proxy
     }
     tc_fence_before();
-    bar_sync_n(2, 160);  // Q is in place for the MMA warp
+    bar_sync_n(2, 288);  // the TMEM address is published and Q is in place
     tc_fence_after();
+    tmem = s_tmem;
   }
-  const uint32_t tm_o = tmem;
-  const uint32_t tm_s0 = tmem + C::S_COL;
-  const uint32_t tm_p0 = tmem + C::P_COL;
-  const uint32_t tm_q = tmem + C::Q_COL;
 
-  if (warp == 5) {
+  if (warp == 9) {
     // =========================== TMA producer ===============================
     if (lane == 0) {
       prefetch_tensormap(&tmK);
@@ -159,7 +212,7 @@ __global__ void __launch_bounds__(192, 1)
     const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
     const int br_log2 = a.box_log2, br = 1 << br_log2;  // rows per tile load (page size, at most 64)
     int bad = 0;
-    // block id of segment `lane` of stage s (0 past the tile's keys)
+    // block id of segment `lane` of stage s (0 past the block's keys)
     auto load_id = [&](int s) -> int {
       const int key = kstart + s * C::SK + (lane << br_log2);
       return (lane < (C::SK >> br_log2) && key < kend) ? __ldg(bt + (key >> a.ps_log2)) : 0;
@@ -183,13 +236,12 @@ __global__ void __launch_bounds__(192, 1)
       const int key0 = kstart + s * C::SK;
       const int nk = min(C::SK, kend - key0);
       const int nseg = (nk + br - 1) >> br_log2;
-      uint8_t* st = smem + slot * C::STAGE;
+      uint8_t* st = ring + slot * C::STAGE;
       if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nseg * br * D * 2 * 2));
       __syncwarp();
-      const int j = lane;  // one (segment, chunk) pair per lane: nseg * CH <= 16
-      const int seg = j / C::CH, c = j % C::CH;
+      const int seg = lane / C::CH, c = lane % C::CH;  // one (segment, chunk) pair per lane: nseg * CH <= 16
       const int sid = __shfl_sync(0xffffffffu, id, seg & 31);
-      if (j < nseg * C::CH) {
+      if (lane < nseg * C::CH) {
         const int key = key0 + (seg << br_log2);
         const uint32_t off = static_cast<uint32_t>((c * C::SK + (seg << br_log2)) * 128);
         tma_load_4d(st + off, &tmK, c * 64, key & (a.ps - 1), g, sid, &full[slot]);
@@ -200,128 +252,188 @@ __global__ void __launch_bounds__(192, 1)
       s_bad = 1;
       atomicOr(a.status, PA_STATUS_BLOCK_ID);
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // =========================== MMA issuer =================================
+    // Per stage s: S_0(s); [PV_1(s-1); S_1(s)]; PV_0(s).  A stage's slot is
+    // released after the last PV that reads it.
     if (lane == 0) {
       bool ok = true;
-      auto issue_pv = [&](int s) -> bool {
-        const int slot = s % C::NS, pb = s & 1;
-        if (!mbar_wait(&p_full[pb], (s >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(smem + slot * C::STAGE + C::TILE);
-#pragma unroll
-        for (int j = 0; j < C::SK / 16; ++j) {
-          const uint64_t bd = sw128_desc(v_base + j * 16 * 128, C::SK * 128, 1024);
-          tc_mma_ta(tm_o, tm_p0 + pb * (C::SK / 2) + 8 * j, bd, C::IDESC_PV, (s > 0 || j > 0) ? 1u : 0u);
-        }
-        tc_commit(&pv_done[pb]);
-        tc_commit(&empty[slot]);
-        return true;
-      };
-      for (int s = 0; s < n_stages && ok; ++s) {
-        const int slot = s % C::NS, sb = s & 1;
-        if (!mbar_wait(&full[slot], (s / C::NS) & 1)) {
-          ok = false;
-          break;
-        }
-        if (s >= 2 && !mbar_wait(&s_free[sb], ((s >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_base = smem_u32(smem + slot * C::STAGE);
+      // S of tile t for stage s into score buffer bi
+      auto issue_s = [&](int t, int bi, int s) {
+        const uint32_t k_base = smem_u32(ring + (s % C::NS) * C::STAGE);
+        const uint32_t q_base = smem_u32(smem + t * C::QT);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int c = kk >> 2, w = kk & 3;
+          const uint64_t ad = sw128_desc(q_base + c * 128 * 128 + 32 * w, 16, 1024);
           const uint64_t bd = sw128_desc(k_base + c * C::SK * 128 + 32 * w, 16, 1024);
-          tc_mma_ta(tm_s0 + sb * C::SK, tm_q + 8 * kk, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          tc_mma(tmem + C::S_COL + bi * C::SK, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[sb]);
-        if (s >= 1) ok = issue_pv(s - 1);
+        tc_commit(&s_full[bi]);
+      };
+      // O_t += P (buffer bi, written in phase ph) . V_s
+      auto issue_pv = [&](int t, int bi, uint32_t ph, int s) -> bool {
+        if (!mbar_wait(&p_full[bi], ph)) return false;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(ring + (s % C::NS) * C::STAGE + C::TILE);
+#pragma unroll
+        for (int j = 0; j < C::SK / 16; ++j) {
+          const uint64_t bd = sw128_desc(v_base + j * 16 * 128, C::SK * 128, 1024);
+          tc_mma_ta(tmem + t * D, tmem + C::P_COL + bi * (C::SK / 2) + 8 * j, bd, C::IDESC_PV,
+                    (s > 0 || j > 0) ? 1u : 0u);
+        }
+        tc_commit(&pv_done[bi]);
+        return true;
+      };
+      if (two) {
+        // two tiles, one buffer each (index t, phase s & 1):
+        // S_0(s); PV_1(s-1); S_1(s); PV_0(s)
+        for (int s = 0; s < n_stages && ok; ++s) {
+          if (!mbar_wait(&full[s % C::NS], (s / C::NS) & 1) || (s >= 1 && !mbar_wait(&s_free[0], (s - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(0, 0, s);
+          if (s >= 1) {
+            if (!(ok = issue_pv(1, 1, (s - 1) & 1, s - 1))) break;
+            tc_commit(&empty[(s - 1) % C::NS]);
+            if (!mbar_wait(&s_free[1], (s - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          issue_s(1, 1, s);
+          if (!(ok = issue_pv(0, 0, s & 1, s))) break;
+        }
+        if (ok && n_stages >= 1) {
+          ok = issue_pv(1, 1, (n_stages - 1) & 1, n_stages - 1);
+          if (ok) tc_commit(&empty[(n_stages - 1) % C::NS]);
+        }
+      } else {
+        // one tile, two buffers (index s & 1, phase (s >> 1) & 1):
+        // S(s) before PV(s-1), so the tensor cores work during the softmax
+        for (int s = 0; s < n_stages && ok; ++s) {
+          const int sb = s & 1;
+          if (!mbar_wait(&full[s % C::NS], (s / C::NS) & 1) ||
+              (s >= 2 && !mbar_wait(&s_free[sb], ((s >> 1) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(0, sb, s);
+          if (s >= 1) {
+            if (!(ok = issue_pv(0, (s - 1) & 1, ((s - 1) >> 1) & 1, s - 1))) break;
+            tc_commit(&empty[(s - 1) % C::NS]);
+          }
+        }
+        if (ok && n_stages >= 1) {
+          ok = issue_pv(0, (n_stages - 1) & 1, ((n_stages - 1) >> 1) & 1, n_stages - 1);
+          if (ok) tc_commit(&empty[(n_stages - 1) % C::NS]);
+        }
       }
-      if (ok && n_stages >= 1) ok = issue_pv(n_stages - 1);
       if (!ok) {
         atomicOr(a.status, PA_STATUS_TIMEOUT);
         atomicOr(&s_timeout, 1);
       }
     }
     __syncwarp();
-  } else {
-    // =========================== softmax warps (rows) =======================
-    const int r = warp * 32 + lane;  // TMEM lane / query row
-    const int rc = min(r, R - 1);    // padding rows mask like the last real row
-    const int i = i0 + rc / a.G;     // the row's new token
+  } else if (warp < 4 || two) {
+    // ===================== softmax warps of tile t (rows) ===================
+    const int t = warp >> 2, quarter = warp & 3;
+    const int r = t * 128 + quarter * 32 + lane;  // row of the block (TMEM lane r % 128 of tile t)
+    const int rc = min(r, R - 1);                 // padding rows mask like the last real row
+    const int i = i0 + rc / a.G;                  // the row's new token
     const int hi = si.L + i;
     const int lo = a.window > 0 ? si.L + i - a.window + 1 : INT_MIN;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tm_o = tmem + t * D + lane_off;
     const float sl2 = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int s = 0; s < n_stages; ++s) {
-      const int sb = s & 1;
-      if (!mbar_wait(&s_full[sb], (s >> 1) & 1)) {
+      // buffer and barrier index of this stage's S and P, and the phase of
+      // stage s on them: one per tile (two tiles), or alternating (one tile)
+      const int bi = two ? t : (s & 1);
+      const uint32_t ph = two ? (s & 1) : ((s >> 1) & 1);
+      if (!mbar_wait(&s_full[bi], ph)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float x[C::SK];
-      tmem_ld32(tm_s0 + sb * C::SK + lane_off, x);
-      tmem_ld32(tm_s0 + sb * C::SK + 32 + lane_off, x + 32);
+      float x[C::SK];  // raw scores q.k (the scale is applied inside the exponent)
+      tmem_ld64(tmem + C::S_COL + bi * C::SK + lane_off, x);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+      if (lane == 0) mbar_arrive(&s_free[bi]);
 
       const int key0 = kstart + s * C::SK;
       const bool clean = key0 >= lo && key0 + C::SK - 1 <= hi;
-      float mt = -INFINITY;
+      if (!clean) {
 #pragma unroll
-      for (int j = 0; j < C::SK; ++j) {
-        float v = x[j] * sl2;
-        if (!clean) {
+        for (int j = 0; j < C::SK; ++j) {
           const int key = key0 + j;
-          v = (key >= lo && key <= hi) ? v : -INFINITY;
+          x[j] = (key >= lo && key <= hi) ? x[j] : -INFINITY;
         }
-        x[j] = v;
-        mt = fmaxf(mt, v);
       }
+      // row max in four independent chains; scaling by sl2 > 0 commutes
+      // with the max (-inf stays -inf)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < C::SK; ++j) m4[j & 3] = fmaxf(m4[j & 3], x[j]);
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+      // lazy running max: move the reference only when the row max grows by
+      // more than 2^8 (or on the first finite score)
       const bool need = (mt > m_ref + 8.f) || (m_ref == -INFINITY && mt != -INFINITY);
       const float m_new = need ? mt : m_ref;
-      const float alpha = need ? ex2(m_ref - m_new) : 1.f;
-      if (__any_sync(0xffffffffu, need) && s >= 1) {
-        if (!mbar_wait(&pv_done[(s - 1) & 1], ((s - 1) >> 1) & 1)) {
+      const float alpha = need ? ex2(m_ref - m_new) : 1.f;  // 0 when m_ref was -inf
+      // O_t is rescaled once PV(s-1) is done; with one P buffer per tile
+      // that is also when P(s) may replace P(s-1)
+      if (s >= 1 && (two || __any_sync(0xffffffffu, need))) {
+        const int pb = two ? t : ((s - 1) & 1);
+        const uint32_t pph = two ? ((s - 1) & 1) : (((s - 1) >> 1) & 1);
+        if (!mbar_wait(&pv_done[pb], pph)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32(tm_o + 32 * c + lane_off, o);
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tm_o + 32 * c, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tm_o + 32 * c + lane_off, o);
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tm_o + 32 * c, o);
+          }
         }
-        tc_fence_before();
       }
-      l *= alpha;
       m_ref = m_new;
-      const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
       uint32_t pk[C::SK / 2];
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < C::SK; j += 2) {
-        const float p0 = ex2(x[j] - mu), p1 = ex2(x[j + 1] - mu);
-        l += p0 + p1;
+        const float p0 = ex2_free(fmaf(x[j], sl2, nmu)), p1 = ex2_free(fmaf(x[j + 1], sl2, nmu));
+        l4[(j >> 1) & 3] += p0 + p1;
         pk[j / 2] = pack2<C::kBf16>(p0, p1);
       }
-      if (s >= 2 && !mbar_wait(&pv_done[sb], ((s >> 1) - 1) & 1)) {
-        ok = false;
-        break;
+      l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+      // one tile: P buffer s & 1 is free once PV(s-2) is done
+      if (!two && s >= 2) {
+        if (!mbar_wait(&pv_done[bi], ((s >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
       }
-      tmem_st32(tm_p0 + sb * (C::SK / 2) + lane_off, reinterpret_cast<const float*>(pk));
-      // V rows of keys outside the tile's range may hold garbage (even NaN):
-      // their weights are 0 but 0 * NaN is not, so clear them
-      if (key0 < klo || key0 + C::SK - 1 > khi) {
-        uint8_t* vt = smem + (s % C::NS) * C::STAGE + C::TILE;
+      tmem_st32(tmem + C::P_COL + bi * (C::SK / 2) + lane_off, reinterpret_cast<const float*>(pk));
+      // V rows of keys outside the block's range may hold garbage (even NaN):
+      // their weights are 0 but 0 * NaN is not, so tile 0's warps clear them
+      // (both tiles' PV of the stage are issued after tile 0's P)
+      if (t == 0 && (key0 < klo || key0 + C::SK - 1 > khi)) {
+        uint8_t* vt = ring + (s % C::NS) * C::STAGE + C::TILE;
         for (int idx = threadIdx.x; idx < C::SK * C::CH * 8; idx += 128) {
           const int k = idx / (C::CH * 8), rem = idx % (C::CH * 8);
           const int key = key0 + k;
@@ -332,10 +444,13 @@ __global__ void __launch_bounds__(192, 1)
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
+      if (lane == 0) mbar_arrive(&p_full[bi]);
     }
     // ---- epilogue: normalised O row from TMEM -> output ----
-    if (ok && n_stages >= 1 && !mbar_wait(&pv_done[(n_stages - 1) & 1], ((n_stages - 1) >> 1) & 1)) ok = false;
+    if (ok && n_stages >= 1) {
+      const int n1 = n_stages - 1;
+      if (!mbar_wait(&pv_done[two ? t : (n1 & 1)], two ? (n1 & 1) : ((n1 >> 1) & 1))) ok = false;
+    }
     if (!ok && lane == 0) {
       atomicOr(a.status, PA_STATUS_TIMEOUT);
       atomicOr(&s_timeout, 1);
@@ -348,7 +463,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       float o[32];
-      tmem_ld32(tm_o + 32 * c + lane_off, o);
+      tmem_ld32(tm_o + 32 * c, o);
       if (real) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, o[e] * inv);
