@@ -113,6 +113,35 @@ __device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// 2^x on the SFU, as a pure function the compiler may schedule freely.
+__device__ __forceinline__ float ex2_free(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Thread i of the warp reads 64 consecutive 32-bit columns of TMEM lane
+// (lane base + i) in one load, waited in the same statement.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, "
+      "%36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, "
+      "%57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
 // start address, leading / stride byte offsets (16-byte units), version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
@@ -491,9 +520,8 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
         break;
       }
       tc_fence_after();
-      float x[C::SK];
-      tmem_ld32(tm_s0 + sb * C::SK + lane_off, x);
-      tmem_ld32(tm_s0 + sb * C::SK + 32 + lane_off, x + 32);
+      float x[C::SK];  // raw scores q.k (the scale is applied inside the exponent)
+      tmem_ld64(tm_s0 + sb * C::SK + lane_off, x);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
@@ -518,21 +546,23 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
           vmask = range & (past | named);
         }
       }
-      float mt = -INFINITY;
+      if (!clean) {
 #pragma unroll
-      for (int j = 0; j < C::SK; ++j) {
-        float v = x[j] * sl2;
-        if (!clean) {
+        for (int j = 0; j < C::SK; ++j) {
           if constexpr (TREE) {
-            v = ((vmask >> j) & 1ull) ? v : -INFINITY;
+            x[j] = ((vmask >> j) & 1ull) ? x[j] : -INFINITY;
           } else {
             const int key = key0 + j;
-            v = (key >= lo && key <= hi) ? v : -INFINITY;
+            x[j] = (key >= lo && key <= hi) ? x[j] : -INFINITY;
           }
         }
-        x[j] = v;
-        mt = fmaxf(mt, v);
       }
+      // row max in four independent chains; scaling by sl2 > 0 commutes
+      // with the max (-inf stays -inf)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < C::SK; ++j) m4[j & 3] = fmaxf(m4[j & 3], x[j]);
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
       // lazy running max: move the reference only when the row max grows by
       // more than 2^8 (or on the first finite score)
       const bool need = (mt > m_ref + 8.f) || (m_ref == -INFINITY && mt != -INFINITY);
@@ -555,16 +585,17 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
         }
         tc_fence_before();
       }
-      l *= alpha;
       m_ref = m_new;
-      const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
       uint32_t pk[C::SK / 2];
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < C::SK; j += 2) {
-        const float p0 = ex2(x[j] - mu), p1 = ex2(x[j + 1] - mu);
-        l += p0 + p1;
+        const float p0 = ex2_free(fmaf(x[j], sl2, nmu)), p1 = ex2_free(fmaf(x[j + 1], sl2, nmu));
+        l4[(j >> 1) & 3] += p0 + p1;
         pk[j / 2] = pack2<C::kBf16>(p0, p1);
       }
+      l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
       // the P buffer is free once the PV two stages back has finished
       if (s >= 2 && !mbar_wait(&pv_done[sb], ((s >> 1) - 1) & 1)) {
         ok = false;

@@ -1,11 +1,11 @@
 """Mixed batches on the GPU (pa_forward_mixed, through the C ABI): verify
 steps (T_b <= 8) on the split-KV kernels and prefill chunks (T_b > 8) on the
 prefill tile kernel, in one call, against the oracle (whose causal rule holds
-for any number of new tokens).  Cases cover every query-head group size the
-tiles handle (G = 1, 2, 4, 6, 8: 128-row tiles of 128 / G tokens, ragged last
-tiles), windows, f16 / bf16 / fp32 caches, large pages, and device errors in
-a prefill chunk; a mixed call with no prefill chunk is pa_verify_forward bit
-for bit."""
+for any number of new tokens).  Cases cover the query-head group sizes the
+tiles handle (G = 1, 2, 4, 6, 8: blocks of 128 / G or 256 / G tokens, ragged
+last blocks, one-tile and two-tile blocks), windows, f16 / bf16 / fp32
+caches, large pages, and device errors in a prefill chunk; a mixed call with
+no prefill chunk is pa_verify_forward bit for bit."""
 import numpy as np
 import pytest
 
@@ -48,6 +48,8 @@ CASES = [
     (mk("mixed_f32", 77, [3, 20], [40, 10], 4, 2, d=64, q_dtype="f32", kv_dtype="f32"), True),
     (mk("prefill_ps128", 78, [70, 2], [1000, 130], 32, 8, ps=128), False),
     (mk("prefill_ps8_win1", 79, [40], [100], 8, 2, ps=8, sliding_window=1), True),
+    # enough rows for two waves of 256-row blocks: the two-tile ping-pong path
+    (mk("prefill_256_rows", 85, [1200, 2], [100, 300], 64, 32, d=64), True),
 ]
 
 
