@@ -134,11 +134,12 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const long long rows = static_cast<long long>(G) * tmax;
   int kernel = (kv == PA_F32) ? 1 : 0;
   int nt = 0, sk = 64, smem = 0, ctas_per_sm = 4;
-  // 16-bit caches with 8 or more query rows per KV head (T > 1 verify
-  // steps, wide GQA groups) go to the tensor-memory path: its cost per key
-  // does not grow with the row count (measured: T=4 x 4 heads and T=8 x 8
-  // heads cost 1.02-1.07x a single-token step).  Up to 4 rows the warp-level
-  // path is slightly faster.
+  // 16-bit caches go to the tensor-memory path: its cost per key does not
+  // grow with the row count (measured: T=4 x 4 heads and T=8 x 8 heads cost
+  // 1.01-1.05x a single-token step), and with head_dim 128 it is also the
+  // faster one for a single token (T=1 x 4 heads at 32k keys: 28.3 us vs
+  // 29.4 us on the warp-level kernel).  With head_dim 64 the warp-level
+  // kernel stays ahead below 8 rows (10.8 vs 10.9 us).
   const bool tc16 = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128);
   const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
   // tree masks run on every kernel but the 16-bit keys-on-M one and the u8
@@ -186,7 +187,7 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
       ctas_per_sm = info.ctas_per_sm;
     }
   }
-  if (kernel == 0 && tc_ok && choice != 1 && ((rows >= 8 && tc16) || choice == 2)) {
+  if (kernel == 0 && tc_ok && choice != 1 && ((tc16 && (rows >= 8 || D == 128)) || choice == 2)) {
     bool ok = false;
     pa::MmaKernelInfo info = pa::tc_info(D, mma_kind(kv), &ok);
     if (ok) {

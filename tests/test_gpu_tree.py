@@ -1,9 +1,9 @@
 """Tree-mask verify on the GPU (pa_verify_forward_tree, through the C ABI)
 against the oracle's tree definition: random draft trees per sequence on
-each default kernel (warp-level mma for <= 7 query rows per KV head, the
-tensor-memory kernel for 8..64 rows, the fp32 path), with windows, batches,
-empty sequences and one- or many-partition contexts; and a chain mask must
-reproduce pa_verify_forward bit for bit."""
+each default kernel (warp-level mma for head_dim 64 below 8 query rows per
+KV head, head_dim 256 and u8; the tensor-memory kernels otherwise; the fp32
+path), with windows, batches, empty sequences and one- or many-partition
+contexts; and a chain mask must reproduce pa_verify_forward bit for bit."""
 import numpy as np
 import pytest
 
@@ -30,7 +30,7 @@ def random_tree_masks(case, seed):
 CASES = [
     # (case, kernel the plan picks, short context -> derived bound)
     (lambda: W.make_case("tree_mma", seed=101, query_lens=[7], past_lens=[3000], num_q_heads=8, num_kv_heads=8,
-                         head_dim=128, page_size=16), 0, False),
+                         head_dim=64, page_size=16), 0, False),
     (lambda: W.qwen_gqa(8, 2500, seed=102), 2, False),
     (lambda: W.long_ctx_b(3000, seed=103), 2, False),
     (lambda: W.make_case("tree_batch_win", seed=104, query_lens=[5, 0, 8, 3], past_lens=[900, 10, 1300, 40],

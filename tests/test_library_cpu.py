@@ -43,7 +43,8 @@ def dims(**kw):
 
 
 def test_plan_fills_the_sms_once_at_long_context(lib):
-    p = pa.plan(dims(total_tokens=1), 32769, 0, pa.PA_BF16, 152)
+    # head_dim 64, 4 rows per KV head: the warp-level kernel, two CTAs per SM
+    p = pa.plan(dims(total_tokens=1, head_dim=64), 32769, 0, pa.PA_BF16, 152)
     assert p.kernel == 0 and p.row_tiles == 1
     assert p.part_tokens % max(p.stage_keys, 16) == 0
     assert p.num_partitions * p.part_tokens >= 32769
@@ -61,8 +62,12 @@ def test_plan_independent_of_query_count(lib):
     dual-radeon-vllm article describe)."""
     ps = [pa.plan(dims(total_tokens=t), 32768 + t, 0, pa.PA_BF16, 152).num_partitions for t in (2, 3, 4)]
     assert min(ps) == max(ps) and ps[0] > 16
-    # T=1 (4 rows) takes the warp-level kernel at two CTAs per SM: twice the split
+    # T=1 (4 rows) keeps the split too
     assert pa.plan(dims(total_tokens=1), 32769, 0, pa.PA_BF16, 152).num_partitions >= ps[0]
+    # and on the warp-level kernel (head_dim 64, two CTAs per SM) T = 1..4 split alike
+    ps64 = [pa.plan(dims(total_tokens=t, head_dim=64), 32768 + t, 0, pa.PA_BF16, 152).num_partitions
+            for t in (1, 2, 3, 4)]
+    assert min(ps64) >= 16
 
 
 def test_plan_window_reads_only_the_window(lib):
