@@ -743,3 +743,15 @@ def test_mixed_batch_is_each_sequence_alone(oracle_mod):
                                    head_dim=case.head_dim, page_size=case.page_size, num_blocks=case.num_blocks,
                                    scale=case.scale)
         assert np.array_equal(got[t0:t1], alone)
+
+
+@pytest.mark.parametrize("ps", [1, 2, 4, 32])
+def test_relayout_keeps_the_logical_cache(oracle_mod, ps):
+    """workloads.relayout (used by the GPU page-size test) moves keys into
+    pages of another size without changing what the definition reads:
+    bitwise the same output, with a window, a batch and 16-bit storage."""
+    case = W.make_case("relay", seed=41, query_lens=[3, 0, 5], past_lens=[37, 4, 60], num_q_heads=8,
+                       num_kv_heads=2, head_dim=16, page_size=8, sliding_window=21)
+    moved = W.relayout(case, ps, seed=5)
+    assert moved.page_size == ps and moved.block_tables.shape[0] == case.num_seqs
+    assert np.array_equal(run_oracle(oracle_mod, moved), run_oracle(oracle_mod, case))
