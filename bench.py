@@ -268,10 +268,8 @@ def kernel_name(wl) -> str:
         return f"pa_partition_tc<D={wl.D},{wl.kv},gather> (tcgen05, cp.async page gather)"
     if p.kernel == 2:
         return f"pa_partition_tc<D={wl.D}, {wl.kv}> (tcgen05, TMEM accumulators)"
-    if p.kernel == 3:
-        return f"pa_partition_tk<D={wl.D}, {wl.kv}, N={p.row_tiles}> (tcgen05, keys on M)"
     if p.kernel == 4:
-        return f"pa_partition_tku8<N={p.row_tiles}> (tcgen05, keys on M, u8 codes in TMEM)"
+        return f"pa_partition_u8<N={p.row_tiles}, page {wl.ps}> (tcgen05, keys on M, u8 codes converted into TMEM)"
     if p.kernel == 1:
         return f"pa_partition_f32<D={wl.D}>"
     return f"pa_partition_mma<D={wl.D}, {wl.kv}, n-tiles={p.row_tiles}> (mma.sync)"
@@ -381,25 +379,45 @@ def time_e2e(wl, steps, warmup, stream, graph=True):
     """Through the public API with host buffers: every step copies its query
     tokens, block table, past_lens and subsequence_begins from pinned host
     memory, runs the verify step, and copies the output back to pinned host
-    memory, all inside the timed region.  The KV cache is resident device
-    state (the cache of a serving engine), as it is between verify steps.
-    graph=True captures the per-step sequence (copies + launches) in a CUDA
-    graph, as a serving loop would; graph=False issues it eagerly."""
+    memory, all inside the timed region.  The step's inputs are packed in one
+    pinned host buffer ([q | block table | past_lens | begins], each part
+    16-byte aligned) and move with one host-to-device copy into a device
+    buffer the call's input pointers point into; the output comes back with
+    one device-to-host copy.  The KV cache is resident device state (the cache
+    of a serving engine), as it is between verify steps.  graph=True captures
+    the per-step sequence (copies + launches) in a CUDA graph, as a serving
+    loop would; graph=False issues it eagerly."""
     import torch
     import paged_attention_speculative_gb300 as pa
-    q_h = wl.q.cpu().pin_memory()
-    pl_h = wl.past_lens.cpu().pin_memory()
-    sb_h = wl.begins.cpu().pin_memory()
-    bt_h = wl.block_tables_host
+
+    def align16(n):
+        return (n + 15) // 16 * 16
+
+    q_bytes = wl.q.numel() * wl.q.element_size()
+    bt_bytes = wl.block_tables[0].numel() * 4
+    pl_bytes = wl.past_lens.numel() * 4
+    sb_bytes = wl.begins.numel() * 4
+    o_bt = align16(q_bytes)
+    o_pl = o_bt + align16(bt_bytes)
+    o_sb = o_pl + align16(pl_bytes)
+    total = o_sb + align16(sb_bytes)
+    # one packed host buffer per replica (its block table differs)
+    host = torch.empty((wl.replicas, total), dtype=torch.uint8).pin_memory()
+    for r in range(wl.replicas):
+        host[r, :q_bytes] = wl.q.cpu().view(torch.uint8).reshape(-1)
+        host[r, o_bt:o_bt + bt_bytes] = wl.block_tables_host[r].view(torch.uint8).reshape(-1)
+        host[r, o_pl:o_pl + pl_bytes] = wl.past_lens.cpu().view(torch.uint8).reshape(-1)
+        host[r, o_sb:o_sb + sb_bytes] = wl.begins.cpu().view(torch.uint8).reshape(-1)
+    dev = torch.empty(total, dtype=torch.uint8, device="cuda")
+    q_d = dev[:q_bytes].view(wl.q.dtype).view(wl.q.shape)
+    bt_d = dev[o_bt:o_bt + bt_bytes].view(torch.int32).view(wl.block_tables[0].shape)
+    pl_d = dev[o_pl:o_pl + pl_bytes].view(torch.int32)
+    sb_d = dev[o_sb:o_sb + sb_bytes].view(torch.int32)
     out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    bt_d = torch.empty_like(wl.block_tables[0])
 
     def step(s):
-        wl.q.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h[s % wl.replicas], non_blocking=True)
-        wl.past_lens.copy_(pl_h, non_blocking=True)
-        wl.begins.copy_(sb_h, non_blocking=True)
-        pa.forward(wl.q, wl.k, wl.v, bt_d, wl.past_lens, wl.begins, wl.max_ctx, wl.scale, wl.window, wl.kv_code,
+        dev.copy_(host[s % wl.replicas], non_blocking=True)
+        pa.forward(q_d, wl.k, wl.v, bt_d, pl_d, sb_d, wl.max_ctx, wl.scale, wl.window, wl.kv_code,
                    wl.out, wl.dims, wl.ws, stream=stream)
         out_h.copy_(wl.out, non_blocking=True)
 
@@ -433,8 +451,10 @@ def time_e2e(wl, steps, warmup, stream, graph=True):
             e1.record(stream)
             e1.synchronize()
             done = steps
+    got = out_h.float()
+    assert torch.isfinite(got).all(), "end-to-end output not finite"
     us = e0.elapsed_time(e1) * 1e3 / done
-    h2d = wl.q.numel() * wl.q.element_size() + bt_d.numel() * 4 + wl.past_lens.numel() * 4 + wl.begins.numel() * 4
+    h2d = total
     d2h = wl.out.numel() * wl.out.element_size()
     return us, h2d, d2h
 

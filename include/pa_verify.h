@@ -203,16 +203,20 @@ int pa_verify_combine(const int32_t* past_lens, const int32_t* subsequence_begin
  * split-KV partials live in a 16 MiB device array inside the library (held
  * by every GPU that loads the library until the process exits).  A call
  * whose partials need more than that (total_tokens x Hq x partitions x
- * (4*head_dim + 8) bytes, plus 256) returns PA_ERR_WORKSPACE and launches
- * nothing; nothing is allocated, on any path.
+ * (4*head_dim + 8) bytes, plus 256) returns PA_ERR_WORKSPACE; nothing is
+ * allocated, on any path.  A call rejected for its arguments (any negative
+ * code but PA_ERR_CUDA) enqueues nothing; the argument checks run before any
+ * CUDA call.
  *
- * The first call on each device resolves the array's device address for
- * that device (cudaGetSymbolAddress); make that first call before any stream
- * capture.  Every call shares the one array: calls that can overlap on the
- * GPU (different streams without ordering between them) race on it and give
- * undefined results.  Device-detected input errors still leave the affected
- * rows zero; their status bits are cleared at the start of each call and
- * are not reported by this entry point. */
+ * The first call in each device context resolves the array's device address
+ * in that context (cudaGetSymbolAddress, with the device current); make that
+ * first call before any stream capture, and again after a device reset,
+ * which makes a new context.  Every call shares the one array: calls that
+ * can overlap on the GPU (different streams without ordering between them)
+ * race on it and give undefined results.  Each accepted call clears the
+ * array's status word on cuda_stream before its kernels; device-detected
+ * input errors still leave the affected rows zero, and their status bits are
+ * not reported by this entry point. */
 int pa_verify_forward_no_alloc(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_tables, const int32_t* past_lens,
                                const int32_t* subsequence_begins, int32_t max_context_len,
@@ -283,8 +287,6 @@ int pa_verify_forward_tree(const void* q, const void* k_cache, const void* v_cac
                            float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
                            void* workspace, size_t workspace_bytes, const uint8_t* tree_mask, void* cuda_stream);
 
-/* Synchronises cuda_stream, then reads and clears the workspace's status word
- * into *bits (PA_STATUS_* flags, 0 = clean). */
 /*
  * pa_forward_mixed — one call for a batch that mixes verify steps with
  * prefill chunks (the MIXED stage of the OpenVINO paged-attention op, issue
@@ -315,6 +317,8 @@ int pa_forward_mixed(const void* q, const void* k_cache, const void* v_cache, co
                      float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
                      void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* Synchronises cuda_stream, then reads and clears the workspace's status word
+ * into *bits (PA_STATUS_* flags, 0 = clean). */
 int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits);
 
 /* Static description of a PA_OK / PA_ERR_* code. */

@@ -1,7 +1,6 @@
 // Tensor-memory (tcgen05) partition kernels: head_dim 64 / 128, bf16 / f16 caches.
 #include "pa_launch.h"
 #include "pa_partition_tc.cuh"
-#include "pa_partition_tcu8.cuh"
 #include "pa_inst_tc.cuh"
 
 namespace pa {
@@ -13,21 +12,6 @@ cudaError_t launch_tc_t(const CUtensorMap& k, const CUtensorMap& v, const PartAr
   return a.tree_mask != nullptr ? launch_tc_tt<D, KV, true, false>(k, v, a, grid, st)
                                 : launch_tc_tt<D, KV, false, false>(k, v, a, grid, st);
 }
-cudaError_t launch_tcu8_128(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
-                            cudaStream_t st) {
-  auto kern = pa_partition_tcu8<128>;
-  const int smem = TcU8Cfg<128>::BYTES;
-  static int configured_for[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && !__atomic_load_n(&configured_for[dev], __ATOMIC_ACQUIRE)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
-  }
-  return launch_dependent(kern, grid, dim3(256), smem, st, k, v, a);
-}
 }  // namespace
 
 MmaKernelInfo tc_info(int D, int kv, bool* ok) {
@@ -36,7 +20,6 @@ MmaKernelInfo tc_info(int D, int kv, bool* ok) {
   if (D == 64 && kv == KV_F16) return MmaKernelInfo{TcCfg<64, KV_F16>::SK, TcCfg<64, KV_F16>::BYTES, 1};
   if (D == 128 && kv == KV_BF16) return MmaKernelInfo{TcCfg<128, KV_BF16>::SK, TcCfg<128, KV_BF16>::BYTES, 1};
   if (D == 128 && kv == KV_F16) return MmaKernelInfo{TcCfg<128, KV_F16>::SK, TcCfg<128, KV_F16>::BYTES, 1};
-  if (D == 128 && kv == KV_U8) return MmaKernelInfo{TcU8Cfg<128>::SK, TcU8Cfg<128>::BYTES, 1};
   *ok = false;
   return MmaKernelInfo{0, 0, 0};
 }
@@ -47,7 +30,6 @@ cudaError_t launch_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v,
   if (D == 64 && kv == KV_F16) return launch_tc_t<64, KV_F16>(k, v, a, grid, st);
   if (D == 128 && kv == KV_BF16) return launch_tc_t<128, KV_BF16>(k, v, a, grid, st);
   if (D == 128 && kv == KV_F16) return launch_tc_t<128, KV_F16>(k, v, a, grid, st);
-  if (D == 128 && kv == KV_U8) return launch_tcu8_128(k, v, a, grid, st);
   return cudaErrorInvalidValue;
 }
 

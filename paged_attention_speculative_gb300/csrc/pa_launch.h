@@ -50,7 +50,7 @@ cudaError_t launch_mma_d256(int kv, int nt, const CUtensorMap& k, const CUtensor
                             cudaStream_t st);
 
 // Tensor-memory (tcgen05) partition kernels: head_dim 64 / 128 with KV_BF16 /
-// KV_F16 caches, head_dim 128 with KV_U8 caches.
+// KV_F16 caches.
 MmaKernelInfo tc_info(int D, int kv, bool* ok);
 cudaError_t launch_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                       cudaStream_t st);
@@ -65,15 +65,10 @@ cudaError_t launch_tc_gather(int D, int kv, const PartArgs& a, dim3 grid, cudaSt
 cudaError_t launch_prefill_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a,
                               dim3 grid, cudaStream_t st);
 
-// Tensor-memory partition kernels with the keys on the MMA's M dimension:
-// head_dim 64 / 128, KV_BF16 / KV_F16 caches, row tiles n = 16 / 32 / 64.
-MmaKernelInfo tk_info(int D, int kv, int n, bool* ok);
-cudaError_t launch_tk(int D, int kv, int n, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
-                      cudaStream_t st);
-// The same for u8 caches, head_dim 128, row tiles n = 16 / 32 (stage_keys =
-// the u8 half stage, 64 keys).
-MmaKernelInfo tku8_info(int n, bool* ok);
-cudaError_t launch_tku8(int n, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
-                        cudaStream_t st);
+// u8 caches, head_dim 128, pages of 16 / 32 / 64 tokens, row tiles n = 16 /
+// 32: the keys-on-M tensor-memory kernel with converter warps; stage_keys =
+// 128.  Only the K cache needs a tensor map (64-byte swizzled records).
+MmaKernelInfo u8_info(int n, int ps, bool* ok);
+cudaError_t launch_u8(int n, int ps, const CUtensorMap& k, const PartArgs& a, dim3 grid, cudaStream_t st);
 
 }  // namespace pa

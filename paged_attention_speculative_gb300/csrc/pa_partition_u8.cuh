@@ -1,0 +1,656 @@
+// pa_partition_u8.cuh — split-KV partition kernel for u8 KV caches with a
+// per-token fp16 scale and zero-point (OpenVINO issue 38153, reproduction
+// step 1: "u8 KV cache precision"), head_dim 128, pages of 16, 32 or 64
+// tokens, up to 32 query rows per KV head, on the 5th-generation tensor cores
+// with the keys of a stage on the MMA's M dimension.
+//
+// Same contract as the other partition kernels: one CTA per (partition, KV
+// head, sequence); every page of the partition is read once for all T_b x G
+// query rows (the GQA read-once of issue 38153, "Cause"); per-token partials,
+// or the output when one partition covers the sequence.
+//
+// The issue's page reports the u8 path as the one whose cost grows fastest
+// with the number of query tokens: an ALU-bound dequantisation per element
+// and per query row.  Here each code is converted once per stage, whatever the
+// row count, by four converter warps that write f16 into tensor memory; the
+// per-token scale and zero-point are scalars of the softmax thread that owns
+// the key (value = (code - zp) * scale):
+//   S^T[k][n] = C'_k . q_n                C'_k = 1024 + K codes of key k (f16, exact)
+//   s[k][n]   = ks_k * (S^T[k][n] - (kz_k + 1024) * sum_d q_n)
+//   P'[k][n]  = f16(2^(s scale log2e - m_n) * vs_k)
+//   O^T[d][n] += sum_k Vc[k][d] P'[k][n]  Vc = V codes (f16, exact)
+//   out[n][d] = (O^T[d][n] - sum_k P'[k][n] vz_k) / sum_k 2^(...)
+// The +1024 of the K operand (a code's byte placed under the exponent of
+// 1024.0) is folded into the zero-point term, so a K code costs one byte
+// permute; the V codes are converted exactly because the value correction is
+// subtracted from the accumulated sum.  The correction uses the same rounded
+// P' that the tensor cores multiply.
+//
+// Per 128-key stage: the K and V records (codes, scales, zero-points) of the
+// stage's pages land in one shared-memory slot with one copy per record — a
+// TMA box with 64-byte swizzle for K (so the converters read key rows without
+// bank conflicts) and a 1-D bulk copy for V — under one mbarrier; a ring of
+// NS such slots keeps ~120 KB in flight per SM.
+//
+// Warp roles (512 threads, 16 warps; q = warp % 4 is the TMEM lane quarter a
+// warp may access, h = warp / 8 its half):
+//   warps 0-3, 8-11   softmax: thread = key 32q + lane of the stage (TMEM lane
+//                     of S^T), rows [h N/2, (h+1) N/2); head dim 32q + lane
+//                     of O^T in the epilogue; they also stage Q.  Thread 0
+//                     issues a stage's PV MMAs once all eight have written P'.
+//   warps 4-7, 12-15  converters: thread t = 32q + lane turns head dims
+//                     [64h, 64h + 64) of key t's K codes into f16 in TMEM (A
+//                     operand of S^T), gathers head dim t of keys [64h,
+//                     64h + 64) of the V codes into TMEM (A operand of O^T =
+//                     V^T P'^T), and writes key t's K (h = 0) or V (h = 1)
+//                     scale / zero-point terms (zero for keys out of range).
+//                     Warps 4 and 5 copy the K records and warp 6 the V
+//                     records of the stage NS ahead, one copy instruction
+//                     each, once all eight have converted a stage; thread
+//                     224 (warp 7) issues the stage's S^T MMAs.
+// The first NS stages' copies are issued right after the barriers exist,
+// while Q is staged and tensor memory allocated.
+#pragma once
+
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+
+template <int N, int PS>
+struct U8Cfg {
+  static_assert(N == 16 || N == 32, "row tile 16 / 32");
+  static_assert(PS == 16 || PS == 32 || PS == 64, "page size 16 / 32 / 64");
+  static constexpr int D = 128;
+  static constexpr int SK = 128;                       // keys per stage (M of the score MMA)
+  static constexpr int PPS = SK / PS;                  // pages per stage
+  static constexpr int REC = PS * (D + 4);             // one page-head record: codes, scales, zero-points
+  static constexpr int K_SLOT = (REC + 1023) / 1024 * 1024;  // swizzled K records start on 1024-byte boundaries
+  static constexpr int K_AREA = PPS * K_SLOT;
+  static constexpr int STAGE = (K_AREA + PPS * REC + 1023) / 1024 * 1024;
+  static constexpr int NB = 3;                         // converted stages in tensor memory
+  static constexpr int SIDE = SK * 16;                 // float4 per key: ks * scale * log2e, kz + 1024, vs, vz
+  static constexpr int Q_BYTES = N * D * 2;            // Q tile (f16), K-major: [chunk][row][128 B]
+  static constexpr int P_BYTES = SK * 128;             // P'^T tile (f16), MN-major: [key][64 row slots x 2 B]
+  static constexpr int MISC = 6656;
+  static constexpr int FIXED = NB * SIDE + Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + MISC + 1024;
+  static constexpr int NS_FIT = (226 * 1024 - FIXED) / STAGE;
+  static constexpr int NS = NS_FIT > 6 ? 6 : NS_FIT;   // stages in the ring
+  static constexpr int Q_OFF = NS * STAGE;
+  static constexpr int P_OFF = Q_OFF + Q_BYTES;
+  static constexpr int SIDE_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int BLK_OFF = SIDE_OFF + NB * SIDE;
+  static constexpr int MISC_OFF = BLK_OFF + 4 * kMaxPagesPerCta;
+  static constexpr int BYTES = MISC_OFF + MISC + 1024;
+  // TMEM columns: O^T [0, N), S^T [N, 3N), K codes [K_COL + 64 b, +64),
+  // V^T codes [V_COL + 64 b, +64) (two f16 per column)
+  static constexpr int K_COL = 128;
+  static constexpr int V_COL = K_COL + 64 * NB;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_S = tk_idesc(128, N, false, false, false);
+  static constexpr uint32_t IDESC_PV = tk_idesc(128, N, false, false, true);
+  static constexpr int NH = N / 2;                     // query rows per softmax thread
+  static_assert(3 * N <= K_COL, "tensor-memory budget");
+  static_assert(V_COL + 64 * NB <= TMEM_COLS, "tensor-memory budget");
+  static_assert(NS >= 3, "the ring needs a few stages");
+  static_assert(STAGE % 1024 == 0 && Q_OFF % 1024 == 0 && P_OFF % 1024 == 0, "swizzled tiles are 1024-aligned");
+  static_assert(REC % 16 == 0, "bulk copies move multiples of 16 bytes");
+  static_assert(BYTES <= 227 * 1024, "shared-memory budget");
+};
+
+// Byte offset, inside a 1024-aligned slot, of logical byte `o` of a record
+// copied with the 64-byte swizzle: the 16-byte unit index (bits 4-5) is XORed
+// with bits 7-8 of the offset.
+__device__ __forceinline__ uint32_t sw64(uint32_t o) { return o ^ (((o >> 7) & 3u) << 4); }
+
+template <int N, int PS>
+__global__ void __launch_bounds__(512, 1)
+    pa_partition_u8(const __grid_constant__ CUtensorMap tmK, const PartArgs a) {
+  using C = U8Cfg<N, PS>;
+  constexpr int D = C::D;
+  constexpr int NH = C::NH;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qt = smem + C::Q_OFF;
+  uint8_t* pt = smem + C::P_OFF;
+  float4* side_buf = reinterpret_cast<float4*>(smem + C::SIDE_OFF);   // [NB][SK]
+  int32_t* blk = reinterpret_cast<int32_t*>(smem + C::BLK_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::MISC_OFF);
+  uint64_t* full = bars;                 // [NS] stage landed (copies of warps 4, 5, 6)
+  uint64_t* empty = full + C::NS;        // [NS] stage converted (8 converter warps)
+  uint64_t* cfull = empty + C::NS;       // [NB] converted stage in TMEM (8 converter warps)
+  uint64_t* cfree = cfull + C::NB;       // [NB] converted stage consumed (MMA commit after PV)
+  uint64_t* s_full = cfree + C::NB;      // [2] S^T buffer written (MMA commit)
+  uint64_t* s_free = s_full + 2;         // [2] S^T buffer read (8 softmax warps)
+  uint64_t* p_full = s_free + 2;         // [2] P'^T buffer written (8 softmax warps)
+  uint64_t* pv_done = p_full + 2;        // [2] PV that read that P'^T buffer done (MMA commit)
+  float* m_sm = reinterpret_cast<float*>(smem + C::MISC_OFF + 512);   // [64] row reference maxima
+  float* xch = m_sm + 64;                                             // [8][64] per-warp row values
+  float* m_next = xch + 512;                                          // [64]
+  float* alpha_sm = m_next + 64;                                      // [64]
+  long long* rowoff = reinterpret_cast<long long*>(alpha_sm + 64);    // [64]
+  float* qsum_sm = reinterpret_cast<float*>(rowoff + 64);             // [64] sum_d of each f16 query row
+  float* xch2 = qsum_sm + 64;                                         // [8][64] second exchange
+  uint32_t* tree_rows = reinterpret_cast<uint32_t*>(xch2 + 512);      // [8] rows that see new token k
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_bad, s_timeout;
+
+  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q4 = warp & 3, hh = warp >> 3;                  // TMEM lane quarter, half
+  const bool soft = (warp & 4) == 0;                        // softmax warps 0-3, 8-11
+  const int st_id = hh * 128 + q4 * 32 + lane;              // index among the 256 threads of a role
+  pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
+  // Without a window a partition's first page is p * part_tokens / page_size
+  // whatever the sequence's length, so its block-table slice is fetched
+  // before the sequence's bounds are known.
+  const bool prefetch = (warp == 4 && a.window == 0);
+  if (prefetch) {
+    const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
+    const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
+                                       max(0LL, static_cast<long long>(a.max_blocks) - lpg)));
+    const int32_t* src = a.block_tables + static_cast<size_t>(b) * a.max_blocks + lpg;
+    for (int j = lane; j < n; j += 32) cp_async4(blk + j, src + j);
+  }
+  const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
+                              a.part_tokens, a.row_cap, a.role);
+  pdl_launch_dependents();
+  if (si.err || si.T <= 0 || p >= si.nparts) {
+    if (prefetch) cp_async_wait_all();  // no copy into shared memory outlives the CTA
+  }
+  if (si.err) {
+    if (p == 0 && threadIdx.x == 0) atomicOr(a.status, si.err);
+    if (p == 0 && si.rows_ok) {
+      const int n = si.T * a.G * D;
+      for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        store_out(a.out, a.out_dtype, (static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G) * D + d,
+                  0.f);
+      }
+    }
+    return;
+  }
+  if (si.T <= 0 || p >= si.nparts) return;
+
+  const int kstart = si.kbase + p * a.part_tokens;
+  const int kend = min(kstart + a.part_tokens, si.khi + 1);
+  const int lp0 = kstart / PS;
+  const int npages = (kend - 1) / PS - lp0 + 1;
+  const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
+  const int R = si.T * a.G;
+  const float sl2 = a.scale_log2;
+
+  if (threadIdx.x == 160) {
+    s_bad = 0;
+    s_timeout = 0;
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(&full[i], 3);
+      mbar_init(&empty[i], 8);
+    }
+    for (int i = 0; i < C::NB; ++i) {
+      mbar_init(&cfull[i], 8);
+      mbar_init(&cfree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 8);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&pv_done[i], 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // Stage s's copies, one copy instruction per warp (a copy instruction costs
+  // its warp hundreds of cycles, so each issuing warp issues one, with one
+  // lane per record): warps 4 / 5 the K records of the first / second half of
+  // the stage's pages (TMA boxes), warp 6 all V records (1-D bulk), each with
+  // its own expect-tx arrival.
+  auto issue_stage = [&](int s) {
+    const int cw = warp - 4;  // 0, 1, 2
+    const int slot = s % C::NS;
+    const int key0 = kstart + s * C::SK;
+    const int npg = (min(C::SK, kend - key0) + PS - 1) / PS;
+    uint8_t* st = smem + slot * C::STAGE;
+    constexpr int HALF = (C::PPS + 1) / 2;
+    const int i0 = cw == 1 ? HALF : 0;
+    const int i1 = cw == 0 ? min(npg, HALF) : npg;
+    const int mine = max(0, i1 - i0);
+    if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(mine * C::REC));
+    __syncwarp();
+    const int i = i0 + lane;
+    if (i < i1) {
+      const int lp = key0 / PS + i;
+      const int id = blk[lp - lp0];
+      if (cw < 2) {
+        tma_load_4d(st + i * C::K_SLOT, &tmK, 0, 0, g, id, &full[slot]);
+        if (a.trace != nullptr)
+          atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
+      } else {
+        bulk_load(st + C::K_AREA + i * C::REC,
+                  a.v_bytes + (static_cast<size_t>(id) * a.Hkv + g) * static_cast<size_t>(C::REC), C::REC,
+                  &full[slot]);
+      }
+    }
+    __syncwarp();
+  };
+
+  // ---- set-up: the first stages' copies start at once; meanwhile tensor
+  // memory is allocated and Q staged ----
+  if (warp >= 4 && warp < 8) {
+    if (warp == 4) {
+      // stage and validate the partition's block ids; a bad id is reported,
+      // clamped to page 0 (every copy stays in bounds) and the partition's
+      // result discarded
+      prefetch_tensormap(&tmK);
+      int bad = 0;
+      if (prefetch) {
+        cp_async_wait_all();
+        __syncwarp();
+      }
+      for (int j = lane; j < npages; j += 32) {
+        int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+        if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+          bad = 1;
+          id = 0;
+        }
+        blk[j] = id;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        s_bad = 1;
+        atomicOr(a.status, PA_STATUS_BLOCK_ID);
+      }
+    }
+    bar_sync_n(3, 128);  // the block ids are staged for warps 4-7
+    if (warp < 7)
+      for (int s = 0; s < min(C::NS, n_stages); ++s) issue_stage(s);
+  }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (soft) {
+    // Q rows -> f16, K-major swizzled tile (rows R..N-1 zero); then the sum of
+    // each f16 row, in head-dim order
+    for (int idx = st_id; idx < N * (D / 8); idx += 256) {
+      const int n = idx / (D / 8), u16 = idx % (D / 8);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (n < R) {
+        const size_t row = static_cast<size_t>(si.t0 + n / a.G) * a.Hq + g * a.G + n % a.G;
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + row * D) + u16);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = (a.q_dtype == PA_BF16) ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]))
+                                                  : __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          const __half2 hh2 = __floats2half2_rn(f.x, f.y);
+          h[e] = *reinterpret_cast<const uint32_t*>(&hh2);
+        }
+        v = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+      *reinterpret_cast<uint4*>(qt + ((u16 >> 3) * N + n) * 128 + swz(u16 & 7, n)) = v;
+    }
+    if (st_id < 64) m_sm[st_id] = -INFINITY;
+    fence_proxy_async();  // the Q tile is read by the tensor cores
+    bar_sync_n(1, 256);
+    if (st_id < N) {
+      const int n = st_id;
+      float sum = 0.f;
+      for (int u16 = 0; u16 < D / 8; ++u16) {
+        const uint4 x = *reinterpret_cast<const uint4*>(qt + ((u16 >> 3) * N + n) * 128 + swz(u16 & 7, n));
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          sum += f.x;
+          sum += f.y;
+        }
+      }
+      qsum_sm[n] = sum;
+    }
+    if (st_id >= 64 && st_id < 64 + PA_MAX_QUERY_LEN) {
+      // tree masks: the rows that see new token k (row n = token n / G)
+      const int k = st_id - 64;
+      uint32_t rows = 0;
+      if (a.tree_mask != nullptr)
+        for (int n = 0; n < R; ++n) rows |= ((ld_once_u8(a.tree_mask + si.t0 + n / a.G) >> k) & 1u) << n;
+      tree_rows[k] = rows;
+    }
+  }
+  // TMEM address, Q tile and row sums published to all warps
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t tm_o = tmem;            // O^T: lane = head dim, column = row
+  const uint32_t tm_s0 = tmem + N;       // S^T buffers: lane = key, column = row
+  const uint32_t tm_k = tmem + C::K_COL; // K codes + 1024: lane = key, two f16 per column
+  const uint32_t tm_v = tmem + C::V_COL; // V^T codes: lane = head dim, two keys per column
+  const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+  bool ok = true;
+
+  if (!soft) {
+    // =================== converters (+ copies, + S^T MMA issue) =============
+    const int ct = q4 * 32 + lane;                             // key (K) and head dim (V^T), 0..127
+    const int pi = ct / PS, kk = ct % PS;
+    const uint32_t k_row = static_cast<uint32_t>(pi * C::K_SLOT + kk * 128 + 64 * hh);  // this half of the row
+    const uint32_t sc = hh == 0 ? static_cast<uint32_t>(pi * C::K_SLOT + 128 * PS + 2 * kk)
+                                : static_cast<uint32_t>(C::K_AREA + pi * C::REC + 128 * PS + 2 * kk);
+    const uint32_t vsel = static_cast<uint32_t>((ct & 3) | ((4 + (ct & 3)) << 4));  // byte ct%4 of two words
+    const uint32_t vcol = static_cast<uint32_t>(ct & ~3);
+    const __half2 k1024 = __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    const uint32_t q_base = smem_u32(qt);
+    int issued = min(C::NS, n_stages);
+    for (int s = 0; s < n_stages && ok; ++s) {
+      const int cb = s % C::NB, slot = s % C::NS;
+      if (!mbar_wait(&full[slot], (s / C::NS) & 1) ||
+          (s >= C::NB && !mbar_wait(&cfree[cb], ((s / C::NB) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint8_t* st = smem + slot * C::STAGE;
+      {
+        // head dims [64h, 64h + 64) of key ct's K codes -> (1024 + code) as
+        // f16 pairs; column j of the half holds dims 64h + 2j, 64h + 2j + 1
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 x = *reinterpret_cast<const uint4*>(st + sw64(k_row + 16 * u));
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            w[8 * u + 2 * e] = __byte_perm(xs[e], 0x64646464u, 0x4140u);
+            w[8 * u + 2 * e + 1] = __byte_perm(xs[e], 0x64646464u, 0x4342u);
+          }
+        }
+        tmem_st32_nowait(tm_k + cb * 64 + 32 * hh + lane_off, w);
+      }
+      {
+        // key ct's dequantisation terms (K for h = 0, V for h = 1); zero
+        // outside every row's range and past the partition (there the scales
+        // may be garbage, even NaN)
+        const int key = kstart + s * C::SK + ct;
+        const bool in = key >= si.klo && key <= si.khi && key < kend;
+        const float sv = __half2float(*reinterpret_cast<const __half*>(st + (hh == 0 ? sw64(sc) : sc)));
+        const float zv = __half2float(*reinterpret_cast<const __half*>(st + (hh == 0 ? sw64(sc + 2 * PS) : sc + 2 * PS)));
+        float2 t = hh == 0 ? make_float2(sv * sl2, zv + 1024.f) : make_float2(sv, zv);
+        if (!in) t = make_float2(0.f, 0.f);
+        reinterpret_cast<float2*>(side_buf + cb * C::SK + ct)[hh] = t;
+      }
+      {
+        // V^T: head dim ct of keys [64h, 64h + 64) -> exact f16 codes, keys
+        // 64h + 2j, 64h + 2j + 1 in column j of the half
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int k0 = 64 * hh + 2 * j;
+          const uint32_t o = static_cast<uint32_t>(C::K_AREA + (k0 / PS) * C::REC + (k0 % PS) * 128) + vcol;
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(st + o);
+          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(st + o + 128);
+          uint32_t h = __byte_perm(__byte_perm(a0, a1, vsel), 0x64646464u, 0x4140u);
+          const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&h), k1024);
+          w[j] = *reinterpret_cast<const uint32_t*>(&c);
+        }
+        tmem_st32_nowait(tm_v + cb * 64 + 32 * hh + lane_off, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&cfull[cb]);
+        mbar_arrive(&empty[slot]);
+      }
+      if (threadIdx.x == 224) {
+        // S^T(s) = K(s) . Q^T once all eight warps have converted stage s and
+        // the softmax has read the S^T buffer two stages back
+        bool go = mbar_wait(&cfull[cb], (s / C::NB) & 1);
+        if (go && s >= 2) go = mbar_wait(&s_free[s & 1], ((s >> 1) - 1) & 1);
+        if (go) {
+          tc_fence_after();
+#pragma unroll
+          for (int kc = 0; kc < D / 16; ++kc) {
+            const uint64_t bd = sw128_desc(q_base + (kc >> 2) * N * 128 + 32 * (kc & 3), 16, 1024);
+            tc_mma_ta(tm_s0 + (s & 1) * N, tm_k + cb * 64 + 8 * kc, bd, C::IDESC_S, kc > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[s & 1]);
+        } else {
+          atomicOr(a.status, PA_STATUS_TIMEOUT);
+          atomicOr(&s_timeout, 1);
+        }
+      }
+      // refill this stage's slot with the stage NS ahead once all eight
+      // warps are done with it
+      if (issued < n_stages) {
+        if (warp >= 4 && warp < 7) {
+          if (!mbar_wait(&empty[slot], (s / C::NS) & 1)) {
+            ok = false;
+            break;
+          }
+          issue_stage(issued);
+        }
+        ++issued;
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(a.status, PA_STATUS_TIMEOUT);
+        atomicOr(&s_timeout, 1);
+      }
+      // let the copies in flight land before the CTA can retire
+      if (warp >= 4 && warp < 7)
+        for (int s = max(0, issued - C::NS); s < issued; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
+    }
+  }
+
+  // =========================== softmax warps (keys) ==========================
+  float l[NH], zc[NH];
+  if (soft) {
+    const int kq = q4 * 32 + lane;     // key of the stage
+    const int n0 = hh * NH;            // this thread's rows [n0, n0 + NH)
+#pragma unroll
+    for (int e = 0; e < NH; ++e) {
+      l[e] = 0.f;
+      zc[e] = 0.f;
+    }
+    const bool tree = a.tree_mask != nullptr;
+    for (int s = 0; s < n_stages; ++s) {
+      const int sb = s & 1, cb = s % C::NB;
+      if (ok) ok = mbar_wait(&s_full[sb], (s >> 1) & 1);
+      tc_fence_after();
+      float v[NH];
+      tmem_ld_small<NH>(tm_s0 + sb * N + n0 + lane_off, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      // this key's dequantisation terms (written by the converters before cfull)
+      if (ok) ok = mbar_wait(&cfull[cb], (s / C::NB) & 1);
+      const float4 sd = side_buf[cb * C::SK + kq];
+
+      const int key = kstart + s * C::SK + kq;
+      const int dk = key - si.L;
+      // rows that see this key, as a bit set: [nlo, nhi) (the causal limit
+      // and the window), or for a tree mask the window and the rows whose
+      // mask names this new token
+      const int nlo = (dk > 0 && !tree) ? dk * a.G : 0;
+      int nhi = R;
+      if (a.window > 0) nhi = min(R, max(0, (dk + a.window) * a.G));
+      if (key >= kend) nhi = 0;  // past the partition: the next partition's keys
+      const uint32_t below_hi = nhi >= 32 ? 0xffffffffu : ((1u << nhi) - 1u);
+      const uint32_t below_lo = nlo >= 32 ? 0xffffffffu : ((1u << nlo) - 1u);
+      uint32_t vrows = below_hi & ~below_lo;
+      if (tree && dk >= 0) vrows &= (dk < PA_MAX_QUERY_LEN) ? tree_rows[dk] : 0u;
+      const bool clean = (nlo == 0 && nhi >= R) && !(tree && dk >= 0);
+      bool need = false;
+#pragma unroll
+      for (int e4 = 0; e4 < NH; e4 += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(m_sm + n0 + e4);
+        const float4 qq = *reinterpret_cast<const float4*>(qsum_sm + n0 + e4);
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        const float qs[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x = fmaf(-sd.y, qs[e], v[e4 + e]) * sd.x;
+          if (!clean) x = ((vrows >> (n0 + e4 + e)) & 1u) ? x : -INFINITY;
+          v[e4 + e] = x;
+          need |= x > mm[e] + 8.f;
+        }
+      }
+      if (bar_any(1, 256, need)) {
+        const int xw = hh * 4 + q4;  // this warp's slot in the exchange
+#pragma unroll
+        for (int e = 0; e < NH; ++e) {
+          float t = v[e];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+          if (lane == 0) xch[xw * 64 + n0 + e] = t;
+        }
+        bar_sync_n(1, 256);
+        if (st_id < N) {
+          const int n = st_id, hn = n / NH;
+          const float rm = fmaxf(fmaxf(xch[(hn * 4) * 64 + n], xch[(hn * 4 + 1) * 64 + n]),
+                                 fmaxf(xch[(hn * 4 + 2) * 64 + n], xch[(hn * 4 + 3) * 64 + n]));
+          const float mo = m_sm[n];
+          const float mn = rm > mo + 8.f ? rm : mo;
+          m_next[n] = mn;
+          alpha_sm[n] = (mn == mo) ? 1.f : ex2(mo - mn);
+        }
+        bar_sync_n(1, 256);
+#pragma unroll
+        for (int e = 0; e < NH; ++e) {
+          l[e] *= alpha_sm[n0 + e];
+          zc[e] *= alpha_sm[n0 + e];
+        }
+        if (st_id < N) m_sm[st_id] = m_next[st_id];
+        if (s >= 1) {
+          // rescale this half's columns of O^T once the previous PV has landed
+          if (ok) ok = mbar_wait(&pv_done[(s - 1) & 1], ((s - 1) >> 1) & 1);
+          tc_fence_after();
+          float o[NH];
+          tmem_ld_small<NH>(tm_o + n0 + lane_off, o);
+#pragma unroll
+          for (int e = 0; e < NH; ++e) o[e] *= alpha_sm[n0 + e];
+          tmem_st_small<NH>(tm_o + n0 + lane_off, reinterpret_cast<const uint32_t*>(o));
+          tc_fence_before();
+        }
+        bar_sync_n(1, 256);
+      }
+      // weights times the key's V scale, rounded to f16 as the MMA reads them
+      // (8 rows = one 16-byte unit of this key's P'^T row at a time); the
+      // zero-point correction uses the rounded values.  The P'^T buffer is
+      // free once the PV two stages back has finished.
+      if (s >= 2 && ok) ok = mbar_wait(&pv_done[sb], ((s >> 1) - 1) & 1);
+      uint8_t* prow = pt + sb * C::P_BYTES + kq * 128;
+#pragma unroll
+      for (int u = 0; u < NH / 8; ++u) {
+        const float4 ma = *reinterpret_cast<const float4*>(m_sm + n0 + 8 * u);
+        const float4 mb = *reinterpret_cast<const float4*>(m_sm + n0 + 8 * u + 4);
+        const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int i = 8 * u + e;
+          const float mu0 = mm[e] == -INFINITY ? 0.f : mm[e];
+          const float mu1 = mm[e + 1] == -INFINITY ? 0.f : mm[e + 1];
+          const float p0 = ex2(v[i] - mu0), p1 = ex2(v[i + 1] - mu1);
+          l[i] += p0;
+          l[i + 1] += p1;
+          const __half2 h = __floats2half2_rn(p0 * sd.z, p1 * sd.z);
+          const float2 hr = __half22float2(h);
+          zc[i] = fmaf(hr.x, sd.w, zc[i]);
+          zc[i + 1] = fmaf(hr.y, sd.w, zc[i + 1]);
+          pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(prow + swz(n0 / 8 + u, kq)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+      if (threadIdx.x == 0) {
+        // O^T += V^T(s) . P'^T(s) once the eight softmax warps have written P'(s)
+        if (ok) ok = mbar_wait(&p_full[sb], (s >> 1) & 1);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t p_base = smem_u32(pt + sb * C::P_BYTES);
+#pragma unroll
+          for (int j = 0; j < C::SK / 16; ++j) {
+            const uint64_t bd = sw128_desc(p_base + j * 16 * 128, 0, 1024);
+            tc_mma_ta(tm_o, tm_v + cb * 64 + 8 * j, bd, C::IDESC_PV, (s > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(&pv_done[sb]);
+          tc_commit(&cfree[cb]);
+        }
+      }
+      __syncwarp();
+    }
+    if (ok && n_stages >= 1) ok = mbar_wait(&pv_done[(n_stages - 1) & 1], ((n_stages - 1) >> 1) & 1);
+    if (!ok && lane == 0) {
+      atomicOr(a.status, PA_STATUS_TIMEOUT);
+      atomicOr(&s_timeout, 1);
+    }
+  }
+  __syncthreads();  // every role is done; s_bad / s_timeout are final
+  if (soft) {
+    // ---- epilogue: row sums and corrections over all keys -> output ----
+    const int n0 = hh * NH;
+    const int xw = hh * 4 + q4;
+    const int dd = q4 * 32 + lane;  // head dim of this thread's O^T lane
+#pragma unroll
+    for (int e = 0; e < NH; ++e) {
+      float t = l[e], z = zc[e];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        t += __shfl_xor_sync(0xffffffffu, t, o);
+        z += __shfl_xor_sync(0xffffffffu, z, o);
+      }
+      if (lane == 0) {
+        xch[xw * 64 + n0 + e] = t;
+        xch2[xw * 64 + n0 + e] = z;
+      }
+    }
+    bar_sync_n(1, 256);
+    const bool poisoned = s_bad != 0 || s_timeout != 0;
+    float* linv = alpha_sm;
+    float* zrow = m_next;
+    if (st_id < R) {
+      const int n = st_id, hn = n / NH;
+      const float lt = (xch[(hn * 4) * 64 + n] + xch[(hn * 4 + 1) * 64 + n]) +
+                       (xch[(hn * 4 + 2) * 64 + n] + xch[(hn * 4 + 3) * 64 + n]);
+      zrow[n] = (xch2[(hn * 4) * 64 + n] + xch2[(hn * 4 + 1) * 64 + n]) +
+                (xch2[(hn * 4 + 2) * 64 + n] + xch2[(hn * 4 + 3) * 64 + n]);
+      const long long row = static_cast<long long>(si.t0 + n / a.G) * a.Hq + g * a.G + n % a.G;
+      if (si.nparts == 1) {
+        rowoff[n] = row * D;
+        linv[n] = (poisoned || !(lt > 0.f)) ? 0.f : 1.f / lt;
+      } else {
+        rowoff[n] = (prow(row, si, a.Hq) * a.num_parts + p) * D;
+        a.pm[prow(row, si, a.Hq) * a.num_parts + p] = m_sm[n];
+        a.pl[prow(row, si, a.Hq) * a.num_parts + p] = poisoned ? -1.f : lt;
+      }
+    }
+    bar_sync_n(1, 256);
+    tc_fence_after();
+    float o[NH];
+    tmem_ld_small<NH>(tm_o + n0 + lane_off, o);
+    if (si.nparts > 1) {
+#pragma unroll
+      for (int e = 0; e < NH; ++e)
+        if (n0 + e < R) a.po[rowoff[n0 + e] + dd] = o[e] - zrow[n0 + e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < NH; ++e)
+        if (n0 + e < R)
+          store_out(a.out, a.out_dtype, rowoff[n0 + e] + dd, (o[e] - zrow[n0 + e]) * linv[n0 + e]);
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace pa

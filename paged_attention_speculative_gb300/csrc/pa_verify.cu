@@ -44,16 +44,15 @@ long long round_up(long long a, long long q) { return ceil_div(a, q) * q; }
 
 int dtype_bytes(pa_dtype t) { return t == PA_F32 ? 4 : (t == PA_U8 ? 1 : 2); }
 
-// Optional override of the partition kernel for the 16-bit paths, read once:
-// "tc" forces the tensor-memory kernel wherever it applies, "mma" the
-// warp-level one; unset = chosen by row count.
+// Optional override of the partition kernel, read once: "tc" forces the
+// 16-bit rows-on-M tensor-memory kernel wherever it applies, "mma" the
+// warp-level one (16-bit and u8 caches); unset = chosen by shape.
 int env_kernel_choice() {
   static const int v = [] {
     const char* s = std::getenv("PA_VERIFY_KERNEL");
     if (s == nullptr) return 0;
     if (std::strcmp(s, "tc") == 0) return 2;
     if (std::strcmp(s, "mma") == 0) return 1;
-    if (std::strcmp(s, "tk") == 0) return 3;
     return 0;
   }();
   return v;
@@ -99,8 +98,7 @@ pa::MmaKernelInfo mma_info(int D, int kind, int nt, bool* ok) {
 }
 
 // Argument checks shared by every entry point; fills the plan.
-int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, int32_t num_sms, pa_plan* plan,
-              bool tree = false) {
+int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, int32_t num_sms, pa_plan* plan) {
   if (d == nullptr || plan == nullptr) return PA_ERR_NULL;
   std::memset(plan, 0, sizeof(*plan));
   if (d->num_seqs < 1 || d->num_seqs > 65535 || d->total_tokens < 0 || d->num_q_heads < 1 ||
@@ -141,32 +139,16 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   // 29.4 us on the warp-level kernel).  With head_dim 64 the warp-level
   // kernel stays ahead below 8 rows (10.8 vs 10.9 us).
   const bool tc16 = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128);
-  const bool tc_ok = (tc16 || (kv == PA_U8 && D == 128)) && rows <= 64;
-  // tree masks run on every kernel but the 16-bit keys-on-M one and the u8
-  // rows-on-M tensor-memory one: a forced choice of those falls back.  Small
-  // pages always take the rows-on-M tensor-memory kernel (16-bit caches).
-  const int choice = small_pages                                             ? 2
-                     : (tree && (env_kernel_choice() == 3 && kv != PA_U8)) ? 0
-                     : (tree && env_kernel_choice() == 2 && kv == PA_U8)   ? 0
-                                                                           : env_kernel_choice();
-  // u8 caches take the tensor-memory kernel only when forced (tuning).
-  // u8 caches with 17..32 query rows per KV head: the keys-on-M kernel's
-  // cost does not grow with the rows, while the warp-level kernel converts
-  // every chunk once per 8-row group (measured at T = 5..8, G = 4: 41 us vs
-  // 52-57 us at 32k keys).  Up to 16 rows the warp-level kernel is as fast.
-  //   The choice follows the rows of an average sequence and needs one wave
-  //   of (sequence, KV head) units: with many short units (large batches)
-  //   the warp-level kernel's two CTAs per SM win (measured: batch 64 x T=4,
-  //   4k keys: 223 us vs 323 us).
-  const long long avg_t = std::min<long long>(PA_MAX_QUERY_LEN, (std::max(d->total_tokens, 1) + d->num_seqs - 1) /
-                                                                     d->num_seqs);
-  const long long rows_avg = static_cast<long long>(G) * avg_t;
-  const bool one_wave = static_cast<long long>(d->num_seqs) * d->num_kv_heads <= num_sms;
-  if (kv == PA_U8 && D == 128 && rows <= 32 && choice != 1 &&
-      (choice == 3 || (rows_avg > 16 && one_wave))) {
+  // Small pages always take the rows-on-M tensor-memory kernel (16-bit caches).
+  const int choice = small_pages ? 2 : env_kernel_choice();
+  // u8 caches with head_dim 128, pages of 16 / 32 / 64 tokens and up to 32
+  // query rows per KV head take the u8 tensor-memory kernel: each code is
+  // converted once per stage whatever the row count, so its cost does not
+  // grow with the query tokens.  Other u8 shapes take the warp-level kernel.
+  if (kv == PA_U8 && D == 128 && rows <= 32 && (ps == 16 || ps == 32 || ps == 64) && choice != 1) {
     const int n = rows <= 16 ? 16 : 32;
     bool ok = false;
-    pa::MmaKernelInfo info = pa::tku8_info(n, &ok);
+    pa::MmaKernelInfo info = pa::u8_info(n, ps, &ok);
     if (ok) {
       kernel = 4;
       nt = n;
@@ -175,19 +157,7 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
       ctas_per_sm = info.ctas_per_sm;
     }
   }
-  if (tc16 && rows <= 64 && choice == 3) {
-    const int n = rows <= 16 ? 16 : (rows <= 32 ? 32 : 64);
-    bool ok = false;
-    pa::MmaKernelInfo info = pa::tk_info(D, mma_kind(kv), n, &ok);
-    if (ok) {
-      kernel = 3;
-      nt = n;
-      sk = info.stage_keys;
-      smem = info.smem_bytes;
-      ctas_per_sm = info.ctas_per_sm;
-    }
-  }
-  if (kernel == 0 && tc_ok && choice != 1 && ((tc16 && (rows >= 8 || D == 128)) || choice == 2)) {
+  if (kernel == 0 && tc16 && rows <= 64 && choice != 1 && (rows >= 8 || D == 128 || choice == 2)) {
     bool ok = false;
     pa::MmaKernelInfo info = pa::tc_info(D, mma_kind(kv), &ok);
     if (ok) {
@@ -341,6 +311,24 @@ int encode_cache_map(CUtensorMap* m, const void* base, pa_dtype kv, const pa_dim
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// TMA descriptor over a u8 cache's page-head records viewed as 64-byte rows:
+// dims {64, record / 64, Hkv, num_blocks}, one box = one whole record (codes,
+// scales, zero-points), 64-byte swizzle.
+int encode_u8_record_map(CUtensorMap* m, const void* base, const pa_dims* d) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PA_ERR_CUDA;
+  const cuuint64_t rec = static_cast<cuuint64_t>(d->page_size) * (d->head_dim + 4);
+  if (rec % 64 != 0 || rec / 64 > 256) return PA_ERR_UNSUPPORTED;
+  cuuint64_t dims[4] = {64, rec / 64, static_cast<cuuint64_t>(d->num_kv_heads), static_cast<cuuint64_t>(d->num_blocks)};
+  cuuint64_t strides[3] = {64, rec, rec * d->num_kv_heads};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(rec / 64), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 struct Call {
   const void* q;
   const void* k;
@@ -360,6 +348,7 @@ struct Call {
   int32_t* trace;
   const uint8_t* tree_mask = nullptr;  // optional (tree-mask verify)
   int role = pa::kRoleAll;             // which sequences the launches serve
+  bool clear_status = false;           // zero the status word on the stream just before the launches
 };
 
 PartArgs part_args(const Call& c, const pa_plan& plan, const Workspace& w) {
@@ -395,7 +384,7 @@ PartArgs part_args(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.box_log2 = ilog2(std::min(d->page_size, plan.stage_keys));
   a.row_cap = plan.kernel == 0   ? pa::kConsumerWarps * 8 * plan.row_tiles
               : plan.kernel == 2 ? 64
-              : (plan.kernel == 3 || plan.kernel == 4) ? plan.row_tiles
+              : plan.kernel == 4 ? plan.row_tiles
                                  : (1 << 30);
   a.q_dtype = d->q_dtype;
   a.out_dtype = d->out_dtype;
@@ -411,13 +400,11 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   const dim3 grid(plan.num_partitions, d->num_kv_heads, d->num_seqs);
 
   cudaError_t e;
-  if (plan.kernel == 3 || plan.kernel == 4) {
-    CUtensorMap mk, mv;
-    int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
-    if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
+  if (plan.kernel == 4) {
+    CUtensorMap mk;
+    const int rc = encode_u8_record_map(&mk, c.k, d);
     if (rc != PA_OK) return rc;
-    e = plan.kernel == 3 ? pa::launch_tk(d->head_dim, mma_kind(c.kv), plan.row_tiles, mk, mv, a, grid, c.stream)
-                         : pa::launch_tku8(plan.row_tiles, mk, mv, a, grid, c.stream);
+    e = pa::launch_u8(plan.row_tiles, d->page_size, mk, a, grid, c.stream);
   } else if (plan.kernel == 2 && d->page_size < pa::kGatherBelowPageSize) {
     e = pa::launch_tc_gather(d->head_dim, mma_kind(c.kv), a, grid, c.stream);
   } else if (plan.kernel == 2) {
@@ -466,7 +453,7 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.num_parts = plan.num_partitions;
   a.row_cap = plan.kernel == 0   ? pa::kConsumerWarps * 8 * plan.row_tiles
               : plan.kernel == 2 ? 64
-              : (plan.kernel == 3 || plan.kernel == 4) ? plan.row_tiles
+              : plan.kernel == 4 ? plan.row_tiles
                                  : (1 << 30);
   a.out_dtype = d->out_dtype;
   a.role = c.role;
@@ -488,10 +475,12 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-int check_pointers(const Call& c, bool need_tensors) {
-  if (c.begins == nullptr || c.past_lens == nullptr || c.out == nullptr || c.ws == nullptr) return PA_ERR_NULL;
+int check_pointers(const Call& c, bool need_tensors, bool need_workspace = true) {
+  if (c.begins == nullptr || c.past_lens == nullptr || c.out == nullptr) return PA_ERR_NULL;
+  if (need_workspace && c.ws == nullptr) return PA_ERR_NULL;
   if (need_tensors && (c.q == nullptr || c.k == nullptr || c.v == nullptr || c.bt == nullptr)) return PA_ERR_NULL;
-  if (!aligned(c.out, 16) || !aligned(c.ws, 16) || !aligned(c.begins, 4) || !aligned(c.past_lens, 4))
+  if (!aligned(c.out, 16) || (need_workspace && !aligned(c.ws, 16)) || !aligned(c.begins, 4) ||
+      !aligned(c.past_lens, 4))
     return PA_ERR_ALIGN;
   if (need_tensors && (!aligned(c.q, 16) || !aligned(c.k, 16) || !aligned(c.v, 16) || !aligned(c.bt, 4)))
     return PA_ERR_ALIGN;
@@ -503,17 +492,19 @@ int run(const Call& c, bool do_partition, bool do_combine) {
   if (c.d == nullptr) return PA_ERR_NULL;
   int sms = 0;
   pa_plan plan;
-  int rc = make_plan(c.d, c.max_ctx, c.window, c.kv, 1, &plan, c.tree_mask != nullptr);  // argument checks first
+  int rc = make_plan(c.d, c.max_ctx, c.window, c.kv, 1, &plan);  // argument checks first
   if (rc != PA_OK) return rc;
   rc = check_pointers(c, do_partition);
   if (rc != PA_OK) return rc;
   if (c.d->total_tokens == 0) return PA_OK;
   rc = device_sm_count(&sms);
   if (rc != PA_OK) return rc;
-  rc = make_plan(c.d, c.max_ctx, c.window, c.kv, sms, &plan, c.tree_mask != nullptr);
+  rc = make_plan(c.d, c.max_ctx, c.window, c.kv, sms, &plan);
   if (rc != PA_OK) return rc;
   if (c.ws_bytes < workspace_bytes_for(c.d, plan)) return PA_ERR_WORKSPACE;
   const Workspace w = carve(c.ws, c.d, plan);
+  // every check has passed: from here on the call enqueues work
+  if (c.clear_status && cudaMemsetAsync(w.status, 0, sizeof(uint32_t), c.stream) != cudaSuccess) return PA_ERR_CUDA;
   if (do_partition) {
     rc = launch_partition(c, plan, w);
     if (rc != PA_OK) return rc;
@@ -610,19 +601,49 @@ int run_mixed(Call c) {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_no_alloc_scratch on the current device, resolved once
-// per device with that device current.  In host code the array's name is
-// only a host-side stand-in; kernels must be given this address instead.
+// Device address of g_no_alloc_scratch in the current context.  In host code
+// the array's name is only a host-side stand-in; kernels must be given this
+// address.  It is resolved (cudaGetSymbolAddress, with the device current)
+// the first time a context calls, and cached per device together with the
+// context's unique id: a context made after a device reset (where the
+// library's module, and so the array, may sit elsewhere) resolves it again.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the calling thread's current context (0 if none or unknown).
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 int no_alloc_scratch(void** ptr) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static unsigned long long ctx_of[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (addr[dev] == nullptr || ctx == 0 || ctx != ctx_of[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
     addr[dev] = p;
+    ctx_of[dev] = current_context_id();  // the symbol lookup made the device's context current
   }
   *ptr = addr[dev];
   return PA_OK;
@@ -638,11 +659,8 @@ size_t pa_verify_workspace_size(const pa_dims* dims, int32_t max_context_len, in
   if (device_sm_count(&sms) != PA_OK) return 0;
   pa_plan plan;
   if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &plan) != PA_OK) return 0;
-  // one size for both entry points: a tree-mask call may run another kernel
-  // (and so another partition count) than the plain verify
-  pa_plan tree_plan;
-  if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &tree_plan, true) != PA_OK) return 0;
-  return std::max(workspace_bytes_for(dims, plan), workspace_bytes_for(dims, tree_plan));
+  // tree-mask calls run the same kernels with the same plan: one size serves both
+  return workspace_bytes_for(dims, plan);
 }
 
 size_t pa_mixed_workspace_size(const pa_dims* dims, int32_t max_context_len, int32_t sliding_window,
@@ -727,18 +745,25 @@ int pa_verify_forward_no_alloc(const void* q, const void* k_cache, const void* v
                                int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
                                void* cuda_stream) {
   if (dims == nullptr) return PA_ERR_NULL;
-  void* scratch = nullptr;
-  int rc = no_alloc_scratch(&scratch);
+  Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+         max_context_len, scale, sliding_window, kv_dtype, out, dims, nullptr, kNoAllocScratchBytes,
+         static_cast<cudaStream_t>(cuda_stream), nullptr};
+  // Host-only checks first, so that a rejected call makes no CUDA call and
+  // enqueues nothing.
+  pa_plan plan;
+  int rc = make_plan(dims, max_context_len, sliding_window, kv_dtype, 1, &plan);
   if (rc != PA_OK) return rc;
+  rc = check_pointers(c, true, false);
+  if (rc != PA_OK) return rc;
+  if (dims->total_tokens == 0) return PA_OK;
+  void* scratch = nullptr;
+  rc = no_alloc_scratch(&scratch);
+  if (rc != PA_OK) return rc;
+  c.ws = scratch;
   // The status word is the only part of the scratch that must start at zero
-  // (the partials are written before they are read).  Clear it on the stream
-  // so calls ordered on one stream see a clean word.
-  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  if (dims->total_tokens > 0 && cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st) != cudaSuccess)
-    return PA_ERR_CUDA;
-  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
-               max_context_len, scale, sliding_window, kv_dtype, out, dims, scratch, kNoAllocScratchBytes,
-               st, nullptr};
+  // (partials are written before they are read); run() clears it on the
+  // stream once the plan and the size check have passed.
+  c.clear_status = true;
   return run(c, true, true);  // PA_ERR_WORKSPACE when the call needs more than the scratch holds
 }
 

@@ -1,7 +1,9 @@
-"""Run in a child process with PA_VERIFY_KERNEL=tc (or tk): every case below
-that the forced kernel accepts goes through that tensor-memory partition
-kernel; prints one JSON line per case with the plan's kernel, the max abs
-error against the oracle and the gather-trace check."""
+"""Run in a child process with PA_VERIFY_KERNEL=tc (the 16-bit rows-on-M
+tensor-memory kernel wherever it applies), PA_VERIFY_KERNEL=mma (the
+warp-level kernel for 16-bit and u8 caches) or neither (the default choice,
+e.g. with a forced partition size): prints one JSON line per case with the
+plan's kernel, the max abs error against the oracle and the gather-trace
+check."""
 import json
 import os
 import sys
@@ -33,16 +35,15 @@ CASES = [
                         head_dim=128, page_size=64),
     lambda: W.qwen_u8(1, 1500, seed=79),
     lambda: W.qwen_u8(3, 2345, seed=80),
-    lambda: W.make_case("tcu8_rows64_f16q", seed=81, query_lens=[8], past_lens=[3100], num_q_heads=64, num_kv_heads=8,
+    lambda: W.make_case("u8_rows64_f16q", seed=81, query_lens=[8], past_lens=[3100], num_q_heads=64, num_kv_heads=8,
                         head_dim=128, page_size=16, kv_dtype="u8", q_dtype="f16"),
-    lambda: W.make_case("tcu8_window_ps32", seed=82, query_lens=[4, 2], past_lens=[1500, 700], num_q_heads=32,
+    lambda: W.make_case("u8_window_ps32", seed=82, query_lens=[4, 2], past_lens=[1500, 700], num_q_heads=32,
                         num_kv_heads=8, head_dim=128, page_size=32, kv_dtype="u8", sliding_window=500),
     lambda: W.make_case("tc_ps8_long", seed=77, query_lens=[7], past_lens=[9000], num_q_heads=64, num_kv_heads=8,
                         head_dim=128, page_size=8),
 ]
 
 if __name__ == "__main__":
-    assert os.environ.get("PA_VERIFY_KERNEL") in ("tc", "tk")
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for make in CASES:

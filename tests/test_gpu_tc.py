@@ -1,8 +1,9 @@
-"""The tensor-memory (tcgen05) partition kernels on every shape they accept:
-a child process forces one of them (PA_VERIFY_KERNEL=tc: rows on the MMA's
-M dimension; tk: keys on M) for 1..64 query rows per KV head, head_dim 64 /
-128, bf16 / f16 and u8 caches, windows and ragged tails, and each case is
-compared with the fp64 oracle (<= 2e-3) and its gather trace bit-exactly."""
+"""Each partition kernel on shapes the default choice would send elsewhere: a
+child process forces one (PA_VERIFY_KERNEL=tc: the 16-bit rows-on-M
+tensor-memory kernel; mma: the warp-level kernel, 16-bit and u8) for 1..64
+query rows per KV head, head_dim 64 / 128, bf16 / f16 and u8 caches, windows
+and ragged tails, and each case is compared with the fp64 oracle (<= 2e-3)
+and its gather trace bit-exactly."""
 import json
 import os
 import subprocess
@@ -16,7 +17,7 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("kernel", ["tc", "tk"])
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
 def test_forced_tensor_memory_path_matches_oracle(kernel):
     env = dict(os.environ, PA_VERIFY_KERNEL=kernel)
     proc = subprocess.run([sys.executable, os.path.join(HERE, "tc_forced_cases.py")], env=env,
@@ -33,11 +34,13 @@ def test_forced_tensor_memory_path_matches_oracle(kernel):
             assert r["excess"] <= 0.0, r
 
 
-def test_forced_partitions_of_odd_half_stages():
-    """704-key partitions: the u8 keys-on-M kernel's 128-key stages end
-    half filled inside a partition (its keys past the partition's end belong
-    to the next one and must not count); every forced case must still match."""
-    env = dict(os.environ, PA_VERIFY_KERNEL="tk", PA_VERIFY_PART_TOKENS="704")
+def test_small_forced_partitions():
+    """384-key partitions (three 128-key stages of the u8 kernel, six 64-key
+    stages of the 16-bit one): many partitions per sequence, partition ends
+    inside pages of 32 and 64 tokens' neighbours; every case must still
+    match, and the u8 tensor-memory kernel must be among the kernels run."""
+    env = dict(os.environ, PA_VERIFY_PART_TOKENS="384")
+    env.pop("PA_VERIFY_KERNEL", None)
     proc = subprocess.run([sys.executable, os.path.join(HERE, "tc_forced_cases.py")], env=env,
                           capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stderr[-3000:]

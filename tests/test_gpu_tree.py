@@ -35,8 +35,10 @@ CASES = [
     (lambda: W.long_ctx_b(3000, seed=103), 2, False),
     (lambda: W.make_case("tree_batch_win", seed=104, query_lens=[5, 0, 8, 3], past_lens=[900, 10, 1300, 40],
                          num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, sliding_window=400), 2, True),
-    (lambda: W.qwen_u8(6, 2200, seed=105), 4, False),   # 24 u8 rows: the u8 keys-on-M kernel
-    (lambda: W.qwen_u8(3, 2200, seed=108), 0, False),
+    (lambda: W.qwen_u8(6, 2200, seed=105), 4, False),   # 24 u8 rows: the u8 tensor-memory kernel (N = 32)
+    (lambda: W.qwen_u8(3, 2200, seed=108), 4, False),   # 12 u8 rows: the same kernel with N = 16
+    (lambda: W.make_case("tree_u8_rows64", seed=109, query_lens=[8], past_lens=[1800], num_q_heads=64,
+                         num_kv_heads=8, head_dim=128, page_size=16, kv_dtype="u8"), 0, False),  # warp-level u8
     (lambda: W.make_case("tree_d256", seed=106, query_lens=[4, 6], past_lens=[1500, 700], num_q_heads=32,
                          num_kv_heads=16, head_dim=256, page_size=64), 0, False),
     (lambda: W.tiny(seed=107), 1, True),

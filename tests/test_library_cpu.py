@@ -160,6 +160,25 @@ def test_forward_host_errors_need_no_gpu(lib):
     assert lib.pa_verify_forward(*bad) == -1
 
 
+def test_no_alloc_rejections_come_before_any_cuda_call(lib):
+    """pa_verify_forward_no_alloc checks its arguments before it resolves its
+    scratch or enqueues anything: on a machine without a GPU, where any CUDA
+    call fails (PA_ERR_CUDA), a bad argument still returns its own code."""
+    a16 = ctypes.c_void_p(4096)
+    z = ctypes.c_void_p(0)
+
+    def call(d, kv=pa.PA_BF16, q=a16, out=a16, mcl=4096):
+        return lib.pa_verify_forward_no_alloc(q, a16, a16, a16, a16, a16, mcl, 0.1, 0, kv, out, ctypes.byref(d), z)
+    assert call(dims(head_dim=96)) == -4
+    assert call(dims(q_dtype=pa.PA_F16)) == -2
+    assert call(dims(), q=z) == -1
+    assert call(dims(), out=ctypes.c_void_p(4100)) == -6
+    assert call(dims(), mcl=0) == -8
+    assert lib.pa_verify_forward_no_alloc(a16, a16, a16, a16, a16, a16, 4096, 0.1, 0, pa.PA_BF16, a16, None, z) == -1
+    # an empty batch is accepted without touching the device
+    assert call(dims(total_tokens=0)) == 0
+
+
 def test_mixed_host_errors_need_no_gpu(lib):
     """pa_forward_mixed rejects what its prefill kernels do not serve before
     touching the device: u8 caches, head_dim 256 with 16-bit caches, 16-bit
