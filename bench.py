@@ -93,7 +93,7 @@ class DeviceWorkload:
         self.q = torch.randn((self.T_total, Hq, D), generator=gd, device="cuda").to(qdt)
         if kv == "u8":
             self.k = self._u8_pool(nb, gd)
-            self.v = self._u8_pool(nb, gd)
+            self.v = self._u8_pool(nb, gd, dim_major=True)  # V records hold their codes dim-major
         else:
             dt = torch.bfloat16 if kv == "bf16" else torch.float16
             self.k = torch.randn((nb, Hkv, ps, D), generator=gd, device="cuda").to(dt)
@@ -129,7 +129,7 @@ class DeviceWorkload:
         slot_bytes = D + 4 if kv == "u8" else D * eb
         self.update_bytes = 2 * self.T_total * Hkv * (D * 2 + slot_bytes)
 
-    def _u8_pool(self, nb, gd):
+    def _u8_pool(self, nb, gd, dim_major=False):
         import torch
         x = torch.randn((nb, self.Hkv, self.ps, self.D), generator=gd, device="cuda")
         mn = x.amin(dim=-1)
@@ -141,7 +141,8 @@ class DeviceWorkload:
         codes = torch.clamp(torch.round(x / s[..., None] + zp[..., None]), 0, 255).to(torch.uint8)
         ps, D = self.ps, self.D
         rec = torch.empty((nb, self.Hkv, ps * (D + 4)), dtype=torch.uint8, device="cuda")
-        rec[:, :, : ps * D] = codes.reshape(nb, self.Hkv, ps * D)
+        c = codes.transpose(2, 3) if dim_major else codes
+        rec[:, :, : ps * D] = c.contiguous().reshape(nb, self.Hkv, ps * D)
         rec[:, :, ps * D: ps * D + 2 * ps] = scale.contiguous().view(torch.uint8).reshape(nb, self.Hkv, 2 * ps)
         rec[:, :, ps * D + 2 * ps:] = zp.half().contiguous().view(torch.uint8).reshape(nb, self.Hkv, 2 * ps)
         return rec

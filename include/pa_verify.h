@@ -66,8 +66,9 @@ enum {
   PA_ERR_PAGE_SIZE = -5,   /* page_size not a power of two in [1, 256]; pages of
                               1, 2 or 4 tokens need an fp32 cache, or a 16-bit
                               cache with head_dim <= 128 and <= 64 query rows
-                              per KV head (pa_cache_update: any power of two
-                              up to 256)                                      */
+                              per KV head; u8 caches need pages of 16 tokens
+                              or more (pa_cache_update: any power of two up
+                              to 256)                                         */
   PA_ERR_ALIGN = -6,       /* a pointer misses its alignment                      */
   PA_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than pa_verify_workspace_size */
   PA_ERR_CONTEXT = -8,     /* max_context_len < 1 while tokens are present, or too large */
@@ -107,14 +108,13 @@ typedef struct {
   int32_t part_tokens;     /* keys per partition (multiple of the stage size)     */
   int32_t stage_keys;      /* keys staged per pipeline step                       */
   int32_t row_tiles;       /* kernel 0: n-tiles of 8 query rows per warp (1 or 2);
-                              kernel 3: query-row tile N (16, 32 or 64)           */
+                              kernel 4: query-row tile N (16 or 32)               */
   int32_t kernel;          /* 0 = warp-level mma path (16-bit / u8 KV), 1 = fp32 path,
                               2 = tensor-memory (tcgen05) path, query rows on the MMA's
-                              M dimension (16-bit KV with D <= 128, or u8 KV with
-                              D = 128; 8..64 query rows per KV head),
-                              3 = tensor-memory path, keys on the MMA's M dimension
-                              (16-bit KV with D <= 128, up to 64 query rows),
-                              4 = the same for u8 KV (D = 128, up to 32 rows).
+                              M dimension (16-bit KV with D <= 128; 8..64 query
+                              rows per KV head), 4 = tensor-memory path for u8 KV,
+                              keys on the MMA's M dimension (D = 128, pages of
+                              16 / 32 / 64 tokens, up to 32 query rows).
                               Pages of 1, 2 or 4 tokens with 16-bit KV always
                               take kernel 2, gathering key rows with 16-byte
                               cp.async copies instead of TMA boxes            */
@@ -130,8 +130,11 @@ typedef struct {
  *  float / 16-bit caches: [num_blocks, Hkv, ps, D] in kv_dtype — one page of
  *       one KV head is a contiguous [ps, D] tile.
  *  u8 caches: [num_blocks, Hkv, ps*(D+4)] bytes — per page per KV head one
- *       record: ps*D code bytes (slot-major), then ps fp16 scales, then ps
- *       fp16 zero-points; value = (code - zero_point) * scale.
+ *       record: ps*D code bytes, then ps fp16 scales, then ps fp16
+ *       zero-points; value = (code - zero_point) * scale.  K records hold their
+ *       codes slot-major (code of slot j, element d at j*D + d); V records
+ *       dim-major (at d*ps + j), so that one head dimension of a page's
+ *       tokens is contiguous for the P.V product.
  *  block_tables [B, max_blocks_per_seq] int32: logical page j/ps of sequence b
  *       lives in physical page block_tables[b][j/ps].
  *  past_lens [B] int32, subsequence_begins [B+1] int32 (device memory).

@@ -56,8 +56,10 @@
  *  - q   [total_tokens, Hq, D] in q_dtype (0 f32, 1 f16, 2 bf16).
  *  - float KV cache  [num_blocks, Hkv, ps, D] in kv_dtype (0, 1 or 2).
  *  - u8 KV cache (kv_dtype 3): per (block, KV head) one record of
- *    ps*D bytes of codes (slot-major), then ps fp16 scales, then ps fp16
- *    zero-points; records are ps*(D+4) bytes, [num_blocks, Hkv, record].
+ *    ps*D bytes of codes, then ps fp16 scales, then ps fp16 zero-points;
+ *    records are ps*(D+4) bytes, [num_blocks, Hkv, record].  K records hold
+ *    their codes slot-major (code of slot j, element d at j*D + d), V
+ *    records dim-major (at d*ps + j).
  *  - block_tables [num_seqs, max_blocks_per_seq] int32 physical block ids.
  *
  * Every stored value is converted exactly to double; all arithmetic is fp64.
@@ -108,16 +110,17 @@ static double load_float(const void* base, int dtype, size_t idx) {
 }
 
 /* The dequantised value of element d of slot `slot` of KV head g in physical
- * block `blk` (OpenVINO issue 38153, reproduction step 1: u8 KV cache). */
+ * block `blk` (OpenVINO issue 38153, reproduction step 1: u8 KV cache).
+ * dim_major: the u8 record keeps its codes dim-major (the V cache). */
 static double cache_value(const void* cache, int kv_dtype, int Hkv, int ps, int D,
-                          int blk, int g, int slot, int d) {
+                          int blk, int g, int slot, int d, int dim_major) {
   if (kv_dtype != OR_U8) {
     size_t idx = (((size_t)blk * Hkv + g) * ps + slot) * (size_t)D + d;
     return load_float(cache, kv_dtype, idx);
   }
   size_t rec_bytes = (size_t)ps * (D + 4);
   const unsigned char* rec = (const unsigned char*)cache + ((size_t)blk * Hkv + g) * rec_bytes;
-  double code = (double)rec[(size_t)slot * D + d];
+  double code = (double)rec[dim_major ? (size_t)d * ps + slot : (size_t)slot * D + d];
   uint16_t s16, z16;
   memcpy(&s16, rec + (size_t)ps * D + 2 * (size_t)slot, 2);
   memcpy(&z16, rec + (size_t)ps * D + 2 * (size_t)ps + 2 * (size_t)slot, 2);
@@ -204,7 +207,7 @@ int pa_oracle_forward_tree(const void* q, int q_dtype, const void* k_cache, cons
       double acc = 0.0;
       for (int d = 0; d < D; ++d)
         acc += load_float(q, q_dtype, qoff + d) *
-               cache_value(k_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d);
+               cache_value(k_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d, 0);
       s[j - lo] = scale * acc;
       if (s[j - lo] > smax) smax = s[j - lo];
       seen = 1;
@@ -223,7 +226,7 @@ int pa_oracle_forward_tree(const void* q, int q_dtype, const void* k_cache, cons
         denom += w;
         const int blk = block_tables[(size_t)b * max_blocks_per_seq + j / ps];
         for (int d = 0; d < D; ++d)
-          o[d] += w * cache_value(v_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d);
+          o[d] += w * cache_value(v_cache, kv_dtype, Hkv, ps, D, blk, g, (int)(j % ps), d, 1);
       }
       for (int d = 0; d < D; ++d) o[d] /= denom;
     }
@@ -342,8 +345,9 @@ static void store_float(void* base, int dtype, size_t idx, float v) {
   }
 }
 
-/* One token's D values of one KV head into slot `slot` of record `rec`. */
-static void quantize_u8_slot(const float* x, int D, int ps, int slot, unsigned char* rec) {
+/* One token's D values of one KV head into slot `slot` of record `rec`
+ * (codes slot-major, or dim-major for the V cache). */
+static void quantize_u8_slot(const float* x, int D, int ps, int slot, unsigned char* rec, int dim_major) {
   float mn = x[0], mx = x[0];
   for (int d = 1; d < D; ++d) {
     if (x[d] < mn) mn = x[d];
@@ -366,7 +370,7 @@ static void quantize_u8_slot(const float* x, int D, int ps, int slot, unsigned c
     float c = rintf(u);
     if (!(c >= 0.0f)) c = 0.0f; /* also NaN */
     if (c > 255.0f) c = 255.0f;
-    rec[(size_t)slot * D + d] = (unsigned char)c;
+    rec[dim_major ? (size_t)d * ps + slot : (size_t)slot * D + d] = (unsigned char)c;
   }
   memcpy(rec + (size_t)ps * D + 2 * (size_t)slot, &s16, 2);
   memcpy(rec + (size_t)ps * D + 2 * (size_t)ps + 2 * (size_t)slot, &z16, 2);
@@ -414,7 +418,7 @@ int pa_oracle_cache_update(const void* k_new, const void* v_new, int src_dtype, 
           } else {
             for (int d = 0; d < D; ++d) x[d] = load_src(src, src_dtype, sbase + d);
             unsigned char* rec = (unsigned char*)cache + ((size_t)blk * Hkv + g) * (size_t)ps * (D + 4);
-            quantize_u8_slot(x, D, ps, slot, rec);
+            quantize_u8_slot(x, D, ps, slot, rec, which);
           }
         }
       }

@@ -163,9 +163,17 @@ __global__ void __launch_bounds__(128) pa_cache_update_kernel(const CacheArgs a)
     else packed[e / 4] |= b << (8 * (e % 4));
   }
   uint8_t* rec = reinterpret_cast<uint8_t*>(cache) + (static_cast<size_t>(blk) * a.Hkv + g) * a.ps * (D + 4);
-  uint32_t* codes = reinterpret_cast<uint32_t*>(rec + static_cast<size_t>(slot) * D + lane * E);
+  if (!is_v) {
+    // K records: codes slot-major, the token's D codes contiguous
+    uint32_t* codes = reinterpret_cast<uint32_t*>(rec + static_cast<size_t>(slot) * D + lane * E);
 #pragma unroll
-  for (int w = 0; w < E / 4; ++w) codes[w] = packed[w];
+    for (int w = 0; w < E / 4; ++w) codes[w] = packed[w];
+  } else {
+    // V records: codes dim-major, code of head dim d at d * ps + slot
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      rec[static_cast<size_t>(lane * E + e) * a.ps + slot] = static_cast<uint8_t>(packed[e / 4] >> (8 * (e % 4)));
+  }
   if (lane == 0) {
     *reinterpret_cast<__half*>(rec + static_cast<size_t>(a.ps) * D + 2 * slot) = s16;
     *reinterpret_cast<__half*>(rec + static_cast<size_t>(a.ps) * D + 2 * a.ps + 2 * slot) = z16;

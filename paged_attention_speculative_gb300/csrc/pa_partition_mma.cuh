@@ -24,7 +24,10 @@
 // u8 caches: codes are exact in f16 (code = f16(0x6400 | code) - 1024), so
 // q.K = scale_j (q.code_j - zp_j sum(q)) and the value sum is
 // sum_j p_j scale_j code_j - sum_j p_j scale_j zp_j — the dequantisation costs
-// one FMA per key, not per element.
+// one FMA per key, not per element.  u8 V pages hold their codes dim-major, so
+// a stage segment of V arrives as a [head dim][key] tile (one TMA box) whose
+// rows are the A operand of O^T = V^T . P^T as they are; u8 keys are taken in
+// their natural order within a 16-key chunk.
 #pragma once
 
 #include "pa_device.cuh"
@@ -68,8 +71,7 @@ struct MmaSmem {
 // Physical head-dim index of mma row m of m-tile mt in the O^T accumulator.
 template <int D, bool kU8>
 __device__ __forceinline__ int out_dim(int mt, int m) {
-  if constexpr (kU8) return (D / 8) * (m & 7) + 2 * mt + (m >> 3);
-  else return 16 * mt + m;
+  return 16 * mt + m;
 }
 
 template <int D, int KV, int NT, bool TREE = false>
@@ -190,10 +192,19 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
       // one copy per lane: a copy instruction costs its thread hundreds of
       // cycles, so copies issued by one lane in a row would pace the stream
       const int nt = nseg * C::CHUNKS;
-      int ncopy = 2 * nt;
+      // K: CHUNKS boxes per segment; V: the same, or for u8 one dim-major
+      // [head dim][key] box per segment
+      const int nv = C::kU8 ? nseg : nt;
+      int ncopy = nt + nv;
       if constexpr (C::kU8) ncopy += nseg * (br == a.ps ? 2 : 4);
       for (int c = lane; c < ncopy; c += 32) {
-        if (c < 2 * nt) {
+        if (C::kU8 && c >= nt && c < nt + nv) {
+          const int seg = c - nt;
+          const int key = key0 + (seg << br_log2);
+          const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+          const int id = blk[lp - lp0];
+          tma_load_4d(st + C::TILE + seg * (D << br_log2), &tmV, slot0, 0, g, id, &full[slot]);
+        } else if (c < (C::kU8 ? nt : 2 * nt)) {
           const bool is_v = c >= nt;
           const int j = is_v ? c - nt : c;
           const int seg = j / C::CHUNKS, ch = j % C::CHUNKS;
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
           // when the segment is a whole page (the record keeps both arrays
           // adjacent), else scales and zero-points separately
           const size_t rec = static_cast<size_t>(a.ps) * (D + 4);
-          const int idx = c - 2 * nt;
+          const int idx = c - nt - nv;
           const bool whole = (br == a.ps);
           const int seg = whole ? idx >> 1 : idx >> 2;
           const bool is_v = whole ? (idx & 1) != 0 : (idx & 2) != 0;
@@ -348,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
       for (int c = c0; c < C::CHUNKS_PER_STAGE; c += KS) {
         const int ck0 = key0 + 16 * c;
         if (ck0 >= kend) break;
-        const int kg0 = ck0 + key_perm(g8);  // keys of accumulator rows g8 and g8 + 8
+        const int kg0 = ck0 + (C::kU8 ? g8 : key_perm(g8));  // keys of accumulator rows g8 and g8 + 8
         const int kg1 = kg0 + 8;
 
         // ---------------- S^T = K . Q^T ----------------
@@ -377,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
           uint4 kw[2][C::CHUNKS][2];
 #pragma unroll
           for (int kh = 0; kh < 2; ++kh) {
-            const int kk = 16 * c + key_perm(g8 + 8 * kh);
+            const int kk = 16 * c + g8 + 8 * kh;
 #pragma unroll
             for (int dc = 0; dc < C::CHUNKS; ++dc)
 #pragma unroll
@@ -469,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
           float vsc[2], vzp[2];
 #pragma unroll
           for (int kh = 0; kh < 2; ++kh) {
-            const int kk = 16 * c + key_perm(g8 + 8 * kh);
+            const int kk = 16 * c + g8 + 8 * kh;
             const int key = kk + key0;
             const bool in_union = key >= si.klo && key <= si.khi;
             const __half* scp = reinterpret_cast<const __half*>(st + 2 * C::TILE + 4 * C::SK +
@@ -520,37 +531,31 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
               if (nt < nt_active) mma16816<kBf>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
           }
         } else {
-          // thread (g8, tig) needs keys k-slots 2tig, 2tig+1, 2tig+8, 2tig+9 at
-          // head-dim range [(D/8) g8, (D/8)(g8+1)) — one or two 16-byte units.
-          constexpr int VW = C::CHUNKS;  // uint4 words per key
-          uint4 vw[4][VW];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int slotk = 2 * tig + (q4 & 1) + 8 * (q4 >> 1);
-            const int kk = 16 * c + key_perm(slotk);
-#pragma unroll
-            for (int w = 0; w < VW; ++w) {
-              const int unit = (VW == 1) ? g8 : ((2 * g8 + w) & 7);
-              const int dc = (VW == 1) ? 0 : (g8 >> 2);
-              vw[q4][w] = *reinterpret_cast<const uint4*>(st + C::TILE + tile_row_off(kk, dc, a.box_log2, C::CHUNKS) +
-                                                          swz(unit, kk));
-            }
-          }
+          // A = V^T (16 head dims x 16 keys) straight from the dim-major
+          // tile [segment][head dim][key]: thread (g8, tig) takes keys
+          // 2tig, 2tig+1 (and + 8) of head dims 16mt + g8 (and + 8), two
+          // adjacent codes per 16-bit load
+          const int brl = a.box_log2;
+          const uint8_t* vt8 = st + C::TILE;
+          const int k0 = 16 * c + 2 * tig, k1 = k0 + 8;
+          const int off0 = ((k0 >> brl) * D) << brl | (k0 & ((1 << brl) - 1));
+          const int off1 = ((k1 >> brl) * D) << brl | (k1 & ((1 << brl) - 1));
+          const __half2 k1024 = __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
 #pragma unroll
           for (int mt = 0; mt < C::MTILES; ++mt) {
-            const int wi = mt >> 1;
-            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-            const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vw[0][wi >> 2])[wi & 3];
-            const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vw[1][wi >> 2])[wi & 3];
-            const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vw[2][wi >> 2])[wi & 3];
-            const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vw[3][wi >> 2])[wi & 3];
-            const uint32_t t01 = __byte_perm(w0, w1, sel);
-            const uint32_t t23 = __byte_perm(w2, w3, sel);
+            const int d0 = 16 * mt + g8;
             uint32_t af[4];
-            af[0] = u8pair_to_f16x2(t01, 0x4140u);
-            af[1] = u8pair_to_f16x2(t01, 0x4342u);
-            af[2] = u8pair_to_f16x2(t23, 0x4140u);
-            af[3] = u8pair_to_f16x2(t23, 0x4342u);
+            const uint32_t c00 = *reinterpret_cast<const uint16_t*>(vt8 + off0 + (d0 << brl));
+            const uint32_t c10 = *reinterpret_cast<const uint16_t*>(vt8 + off0 + ((d0 + 8) << brl));
+            const uint32_t c01 = *reinterpret_cast<const uint16_t*>(vt8 + off1 + (d0 << brl));
+            const uint32_t c11 = *reinterpret_cast<const uint16_t*>(vt8 + off1 + ((d0 + 8) << brl));
+            const uint32_t w[4] = {c00, c10, c01, c11};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t h = __byte_perm(w[i], 0x64646464u, 0x4140u);
+              const __half2 cv = __hsub2(*reinterpret_cast<const __half2*>(&h), k1024);
+              af[i] = *reinterpret_cast<const uint32_t*>(&cv);
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               if (nt < nt_active) mma16816<false>(o[mt][nt], af, pb[nt][0], pb[nt][1]);

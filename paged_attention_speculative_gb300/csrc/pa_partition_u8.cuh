@@ -32,24 +32,29 @@
 // bank conflicts) and a 1-D bulk copy for V — under one mbarrier; a ring of
 // NS such slots keeps ~120 KB in flight per SM.
 //
-// Warp roles (512 threads, 16 warps; q = warp % 4 is the TMEM lane quarter a
-// warp may access, h = warp / 8 its half):
+// Warp roles (608 threads, 19 warps; for warps 0-15, q = warp % 4 is the
+// TMEM lane quarter a warp may access and h = warp / 8 its half):
 //   warps 0-3, 8-11   softmax: thread = key 32q + lane of the stage (TMEM lane
 //                     of S^T), rows [h N/2, (h+1) N/2); head dim 32q + lane
-//                     of O^T in the epilogue; they also stage Q.  Thread 0
-//                     issues a stage's PV MMAs once all eight have written P'.
+//                     of O^T in the epilogue; they also stage Q.
 //   warps 4-7, 12-15  converters: thread t = 32q + lane turns head dims
 //                     [64h, 64h + 64) of key t's K codes into f16 in TMEM (A
-//                     operand of S^T), gathers head dim t of keys [64h,
-//                     64h + 64) of the V codes into TMEM (A operand of O^T =
-//                     V^T P'^T), and writes key t's K (h = 0) or V (h = 1)
+//                     operand of S^T), turns head dim t of keys [64h,
+//                     64h + 64) of the V codes (stored dim-major) into TMEM
+//                     (A operand of O^T = V^T P'^T), and writes key t's K
+//                     (h = 0) or V (h = 1)
 //                     scale / zero-point terms (zero for keys out of range).
-//                     Warps 4 and 5 copy the K records and warp 6 the V
-//                     records of the stage NS ahead, one copy instruction
-//                     each, once all eight have converted a stage; thread
-//                     224 (warp 7) issues the stage's S^T MMAs.
-// The first NS stages' copies are issued right after the barriers exist,
-// while Q is staged and tensor memory allocated.
+//   warp 16           producer: block ids, then per stage one TMA copy
+//                     instruction (K records, one lane each) and one bulk
+//                     copy instruction (V records); the first NS stages go
+//                     out right after the barriers exist, while Q is staged
+//   warp 17           S^T MMA issuer (one thread): S^T(s) once stage s is
+//                     converted and its S^T buffer free
+//   warp 18           PV MMA issuer (one thread): PV(s) once P'(s) is written
+// The compute warps only compute: every copy, MMA issue and the waits they
+// need sit on the three control warps.  Two MMA issuers, because a
+// tcgen05.mma of these shapes costs its issuing thread ~75-100 cycles and a
+// 128-key stage takes 16 of them.
 #pragma once
 
 #include "pa_tcgen05.cuh"
@@ -103,7 +108,7 @@ struct U8Cfg {
 __device__ __forceinline__ uint32_t sw64(uint32_t o) { return o ^ (((o >> 7) & 3u) << 4); }
 
 template <int N, int PS>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(608, 1)
     pa_partition_u8(const __grid_constant__ CUtensorMap tmK, const PartArgs a) {
   using C = U8Cfg<N, PS>;
   constexpr int D = C::D;
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(512, 1)
   float4* side_buf = reinterpret_cast<float4*>(smem + C::SIDE_OFF);   // [NB][SK]
   int32_t* blk = reinterpret_cast<int32_t*>(smem + C::BLK_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::MISC_OFF);
-  uint64_t* full = bars;                 // [NS] stage landed (copies of warps 4, 5, 6)
+  uint64_t* full = bars;                 // [NS] stage landed (producer's copies)
   uint64_t* empty = full + C::NS;        // [NS] stage converted (8 converter warps)
   uint64_t* cfull = empty + C::NS;       // [NB] converted stage in TMEM (8 converter warps)
   uint64_t* cfree = cfull + C::NB;       // [NB] converted stage consumed (MMA commit after PV)
@@ -137,13 +142,14 @@ __global__ void __launch_bounds__(512, 1)
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q4 = warp & 3, hh = warp >> 3;                  // TMEM lane quarter, half
-  const bool soft = (warp & 4) == 0;                        // softmax warps 0-3, 8-11
+  const bool soft = warp < 16 && (warp & 4) == 0;           // softmax warps 0-3, 8-11
+  const bool conv = warp < 16 && (warp & 4) != 0;           // converter warps 4-7, 12-15
   const int st_id = hh * 128 + q4 * 32 + lane;              // index among the 256 threads of a role
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so its block-table slice is fetched
   // before the sequence's bounds are known.
-  const bool prefetch = (warp == 4 && a.window == 0);
+  const bool prefetch = (warp == 16 && a.window == 0);
   if (prefetch) {
     const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
     const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
@@ -183,7 +189,7 @@ __global__ void __launch_bounds__(512, 1)
     s_bad = 0;
     s_timeout = 0;
     for (int i = 0; i < C::NS; ++i) {
-      mbar_init(&full[i], 3);
+      mbar_init(&full[i], 1);
       mbar_init(&empty[i], 8);
     }
     for (int i = 0; i < C::NB; ++i) {
@@ -200,69 +206,55 @@ __global__ void __launch_bounds__(512, 1)
   }
   __syncthreads();
 
-  // Stage s's copies, one copy instruction per warp (a copy instruction costs
-  // its warp hundreds of cycles, so each issuing warp issues one, with one
-  // lane per record): warps 4 / 5 the K records of the first / second half of
-  // the stage's pages (TMA boxes), warp 6 all V records (1-D bulk), each with
-  // its own expect-tx arrival.
+  // Stage s's copies from the producer warp: one TMA instruction for the K
+  // records and one bulk instruction for the V records, one lane per page
+  // (a copy instruction costs its warp hundreds of cycles whatever the lanes).
   auto issue_stage = [&](int s) {
-    const int cw = warp - 4;  // 0, 1, 2
     const int slot = s % C::NS;
     const int key0 = kstart + s * C::SK;
     const int npg = (min(C::SK, kend - key0) + PS - 1) / PS;
     uint8_t* st = smem + slot * C::STAGE;
-    constexpr int HALF = (C::PPS + 1) / 2;
-    const int i0 = cw == 1 ? HALF : 0;
-    const int i1 = cw == 0 ? min(npg, HALF) : npg;
-    const int mine = max(0, i1 - i0);
-    if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(mine * C::REC));
+    if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(npg * 2 * C::REC));
     __syncwarp();
-    const int i = i0 + lane;
-    if (i < i1) {
-      const int lp = key0 / PS + i;
+    if (lane < npg) {
+      const int lp = key0 / PS + lane;
       const int id = blk[lp - lp0];
-      if (cw < 2) {
-        tma_load_4d(st + i * C::K_SLOT, &tmK, 0, 0, g, id, &full[slot]);
-        if (a.trace != nullptr)
-          atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
-      } else {
-        bulk_load(st + C::K_AREA + i * C::REC,
-                  a.v_bytes + (static_cast<size_t>(id) * a.Hkv + g) * static_cast<size_t>(C::REC), C::REC,
-                  &full[slot]);
-      }
+      tma_load_4d(st + lane * C::K_SLOT, &tmK, 0, 0, g, id, &full[slot]);
+      if (a.trace != nullptr)
+        atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
+      bulk_load(st + C::K_AREA + lane * C::REC,
+                a.v_bytes + (static_cast<size_t>(id) * a.Hkv + g) * static_cast<size_t>(C::REC), C::REC,
+                &full[slot]);
     }
     __syncwarp();
   };
 
   // ---- set-up: the first stages' copies start at once; meanwhile tensor
   // memory is allocated and Q staged ----
-  if (warp >= 4 && warp < 8) {
-    if (warp == 4) {
-      // stage and validate the partition's block ids; a bad id is reported,
-      // clamped to page 0 (every copy stays in bounds) and the partition's
-      // result discarded
-      prefetch_tensormap(&tmK);
-      int bad = 0;
-      if (prefetch) {
-        cp_async_wait_all();
-        __syncwarp();
-      }
-      for (int j = lane; j < npages; j += 32) {
-        int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
-        if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
-          bad = 1;
-          id = 0;
-        }
-        blk[j] = id;
-      }
-      if (__any_sync(0xffffffffu, bad) && lane == 0) {
-        s_bad = 1;
-        atomicOr(a.status, PA_STATUS_BLOCK_ID);
-      }
+  if (warp == 16) {
+    // stage and validate the partition's block ids; a bad id is reported,
+    // clamped to page 0 (every copy stays in bounds) and the partition's
+    // result discarded
+    prefetch_tensormap(&tmK);
+    int bad = 0;
+    if (prefetch) {
+      cp_async_wait_all();
+      __syncwarp();
     }
-    bar_sync_n(3, 128);  // the block ids are staged for warps 4-7
-    if (warp < 7)
-      for (int s = 0; s < min(C::NS, n_stages); ++s) issue_stage(s);
+    for (int j = lane; j < npages; j += 32) {
+      int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+      if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+        bad = 1;
+        id = 0;
+      }
+      blk[j] = id;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+      s_bad = 1;
+      atomicOr(a.status, PA_STATUS_BLOCK_ID);
+    }
+    __syncwarp();
+    for (int s = 0; s < min(C::NS, n_stages); ++s) issue_stage(s);
   }
   if (warp == 0) {
     tmem_alloc(&s_tmem, C::TMEM_COLS);
@@ -329,18 +321,14 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
   bool ok = true;
 
-  if (!soft) {
-    // =================== converters (+ copies, + S^T MMA issue) =============
+  if (conv) {
+    // =========================== converters =================================
     const int ct = q4 * 32 + lane;                             // key (K) and head dim (V^T), 0..127
     const int pi = ct / PS, kk = ct % PS;
     const uint32_t k_row = static_cast<uint32_t>(pi * C::K_SLOT + kk * 128 + 64 * hh);  // this half of the row
     const uint32_t sc = hh == 0 ? static_cast<uint32_t>(pi * C::K_SLOT + 128 * PS + 2 * kk)
                                 : static_cast<uint32_t>(C::K_AREA + pi * C::REC + 128 * PS + 2 * kk);
-    const uint32_t vsel = static_cast<uint32_t>((ct & 3) | ((4 + (ct & 3)) << 4));  // byte ct%4 of two words
-    const uint32_t vcol = static_cast<uint32_t>(ct & ~3);
     const __half2 k1024 = __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
-    const uint32_t q_base = smem_u32(qt);
-    int issued = min(C::NS, n_stages);
     for (int s = 0; s < n_stages && ok; ++s) {
       const int cb = s % C::NB, slot = s % C::NS;
       if (!mbar_wait(&full[slot], (s / C::NS) & 1) ||
@@ -380,17 +368,24 @@ __global__ void __launch_bounds__(512, 1)
       }
       {
         // V^T: head dim ct of keys [64h, 64h + 64) -> exact f16 codes, keys
-        // 64h + 2j, 64h + 2j + 1 in column j of the half
+        // 64h + 2j, 64h + 2j + 1 in column j of the half.  V records hold
+        // their codes dim-major, so the 16 codes of one head dim over 16 keys
+        // of a page are one 16-byte load.
         uint32_t w[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int k0 = 64 * hh + 2 * j;
-          const uint32_t o = static_cast<uint32_t>(C::K_AREA + (k0 / PS) * C::REC + (k0 % PS) * 128) + vcol;
-          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(st + o);
-          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(st + o + 128);
-          uint32_t h = __byte_perm(__byte_perm(a0, a1, vsel), 0x64646464u, 0x4140u);
-          const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&h), k1024);
-          w[j] = *reinterpret_cast<const uint32_t*>(&c);
+        for (int m = 0; m < 4; ++m) {
+          const int k0 = 64 * hh + 16 * m;
+          const uint4 x = *reinterpret_cast<const uint4*>(st + C::K_AREA + (k0 / PS) * C::REC + ct * PS + (k0 % PS));
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint32_t h0 = __byte_perm(xs[e], 0x64646464u, 0x4140u);
+            uint32_t h1 = __byte_perm(xs[e], 0x64646464u, 0x4342u);
+            const __half2 c0 = __hsub2(*reinterpret_cast<const __half2*>(&h0), k1024);
+            const __half2 c1 = __hsub2(*reinterpret_cast<const __half2*>(&h1), k1024);
+            w[8 * m + 2 * e] = *reinterpret_cast<const uint32_t*>(&c0);
+            w[8 * m + 2 * e + 1] = *reinterpret_cast<const uint32_t*>(&c1);
+          }
         }
         tmem_st32_nowait(tm_v + cb * 64 + 32 * hh + lane_off, w);
       }
@@ -401,37 +396,21 @@ __global__ void __launch_bounds__(512, 1)
         mbar_arrive(&cfull[cb]);
         mbar_arrive(&empty[slot]);
       }
-      if (threadIdx.x == 224) {
-        // S^T(s) = K(s) . Q^T once all eight warps have converted stage s and
-        // the softmax has read the S^T buffer two stages back
-        bool go = mbar_wait(&cfull[cb], (s / C::NB) & 1);
-        if (go && s >= 2) go = mbar_wait(&s_free[s & 1], ((s >> 1) - 1) & 1);
-        if (go) {
-          tc_fence_after();
-#pragma unroll
-          for (int kc = 0; kc < D / 16; ++kc) {
-            const uint64_t bd = sw128_desc(q_base + (kc >> 2) * N * 128 + 32 * (kc & 3), 16, 1024);
-            tc_mma_ta(tm_s0 + (s & 1) * N, tm_k + cb * 64 + 8 * kc, bd, C::IDESC_S, kc > 0 ? 1u : 0u);
-          }
-          tc_commit(&s_full[s & 1]);
-        } else {
-          atomicOr(a.status, PA_STATUS_TIMEOUT);
-          atomicOr(&s_timeout, 1);
-        }
-      }
-      // refill this stage's slot with the stage NS ahead once all eight
-      // warps are done with it
-      if (issued < n_stages) {
-        if (warp >= 4 && warp < 7) {
-          if (!mbar_wait(&empty[slot], (s / C::NS) & 1)) {
-            ok = false;
-            break;
-          }
-          issue_stage(issued);
-        }
-        ++issued;
-      }
       __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      atomicOr(a.status, PA_STATUS_TIMEOUT);
+      atomicOr(&s_timeout, 1);
+    }
+  } else if (warp == 16) {
+    // =========================== producer ===================================
+    for (int s = C::NS; s < n_stages && ok; ++s) {
+      // the slot is free once the eight converter warps are done with stage s - NS
+      if (!mbar_wait(&empty[s % C::NS], ((s / C::NS) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      issue_stage(s);
     }
     if (!ok) {
       if (lane == 0) {
@@ -439,9 +418,56 @@ __global__ void __launch_bounds__(512, 1)
         atomicOr(&s_timeout, 1);
       }
       // let the copies in flight land before the CTA can retire
-      if (warp >= 4 && warp < 7)
-        for (int s = max(0, issued - C::NS); s < issued; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
+      for (int s = 0; s < n_stages; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
     }
+  } else if (warp == 17) {
+    // =========================== S^T MMA issuer =============================
+    if (lane == 0) {
+      const uint32_t q_base = smem_u32(qt);
+      bool fine = true;
+      for (int ns = 0; ns < n_stages && fine; ++ns) {
+        const int cb = ns % C::NB, sb = ns & 1;
+        fine = mbar_wait(&cfull[cb], (ns / C::NB) & 1);
+        if (fine && ns >= 2) fine = mbar_wait(&s_free[sb], ((ns >> 1) - 1) & 1);
+        if (!fine) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kc = 0; kc < D / 16; ++kc) {
+          const uint64_t bd = sw128_desc(q_base + (kc >> 2) * N * 128 + 32 * (kc & 3), 16, 1024);
+          tc_mma_ta(tm_s0 + sb * N, tm_k + cb * 64 + 8 * kc, bd, C::IDESC_S, kc > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[sb]);
+      }
+      if (!fine) {
+        atomicOr(a.status, PA_STATUS_TIMEOUT);
+        atomicOr(&s_timeout, 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 18) {
+    // =========================== PV MMA issuer ==============================
+    if (lane == 0) {
+      bool fine = true;
+      for (int np = 0; np < n_stages && fine; ++np) {
+        const int pb = np & 1, cb = np % C::NB;
+        fine = mbar_wait(&p_full[pb], (np >> 1) & 1);
+        if (!fine) break;
+        tc_fence_after();
+        const uint32_t p_base = smem_u32(pt + pb * C::P_BYTES);
+#pragma unroll
+        for (int j = 0; j < C::SK / 16; ++j) {
+          const uint64_t bd = sw128_desc(p_base + j * 16 * 128, 0, 1024);
+          tc_mma_ta(tm_o, tm_v + cb * 64 + 8 * j, bd, C::IDESC_PV, (np > 0 || j > 0) ? 1u : 0u);
+        }
+        tc_commit(&pv_done[pb]);
+        tc_commit(&cfree[cb]);
+      }
+      if (!fine) {
+        atomicOr(a.status, PA_STATUS_TIMEOUT);
+        atomicOr(&s_timeout, 1);
+      }
+    }
+    __syncwarp();
   }
 
   // =========================== softmax warps (keys) ==========================
@@ -568,22 +594,6 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
-      if (threadIdx.x == 0) {
-        // O^T += V^T(s) . P'^T(s) once the eight softmax warps have written P'(s)
-        if (ok) ok = mbar_wait(&p_full[sb], (s >> 1) & 1);
-        if (ok) {
-          tc_fence_after();
-          const uint32_t p_base = smem_u32(pt + sb * C::P_BYTES);
-#pragma unroll
-          for (int j = 0; j < C::SK / 16; ++j) {
-            const uint64_t bd = sw128_desc(p_base + j * 16 * 128, 0, 1024);
-            tc_mma_ta(tm_o, tm_v + cb * 64 + 8 * j, bd, C::IDESC_PV, (s > 0 || j > 0) ? 1u : 0u);
-          }
-          tc_commit(&pv_done[sb]);
-          tc_commit(&cfree[cb]);
-        }
-      }
-      __syncwarp();
     }
     if (ok && n_stages >= 1) ok = mbar_wait(&pv_done[(n_stages - 1) & 1], ((n_stages - 1) >> 1) & 1);
     if (!ok && lane == 0) {

@@ -116,6 +116,8 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   // with TMA boxes and take 8 tokens or more.
   const bool small_pages = ps < pa::kGatherBelowPageSize;
   if (small_pages && !(kv == PA_F32 || ((kv == PA_BF16 || kv == PA_F16) && D <= 128))) return PA_ERR_PAGE_SIZE;
+  // u8 V pages are copied as [head dim][key] boxes at least 16 keys wide
+  if (kv == PA_U8 && ps < 16) return PA_ERR_PAGE_SIZE;
   const pa_dtype qd = d->q_dtype, od = d->out_dtype;
   if (od != PA_F32 && od != PA_F16 && od != PA_BF16) return PA_ERR_DTYPE;
   bool combo = (kv == PA_F32 && (qd == PA_F32 || qd == PA_F16 || qd == PA_BF16)) ||
@@ -329,6 +331,24 @@ int encode_u8_record_map(CUtensorMap* m, const void* base, const pa_dims* d) {
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// TMA descriptor over a u8 V cache for the warp-level kernel: the codes of a
+// page-head record are dim-major, viewed as dims {ps (keys), D (head dims),
+// Hkv, num_blocks}; one box = box_rows keys of every head dim, no swizzle.
+int encode_u8_v_map(CUtensorMap* m, const void* base, const pa_dims* d, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PA_ERR_CUDA;
+  const cuuint64_t ps = d->page_size, D = d->head_dim;
+  const cuuint64_t rec = ps * (D + 4);
+  cuuint64_t dims[4] = {ps, D, static_cast<cuuint64_t>(d->num_kv_heads), static_cast<cuuint64_t>(d->num_blocks)};
+  cuuint64_t strides[3] = {ps, rec, rec * d->num_kv_heads};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(D), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 struct Call {
   const void* q;
   const void* k;
@@ -416,7 +436,8 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
   } else if (plan.kernel == 0) {
     CUtensorMap mk, mv;
     int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);
-    if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
+    if (rc == PA_OK)
+      rc = c.kv == PA_U8 ? encode_u8_v_map(&mv, c.v, d, box_rows) : encode_cache_map(&mv, c.v, c.kv, d, box_rows);
     if (rc != PA_OK) return rc;
     const int kind = mma_kind(c.kv);
     if (d->head_dim == 64) e = pa::launch_mma_d64(kind, plan.row_tiles, mk, mv, a, grid, c.stream);

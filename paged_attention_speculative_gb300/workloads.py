@@ -96,15 +96,29 @@ def u8_record_bytes(page_size: int, head_dim: int) -> int:
     return page_size * (head_dim + 4)
 
 
-def pack_u8_records(codes: np.ndarray, scale: np.ndarray, zp: np.ndarray) -> np.ndarray:
+def pack_u8_records(codes: np.ndarray, scale: np.ndarray, zp: np.ndarray, dim_major: bool = False) -> np.ndarray:
     """[nb, Hkv, ps, D] codes + [nb, Hkv, ps] fp16 scale / zp -> the u8 page
-    records [nb, Hkv, ps*(D+4)] (codes slot-major, then scales, then zps)."""
+    records [nb, Hkv, ps*(D+4)]: codes, then scales, then zps.  K records hold
+    the codes slot-major ([ps][D]); V records (dim_major) hold them dim-major
+    ([D][ps]), so one head dimension of a page's tokens is contiguous."""
     nb, hkv, ps, d = codes.shape
     rec = np.empty((nb, hkv, ps * (d + 4)), dtype=np.uint8)
-    rec[:, :, : ps * d] = codes.reshape(nb, hkv, ps * d)
+    c = np.swapaxes(codes, 2, 3) if dim_major else codes
+    rec[:, :, : ps * d] = np.ascontiguousarray(c).reshape(nb, hkv, ps * d)
     rec[:, :, ps * d: ps * d + 2 * ps] = np.ascontiguousarray(scale).view(np.uint8).reshape(nb, hkv, 2 * ps)
     rec[:, :, ps * d + 2 * ps:] = np.ascontiguousarray(zp).view(np.uint8).reshape(nb, hkv, 2 * ps)
     return rec
+
+
+def unpack_u8_codes(rec: np.ndarray, page_size: int, head_dim: int, dim_major: bool = False) -> np.ndarray:
+    """The codes of u8 page records as [nb, Hkv, ps, D] (inverse of the code
+    part of pack_u8_records)."""
+    nb, hkv = rec.shape[0], rec.shape[1]
+    ps, d = page_size, head_dim
+    c = rec.reshape(nb, hkv, ps * (d + 4))[:, :, : ps * d]
+    if dim_major:
+        return np.swapaxes(c.reshape(nb, hkv, d, ps), 2, 3)
+    return c.reshape(nb, hkv, ps, d)
 
 
 @dataclasses.dataclass
@@ -226,19 +240,19 @@ def make_case(name: str, *, seed: int, query_lens: Sequence[int], past_lens: Seq
     if not poison:
         valid[:] = True
 
-    def draw_cache():
+    def draw_cache(dim_major):
         x = rng.standard_normal((nb, Hkv, ps, D), dtype=np.float32)
         if kv_dtype == "u8":
             codes, s, z = quantize_u8(x)
             bad = ~valid
             s[np.broadcast_to(bad[:, None, :], s.shape)] = np.float16(np.nan)
             z[np.broadcast_to(bad[:, None, :], z.shape)] = np.float16(np.nan)
-            return pack_u8_records(codes, s, z)
+            return pack_u8_records(codes, s, z, dim_major=dim_major)
         x[np.broadcast_to(~valid[:, None, :, None], x.shape)] = np.nan
         return to_storage(x, kv_dtype)
 
-    k = draw_cache()
-    v = draw_cache()
+    k = draw_cache(False)
+    v = draw_cache(True)  # u8 V records hold their codes dim-major
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     return Case(name=name, q=q, k_cache=k, v_cache=v, block_tables=bt, past_lens=pl.astype(np.int32),

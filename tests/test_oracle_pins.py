@@ -35,9 +35,9 @@ def _decode_cache(case):
         return (W.storage_to_f64(case.k_cache, case.kv_dtype).reshape(case.num_blocks, case.num_kv_heads, ps, D),
                 W.storage_to_f64(case.v_cache, case.kv_dtype).reshape(case.num_blocks, case.num_kv_heads, ps, D))
     out = []
-    for rec in (case.k_cache, case.v_cache):
+    for rec, dim_major in ((case.k_cache, False), (case.v_cache, True)):
         rec = rec.reshape(case.num_blocks, case.num_kv_heads, ps * (D + 4))
-        codes = rec[:, :, : ps * D].reshape(case.num_blocks, case.num_kv_heads, ps, D).astype(np.float64)
+        codes = W.unpack_u8_codes(rec, ps, D, dim_major=dim_major).astype(np.float64)
         sc = np.ascontiguousarray(rec[:, :, ps * D: ps * D + 2 * ps]).view(np.float16).astype(np.float64)
         zp = np.ascontiguousarray(rec[:, :, ps * D + 2 * ps:]).view(np.float16).astype(np.float64)
         out.append((codes - zp[..., None]) * sc[..., None])
@@ -167,7 +167,7 @@ def test_golden_u8_records(oracle_mod):
     sc = np.full((nb, 1, ps), u["scale_fp16"], np.float16)
     zp = np.full((nb, 1, ps), u["zp_fp16"], np.float16)
     kr = W.pack_u8_records(codes_k, sc, zp)
-    vr = W.pack_u8_records(codes_v, sc, zp)
+    vr = W.pack_u8_records(codes_v, sc, zp, dim_major=True)
     q = np.array(c["q"], dtype=np.float32)
     got = oracle_mod.forward(q, "f32", kr, vr, "u8", bt, c["past_lens"], c["subsequence_begins"],
                              num_q_heads=1, num_kv_heads=1, head_dim=D, page_size=ps, num_blocks=nb,
@@ -413,7 +413,14 @@ def _cu_one_token(oracle, x, kv_dtype, D=4, ps=4):
     else:
         cache = np.zeros((1, 1, ps, D), dtype=np.uint16)
     kc, vc = oracle.cache_update(kn, kn, "f32", cache, cache, kv_dtype, [[0]], [1], [0, 1], **_cu_layout(D, ps))
-    assert np.array_equal(kc, vc)
+    if kv_dtype == "u8":
+        # the V record holds the same codes dim-major, and the same scales and zero-points
+        kcodes = W.unpack_u8_codes(kc.reshape(1, 1, -1), ps, D)
+        vcodes = W.unpack_u8_codes(vc.reshape(1, 1, -1), ps, D, dim_major=True)
+        assert np.array_equal(kcodes, vcodes)
+        assert np.array_equal(kc.reshape(-1)[ps * D:], vc.reshape(-1)[ps * D:])
+    else:
+        assert np.array_equal(kc, vc)
     return kc
 
 
