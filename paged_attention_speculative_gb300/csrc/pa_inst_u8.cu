@@ -19,7 +19,7 @@ cudaError_t launch_u8_t(const CUtensorMap& k, const PartArgs& a, dim3 grid, cuda
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  return launch_dependent(kern, grid, dim3(608), smem, st, k, a);
+  return launch_dependent(kern, grid, dim3(640), smem, st, k, a);
 }
 
 template <int N>

@@ -29,14 +29,19 @@
 // Per 128-key stage: the K and V records (codes, scales, zero-points) of the
 // stage's pages land in one shared-memory slot with one copy per record — a
 // TMA box with 64-byte swizzle for K (so the converters read key rows without
-// bank conflicts) and a 1-D bulk copy for V — under one mbarrier; a ring of
-// NS such slots keeps ~120 KB in flight per SM.
+// bank conflicts) and a 1-D bulk copy for V — K and V each under their own
+// mbarrier; a ring of NS = 4 such slots keeps ~135 KB in flight per SM.
+// Converted codes live in tensor memory in two rings: K buffers (free once
+// their S^T MMA is done) and deeper V^T buffers (free only after the PV
+// MMA, which follows the softmax).
 //
-// Warp roles (608 threads, 19 warps; for warps 0-15, q = warp % 4 is the
+// Warp roles (640 threads, 20 warps; for warps 0-15, q = warp % 4 is the
 // TMEM lane quarter a warp may access and h = warp / 8 its half):
 //   warps 0-3, 8-11   softmax: thread = key 32q + lane of the stage (TMEM lane
 //                     of S^T), rows [h N/2, (h+1) N/2); head dim 32q + lane
-//                     of O^T in the epilogue; they also stage Q.
+//                     of O^T in the epilogue; they also stage Q.  The four
+//                     warps of a half share their rows' maxima and rescale
+//                     decisions (named barrier 3 + h), not the other half.
 //   warps 4-7, 12-15  converters: thread t = 32q + lane turns head dims
 //                     [64h, 64h + 64) of key t's K codes into f16 in TMEM (A
 //                     operand of S^T), turns head dim t of keys [64h,
@@ -44,10 +49,15 @@
 //                     (A operand of O^T = V^T P'^T), and writes key t's K
 //                     (h = 0) or V (h = 1)
 //                     scale / zero-point terms (zero for keys out of range).
-//   warp 16           producer: block ids, then per stage one TMA copy
-//                     instruction (K records, one lane each) and one bulk
-//                     copy instruction (V records); the first NS stages go
-//                     out right after the barriers exist, while Q is staged
+//   warp 16           K producer: block ids, then per stage one TMA copy
+//                     instruction (K records, one lane each); the first NS
+//                     stages go out as soon as their ids are read and
+//                     checked, while Q is staged
+//   warp 19           V producer: per stage one bulk copy instruction (V
+//                     records, one lane each).  A copy instruction costs its
+//                     warp ~500 cycles whatever the lanes, so K and V are
+//                     issued by two warps in parallel, each under its own
+//                     mbarrier (the converters start on K before V lands).
 //   warp 17           S^T MMA issuer (one thread): S^T(s) once stage s is
 //                     converted and its S^T buffer free
 //   warp 18           PV MMA issuer (one thread): PV(s) once P'(s) is written
@@ -69,46 +79,63 @@ struct U8Cfg {
   static constexpr int SK = 128;                       // keys per stage (M of the score MMA)
   static constexpr int PPS = SK / PS;                  // pages per stage
   static constexpr int REC = PS * (D + 4);             // one page-head record: codes, scales, zero-points
-  static constexpr int K_SLOT = (REC + 1023) / 1024 * 1024;  // swizzled K records start on 1024-byte boundaries
+  // K records start on 128-byte boundaries (a swizzled TMA destination); the
+  // 64-byte swizzle permutes by absolute shared-memory address bits, and the
+  // stages start on 512-byte boundaries (the pattern's period), so a
+  // record's bytes sit at sw64(offset in the stage)
+  static constexpr int K_SLOT = (REC + 127) / 128 * 128;
   static constexpr int K_AREA = PPS * K_SLOT;
-  static constexpr int STAGE = (K_AREA + PPS * REC + 1023) / 1024 * 1024;
-  static constexpr int NB = 3;                         // converted stages in tensor memory
+  static constexpr int STAGE = (K_AREA + PPS * REC + 511) / 512 * 512;
+  // Converted stages in tensor memory: a K buffer is free once its S^T MMA
+  // is done, a V^T buffer only once its PV MMA is (after the softmax), so
+  // the V ring is the deeper one.  Stage s + NBV's V conversion waits for
+  // PV(s); with a stage's path from landing to PV done ~5,500 cycles, four V
+  // buffers keep that wait off the ~1,500-cycle stage period.
+  static constexpr int NBK = 2;
+  static constexpr int NBV = 4;
   static constexpr int SIDE = SK * 16;                 // float4 per key: ks * scale * log2e, kz + 1024, vs, vz
   static constexpr int Q_BYTES = N * D * 2;            // Q tile (f16), K-major: [chunk][row][128 B]
   static constexpr int P_BYTES = SK * 128;             // P'^T tile (f16), MN-major: [key][64 row slots x 2 B]
   static constexpr int MISC = 6656;
-  static constexpr int FIXED = NB * SIDE + Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + MISC + 1024;
+  static constexpr int FIXED = NBV * SIDE + Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + MISC + 1024;
   static constexpr int NS_FIT = (226 * 1024 - FIXED) / STAGE;
-  static constexpr int NS = NS_FIT > 6 ? 6 : NS_FIT;   // stages in the ring
-  static constexpr int Q_OFF = NS * STAGE;
-  static constexpr int P_OFF = Q_OFF + Q_BYTES;
-  static constexpr int SIDE_OFF = P_OFF + 2 * P_BYTES;
-  static constexpr int BLK_OFF = SIDE_OFF + NB * SIDE;
+  // stages in the ring; a fifth stage measured slower (every CTA's first
+  // stage then shares HBM with more bytes at start-up) and no faster after
+  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+  static constexpr int P_OFF = 0;                      // the 128-byte-swizzled tiles first (1024-aligned)
+  static constexpr int Q_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int ST_OFF = Q_OFF + Q_BYTES;       // the ring of stages
+  static constexpr int SIDE_OFF = ST_OFF + NS * STAGE;
+  static constexpr int BLK_OFF = SIDE_OFF + NBV * SIDE;
   static constexpr int MISC_OFF = BLK_OFF + 4 * kMaxPagesPerCta;
   static constexpr int BYTES = MISC_OFF + MISC + 1024;
   // TMEM columns: O^T [0, N), S^T [N, 3N), K codes [K_COL + 64 b, +64),
   // V^T codes [V_COL + 64 b, +64) (two f16 per column)
   static constexpr int K_COL = 128;
-  static constexpr int V_COL = K_COL + 64 * NB;
+  static constexpr int V_COL = K_COL + 64 * NBK;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = tk_idesc(128, N, false, false, false);
   static constexpr uint32_t IDESC_PV = tk_idesc(128, N, false, false, true);
   static constexpr int NH = N / 2;                     // query rows per softmax thread
   static_assert(3 * N <= K_COL, "tensor-memory budget");
-  static_assert(V_COL + 64 * NB <= TMEM_COLS, "tensor-memory budget");
+  static_assert(V_COL + 64 * NBV <= TMEM_COLS, "tensor-memory budget");
   static_assert(NS >= 3, "the ring needs a few stages");
-  static_assert(STAGE % 1024 == 0 && Q_OFF % 1024 == 0 && P_OFF % 1024 == 0, "swizzled tiles are 1024-aligned");
+  static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0, "128-byte-swizzled tiles are 1024-aligned");
+  static_assert(ST_OFF % 512 == 0 && STAGE % 512 == 0 && K_SLOT % 128 == 0, "64-byte-swizzled records");
   static_assert(REC % 16 == 0, "bulk copies move multiples of 16 bytes");
   static_assert(BYTES <= 227 * 1024, "shared-memory budget");
 };
 
-// Byte offset, inside a 1024-aligned slot, of logical byte `o` of a record
+// Running maximum of a row before its first visible key (log2 domain).
+constexpr float kNoMax = -1e30f;
+
+// Byte offset, inside a stage (stages start on 512-byte boundaries), of logical byte `o` of a record
 // copied with the 64-byte swizzle: the 16-byte unit index (bits 4-5) is XORed
 // with bits 7-8 of the offset.
 __device__ __forceinline__ uint32_t sw64(uint32_t o) { return o ^ (((o >> 7) & 3u) << 4); }
 
 template <int N, int PS>
-__global__ void __launch_bounds__(608, 1)
+__global__ void __launch_bounds__(640, 1)
     pa_partition_u8(const __grid_constant__ CUtensorMap tmK, const PartArgs a) {
   using C = U8Cfg<N, PS>;
   constexpr int D = C::D;
@@ -117,14 +144,17 @@ __global__ void __launch_bounds__(608, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qt = smem + C::Q_OFF;
   uint8_t* pt = smem + C::P_OFF;
-  float4* side_buf = reinterpret_cast<float4*>(smem + C::SIDE_OFF);   // [NB][SK]
+  float4* side_buf = reinterpret_cast<float4*>(smem + C::SIDE_OFF);   // [NBV][SK]
   int32_t* blk = reinterpret_cast<int32_t*>(smem + C::BLK_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::MISC_OFF);
-  uint64_t* full = bars;                 // [NS] stage landed (producer's copies)
-  uint64_t* empty = full + C::NS;        // [NS] stage converted (8 converter warps)
-  uint64_t* cfull = empty + C::NS;       // [NB] converted stage in TMEM (8 converter warps)
-  uint64_t* cfree = cfull + C::NB;       // [NB] converted stage consumed (MMA commit after PV)
-  uint64_t* s_full = cfree + C::NB;      // [2] S^T buffer written (MMA commit)
+  uint64_t* full_k = bars;               // [NS] stage's K records landed
+  uint64_t* full_v = full_k + C::NS;     // [NS] stage's V records landed
+  uint64_t* empty = full_v + C::NS;      // [NS] stage converted (8 converter warps)
+  uint64_t* kfull = empty + C::NS;       // [NBK] K codes in TMEM (8 converter warps)
+  uint64_t* kfree = kfull + C::NBK;      // [NBK] K codes consumed (MMA commit after S^T)
+  uint64_t* vfull = kfree + C::NBK;      // [NBV] V^T codes in TMEM, side terms written (8 converter warps)
+  uint64_t* vfree = vfull + C::NBV;      // [NBV] V^T codes consumed (MMA commit after PV)
+  uint64_t* s_full = vfree + C::NBV;     // [2] S^T buffer written (MMA commit)
   uint64_t* s_free = s_full + 2;         // [2] S^T buffer read (8 softmax warps)
   uint64_t* p_full = s_free + 2;         // [2] P'^T buffer written (8 softmax warps)
   uint64_t* pv_done = p_full + 2;        // [2] PV that read that P'^T buffer done (MMA commit)
@@ -189,12 +219,17 @@ __global__ void __launch_bounds__(608, 1)
     s_bad = 0;
     s_timeout = 0;
     for (int i = 0; i < C::NS; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full_k[i], 1);
+      mbar_init(&full_v[i], 1);
       mbar_init(&empty[i], 8);
     }
-    for (int i = 0; i < C::NB; ++i) {
-      mbar_init(&cfull[i], 8);
-      mbar_init(&cfree[i], 1);
+    for (int i = 0; i < C::NBK; ++i) {
+      mbar_init(&kfull[i], 8);
+      mbar_init(&kfree[i], 1);
+    }
+    for (int i = 0; i < C::NBV; ++i) {
+      mbar_init(&vfull[i], 8);
+      mbar_init(&vfree[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -206,55 +241,72 @@ __global__ void __launch_bounds__(608, 1)
   }
   __syncthreads();
 
-  // Stage s's copies from the producer warp: one TMA instruction for the K
-  // records and one bulk instruction for the V records, one lane per page
-  // (a copy instruction costs its warp hundreds of cycles whatever the lanes).
-  auto issue_stage = [&](int s) {
+  // Stage s's copies from a producer warp, one lane per page: the K records
+  // (warp 16, one TMA instruction) or the V records (warp 19, one bulk
+  // instruction), each half under its own mbarrier.
+  // id_of(j) gives the checked block id of the partition's page j.
+  const bool k_producer = warp == 16;
+  auto issue_stage = [&](int s, auto id_of) {
     const int slot = s % C::NS;
     const int key0 = kstart + s * C::SK;
     const int npg = (min(C::SK, kend - key0) + PS - 1) / PS;
-    uint8_t* st = smem + slot * C::STAGE;
-    if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(npg * 2 * C::REC));
+    uint8_t* st = smem + C::ST_OFF + slot * C::STAGE;
+    uint64_t* bar = k_producer ? &full_k[slot] : &full_v[slot];
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npg * C::REC));
     __syncwarp();
     if (lane < npg) {
       const int lp = key0 / PS + lane;
-      const int id = blk[lp - lp0];
-      tma_load_4d(st + lane * C::K_SLOT, &tmK, 0, 0, g, id, &full[slot]);
-      if (a.trace != nullptr)
-        atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
-      bulk_load(st + C::K_AREA + lane * C::REC,
-                a.v_bytes + (static_cast<size_t>(id) * a.Hkv + g) * static_cast<size_t>(C::REC), C::REC,
-                &full[slot]);
+      const int id = id_of(lp - lp0);
+      if (k_producer) {
+        tma_load_4d(st + lane * C::K_SLOT, &tmK, 0, 0, g, id, bar);
+        if (a.trace != nullptr)
+          atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
+      } else {
+        bulk_load(st + C::K_AREA + lane * C::REC,
+                  a.v_bytes + (static_cast<size_t>(id) * a.Hkv + g) * static_cast<size_t>(C::REC), C::REC, bar);
+      }
     }
     __syncwarp();
   };
 
-  // ---- set-up: the first stages' copies start at once; meanwhile tensor
-  // memory is allocated and Q staged ----
+  // ---- set-up: the first stages' copies go out as soon as their block ids
+  // are known; meanwhile tensor memory is allocated and Q staged.  A bad id
+  // is reported, clamped to page 0 (every copy stays in bounds) and the
+  // partition's result discarded. ----
+  const int32_t* bt_row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0;
   if (warp == 16) {
-    // stage and validate the partition's block ids; a bad id is reported,
-    // clamped to page 0 (every copy stays in bounds) and the partition's
-    // result discarded
     prefetch_tensormap(&tmK);
     int bad = 0;
     if (prefetch) {
       cp_async_wait_all();
       __syncwarp();
     }
-    for (int j = lane; j < npages; j += 32) {
-      int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+    auto checked = [&](int j) {
+      int id = prefetch ? blk[j] : ld_once(bt_row + j);
       if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
         bad = 1;
         id = 0;
       }
-      blk[j] = id;
-    }
+      return id;
+    };
+    for (int s = 0; s < min(C::NS, n_stages); ++s) issue_stage(s, checked);
+    // the later stages' ids, checked once, for both producers
+    for (int j = C::NS * C::PPS + lane; j < npages; j += 32) blk[j] = checked(j);
     if (__any_sync(0xffffffffu, bad) && lane == 0) {
       s_bad = 1;
       atomicOr(a.status, PA_STATUS_BLOCK_ID);
     }
     __syncwarp();
-    for (int s = 0; s < min(C::NS, n_stages); ++s) issue_stage(s);
+    bar_sync_n(2, 64);  // checked ids published to the V producer
+  } else if (warp == 19) {
+    // the V producer's first stages read the ids itself (the K producer
+    // reports bad ones)
+    auto clamped = [&](int j) {
+      const int id = ld_once(bt_row + j);
+      return static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks) ? id : 0;
+    };
+    for (int s = 0; s < min(C::NS, n_stages); ++s) issue_stage(s, clamped);
+    bar_sync_n(2, 64);
   }
   if (warp == 0) {
     tmem_alloc(&s_tmem, C::TMEM_COLS);
@@ -282,7 +334,11 @@ __global__ void __launch_bounds__(608, 1)
       }
       *reinterpret_cast<uint4*>(qt + ((u16 >> 3) * N + n) * 128 + swz(u16 & 7, n)) = v;
     }
-    if (st_id < 64) m_sm[st_id] = -INFINITY;
+    // No key seen yet: a finite floor far below any score (a row's first
+    // visible key always exceeds it by more than the rescale threshold; the
+    // weights 2^(x - m) of masked keys (x = -inf) stay 0 and the rescale
+    // factor 2^(floor - m) of the first rescale is 0).
+    if (st_id < 64) m_sm[st_id] = kNoMax;
     fence_proxy_async();  // the Q tile is read by the tensor cores
     bar_sync_n(1, 256);
     if (st_id < N) {
@@ -329,15 +385,27 @@ __global__ void __launch_bounds__(608, 1)
     const uint32_t sc = hh == 0 ? static_cast<uint32_t>(pi * C::K_SLOT + 128 * PS + 2 * kk)
                                 : static_cast<uint32_t>(C::K_AREA + pi * C::REC + 128 * PS + 2 * kk);
     const __half2 k1024 = __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    // key ct's dequantisation terms (K for h = 0, V for h = 1); zero
+    // outside every row's range and past the partition (there the scales
+    // may be garbage, even NaN)
+    auto side_terms = [&](const uint8_t* st, int s, int vb) {
+      const int key = kstart + s * C::SK + ct;
+      const bool in = key >= si.klo && key <= si.khi && key < kend;
+      const float sv = __half2float(*reinterpret_cast<const __half*>(st + (hh == 0 ? sw64(sc) : sc)));
+      const float zv = __half2float(*reinterpret_cast<const __half*>(st + (hh == 0 ? sw64(sc + 2 * PS) : sc + 2 * PS)));
+      float2 t = hh == 0 ? make_float2(sv * sl2, zv + 1024.f) : make_float2(sv, zv);
+      if (!in) t = make_float2(0.f, 0.f);
+      reinterpret_cast<float2*>(side_buf + vb * C::SK + ct)[hh] = t;
+    };
     for (int s = 0; s < n_stages && ok; ++s) {
-      const int cb = s % C::NB, slot = s % C::NS;
-      if (!mbar_wait(&full[slot], (s / C::NS) & 1) ||
-          (s >= C::NB && !mbar_wait(&cfree[cb], ((s / C::NB) - 1) & 1))) {
+      const int kb = s % C::NBK, vb = s % C::NBV, slot = s % C::NS;
+      if (!mbar_wait(&full_k[slot], (s / C::NS) & 1) ||
+          (s >= C::NBK && !mbar_wait(&kfree[kb], ((s / C::NBK) - 1) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint8_t* st = smem + slot * C::STAGE;
+      const uint8_t* st = smem + C::ST_OFF + slot * C::STAGE;
       {
         // head dims [64h, 64h + 64) of key ct's K codes -> (1024 + code) as
         // f16 pairs; column j of the half holds dims 64h + 2j, 64h + 2j + 1
@@ -352,20 +420,21 @@ __global__ void __launch_bounds__(608, 1)
             w[8 * u + 2 * e + 1] = __byte_perm(xs[e], 0x64646464u, 0x4342u);
           }
         }
-        tmem_st32_nowait(tm_k + cb * 64 + 32 * hh + lane_off, w);
+        tmem_st32_nowait(tm_k + kb * 64 + 32 * hh + lane_off, w);
       }
-      {
-        // key ct's dequantisation terms (K for h = 0, V for h = 1); zero
-        // outside every row's range and past the partition (there the scales
-        // may be garbage, even NaN)
-        const int key = kstart + s * C::SK + ct;
-        const bool in = key >= si.klo && key <= si.khi && key < kend;
-        const float sv = __half2float(*reinterpret_cast<const __half*>(st + (hh == 0 ? sw64(sc) : sc)));
-        const float zv = __half2float(*reinterpret_cast<const __half*>(st + (hh == 0 ? sw64(sc + 2 * PS) : sc + 2 * PS)));
-        float2 t = hh == 0 ? make_float2(sv * sl2, zv + 1024.f) : make_float2(sv, zv);
-        if (!in) t = make_float2(0.f, 0.f);
-        reinterpret_cast<float2*>(side_buf + cb * C::SK + ct)[hh] = t;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kfull[kb]);  // S^T(s) may start
+      if (!mbar_wait(&full_v[slot], (s / C::NS) & 1) ||
+          (s >= C::NBV && !mbar_wait(&vfree[vb], ((s / C::NBV) - 1) & 1))) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
+      // the side terms' slot was last read by the softmax of stage s - NBV,
+      // which finished before PV(s - NBV) was issued
+      side_terms(st, s, vb);
       {
         // V^T: head dim ct of keys [64h, 64h + 64) -> exact f16 codes, keys
         // 64h + 2j, 64h + 2j + 1 in column j of the half.  V records hold
@@ -387,13 +456,13 @@ __global__ void __launch_bounds__(608, 1)
             w[8 * m + 2 * e + 1] = *reinterpret_cast<const uint32_t*>(&c1);
           }
         }
-        tmem_st32_nowait(tm_v + cb * 64 + 32 * hh + lane_off, w);
+        tmem_st32_nowait(tm_v + vb * 64 + 32 * hh + lane_off, w);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&cfull[cb]);
+        mbar_arrive(&vfull[vb]);
         mbar_arrive(&empty[slot]);
       }
       __syncwarp();
@@ -402,23 +471,26 @@ __global__ void __launch_bounds__(608, 1)
       atomicOr(a.status, PA_STATUS_TIMEOUT);
       atomicOr(&s_timeout, 1);
     }
-  } else if (warp == 16) {
-    // =========================== producer ===================================
+  } else if (warp == 16 || warp == 19) {
+    // =========================== producers ==================================
+    int issued = min(C::NS, n_stages);
     for (int s = C::NS; s < n_stages && ok; ++s) {
       // the slot is free once the eight converter warps are done with stage s - NS
       if (!mbar_wait(&empty[s % C::NS], ((s / C::NS) - 1) & 1)) {
         ok = false;
         break;
       }
-      issue_stage(s);
+      issue_stage(s, [&](int j) { return blk[j]; });
+      issued = s + 1;
     }
     if (!ok) {
       if (lane == 0) {
         atomicOr(a.status, PA_STATUS_TIMEOUT);
         atomicOr(&s_timeout, 1);
       }
-      // let the copies in flight land before the CTA can retire
-      for (int s = 0; s < n_stages; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
+      // let this warp's copies in flight land before the CTA can retire
+      uint64_t* mine = k_producer ? full_k : full_v;
+      for (int s = max(0, issued - C::NS); s < issued; ++s) mbar_wait(&mine[s % C::NS], (s / C::NS) & 1);
     }
   } else if (warp == 17) {
     // =========================== S^T MMA issuer =============================
@@ -426,17 +498,18 @@ __global__ void __launch_bounds__(608, 1)
       const uint32_t q_base = smem_u32(qt);
       bool fine = true;
       for (int ns = 0; ns < n_stages && fine; ++ns) {
-        const int cb = ns % C::NB, sb = ns & 1;
-        fine = mbar_wait(&cfull[cb], (ns / C::NB) & 1);
+        const int kb = ns % C::NBK, sb = ns & 1;
+        fine = mbar_wait(&kfull[kb], (ns / C::NBK) & 1);
         if (fine && ns >= 2) fine = mbar_wait(&s_free[sb], ((ns >> 1) - 1) & 1);
         if (!fine) break;
         tc_fence_after();
 #pragma unroll
         for (int kc = 0; kc < D / 16; ++kc) {
           const uint64_t bd = sw128_desc(q_base + (kc >> 2) * N * 128 + 32 * (kc & 3), 16, 1024);
-          tc_mma_ta(tm_s0 + sb * N, tm_k + cb * 64 + 8 * kc, bd, C::IDESC_S, kc > 0 ? 1u : 0u);
+          tc_mma_ta(tm_s0 + sb * N, tm_k + kb * 64 + 8 * kc, bd, C::IDESC_S, kc > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[sb]);
+        tc_commit(&kfree[kb]);
       }
       if (!fine) {
         atomicOr(a.status, PA_STATUS_TIMEOUT);
@@ -449,7 +522,7 @@ __global__ void __launch_bounds__(608, 1)
     if (lane == 0) {
       bool fine = true;
       for (int np = 0; np < n_stages && fine; ++np) {
-        const int pb = np & 1, cb = np % C::NB;
+        const int pb = np & 1, vb = np % C::NBV;
         fine = mbar_wait(&p_full[pb], (np >> 1) & 1);
         if (!fine) break;
         tc_fence_after();
@@ -457,10 +530,10 @@ __global__ void __launch_bounds__(608, 1)
 #pragma unroll
         for (int j = 0; j < C::SK / 16; ++j) {
           const uint64_t bd = sw128_desc(p_base + j * 16 * 128, 0, 1024);
-          tc_mma_ta(tm_o, tm_v + cb * 64 + 8 * j, bd, C::IDESC_PV, (np > 0 || j > 0) ? 1u : 0u);
+          tc_mma_ta(tm_o, tm_v + vb * 64 + 8 * j, bd, C::IDESC_PV, (np > 0 || j > 0) ? 1u : 0u);
         }
         tc_commit(&pv_done[pb]);
-        tc_commit(&cfree[cb]);
+        tc_commit(&vfree[vb]);
       }
       if (!fine) {
         atomicOr(a.status, PA_STATUS_TIMEOUT);
@@ -475,6 +548,7 @@ __global__ void __launch_bounds__(608, 1)
   if (soft) {
     const int kq = q4 * 32 + lane;     // key of the stage
     const int n0 = hh * NH;            // this thread's rows [n0, n0 + NH)
+    const int hbar = 3 + hh;           // named barrier of this half's four warps
 #pragma unroll
     for (int e = 0; e < NH; ++e) {
       l[e] = 0.f;
@@ -482,7 +556,7 @@ __global__ void __launch_bounds__(608, 1)
     }
     const bool tree = a.tree_mask != nullptr;
     for (int s = 0; s < n_stages; ++s) {
-      const int sb = s & 1, cb = s % C::NB;
+      const int sb = s & 1, vb = s % C::NBV;
       if (ok) ok = mbar_wait(&s_full[sb], (s >> 1) & 1);
       tc_fence_after();
       float v[NH];
@@ -490,24 +564,33 @@ __global__ void __launch_bounds__(608, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
-      // this key's dequantisation terms (written by the converters before cfull)
-      if (ok) ok = mbar_wait(&cfull[cb], (s / C::NB) & 1);
-      const float4 sd = side_buf[cb * C::SK + kq];
+      // this key's dequantisation terms (written by the converters before vfull)
+      if (ok) ok = mbar_wait(&vfull[vb], (s / C::NBV) & 1);
+      const float4 sd = side_buf[vb * C::SK + kq];
 
-      const int key = kstart + s * C::SK + kq;
-      const int dk = key - si.L;
-      // rows that see this key, as a bit set: [nlo, nhi) (the causal limit
-      // and the window), or for a tree mask the window and the rows whose
-      // mask names this new token
-      const int nlo = (dk > 0 && !tree) ? dk * a.G : 0;
-      int nhi = R;
-      if (a.window > 0) nhi = min(R, max(0, (dk + a.window) * a.G));
-      if (key >= kend) nhi = 0;  // past the partition: the next partition's keys
-      const uint32_t below_hi = nhi >= 32 ? 0xffffffffu : ((1u << nhi) - 1u);
-      const uint32_t below_lo = nlo >= 32 ? 0xffffffffu : ((1u << nlo) - 1u);
-      uint32_t vrows = below_hi & ~below_lo;
-      if (tree && dk >= 0) vrows &= (dk < PA_MAX_QUERY_LEN) ? tree_rows[dk] : 0u;
-      const bool clean = (nlo == 0 && nhi >= R) && !(tree && dk >= 0);
+      // Every row sees every key of the stage (the common case: past keys
+      // inside every row's window and the partition) -- the same for all
+      // threads, so the per-key row mask is skipped.  Only for 16-row tiles:
+      // with 16 rows per thread the extra code spills and measured slower.
+      const int k0 = kstart + s * C::SK;
+      const bool stage_clean = NH <= 8 && !tree && k0 + C::SK - 1 <= si.L && k0 + C::SK <= kend &&
+                               (a.window == 0 || k0 - si.L + a.window >= si.T);
+      uint32_t vrows = 0xffffffffu;
+      if (!stage_clean) {
+        const int key = k0 + kq;
+        const int dk = key - si.L;
+        // rows that see this key, as a bit set: [nlo, nhi) (the causal limit
+        // and the window), or for a tree mask the window and the rows whose
+        // mask names this new token
+        const int nlo = (dk > 0 && !tree) ? dk * a.G : 0;
+        int nhi = R;
+        if (a.window > 0) nhi = min(R, max(0, (dk + a.window) * a.G));
+        if (key >= kend) nhi = 0;  // past the partition: the next partition's keys
+        const uint32_t below_hi = nhi >= 32 ? 0xffffffffu : ((1u << nhi) - 1u);
+        const uint32_t below_lo = nlo >= 32 ? 0xffffffffu : ((1u << nlo) - 1u);
+        vrows = below_hi & ~below_lo;
+        if (tree && dk >= 0) vrows &= (dk < PA_MAX_QUERY_LEN) ? tree_rows[dk] : 0u;
+      }
       bool need = false;
 #pragma unroll
       for (int e4 = 0; e4 < NH; e4 += 4) {
@@ -518,12 +601,14 @@ __global__ void __launch_bounds__(608, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float x = fmaf(-sd.y, qs[e], v[e4 + e]) * sd.x;
-          if (!clean) x = ((vrows >> (n0 + e4 + e)) & 1u) ? x : -INFINITY;
+          if (!stage_clean) x = ((vrows >> (n0 + e4 + e)) & 1u) ? x : -INFINITY;
           v[e4 + e] = x;
           need |= x > mm[e] + 8.f;
         }
       }
-      if (bar_any(1, 256, need)) {
+      // A half's four warps own the same rows, so the rescale decision and
+      // the new maxima involve only them (named barrier 3 + h).
+      if (bar_any(hbar, 128, need)) {
         const int xw = hh * 4 + q4;  // this warp's slot in the exchange
 #pragma unroll
         for (int e = 0; e < NH; ++e) {
@@ -532,23 +617,24 @@ __global__ void __launch_bounds__(608, 1)
           for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
           if (lane == 0) xch[xw * 64 + n0 + e] = t;
         }
-        bar_sync_n(1, 256);
-        if (st_id < N) {
-          const int n = st_id, hn = n / NH;
-          const float rm = fmaxf(fmaxf(xch[(hn * 4) * 64 + n], xch[(hn * 4 + 1) * 64 + n]),
-                                 fmaxf(xch[(hn * 4 + 2) * 64 + n], xch[(hn * 4 + 3) * 64 + n]));
+        bar_sync_n(hbar, 128);
+        const int hr = q4 * 32 + lane;  // a row of this half, for the first NH threads
+        if (hr < NH) {
+          const int n = n0 + hr;
+          const float rm = fmaxf(fmaxf(xch[(hh * 4) * 64 + n], xch[(hh * 4 + 1) * 64 + n]),
+                                 fmaxf(xch[(hh * 4 + 2) * 64 + n], xch[(hh * 4 + 3) * 64 + n]));
           const float mo = m_sm[n];
           const float mn = rm > mo + 8.f ? rm : mo;
           m_next[n] = mn;
           alpha_sm[n] = (mn == mo) ? 1.f : ex2(mo - mn);
         }
-        bar_sync_n(1, 256);
+        bar_sync_n(hbar, 128);
 #pragma unroll
         for (int e = 0; e < NH; ++e) {
           l[e] *= alpha_sm[n0 + e];
           zc[e] *= alpha_sm[n0 + e];
         }
-        if (st_id < N) m_sm[st_id] = m_next[st_id];
+        if (hr < NH) m_sm[n0 + hr] = m_next[n0 + hr];
         if (s >= 1) {
           // rescale this half's columns of O^T once the previous PV has landed
           if (ok) ok = mbar_wait(&pv_done[(s - 1) & 1], ((s - 1) >> 1) & 1);
@@ -560,7 +646,7 @@ __global__ void __launch_bounds__(608, 1)
           tmem_st_small<NH>(tm_o + n0 + lane_off, reinterpret_cast<const uint32_t*>(o));
           tc_fence_before();
         }
-        bar_sync_n(1, 256);
+        bar_sync_n(hbar, 128);
       }
       // weights times the key's V scale, rounded to f16 as the MMA reads them
       // (8 rows = one 16-byte unit of this key's P'^T row at a time); the
@@ -577,9 +663,7 @@ __global__ void __launch_bounds__(608, 1)
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
           const int i = 8 * u + e;
-          const float mu0 = mm[e] == -INFINITY ? 0.f : mm[e];
-          const float mu1 = mm[e + 1] == -INFINITY ? 0.f : mm[e + 1];
-          const float p0 = ex2(v[i] - mu0), p1 = ex2(v[i + 1] - mu1);
+          const float p0 = ex2(v[i] - mm[e]), p1 = ex2(v[i + 1] - mm[e + 1]);
           l[i] += p0;
           l[i + 1] += p1;
           const __half2 h = __floats2half2_rn(p0 * sd.z, p1 * sd.z);
