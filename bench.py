@@ -804,6 +804,11 @@ def run_ours(args, rank, world):
 # cp.async page gather (one token per page) and a prefill chunk alone.
 PROFILE_EXTRA = {
     "long_T8_L131072_ps1": dict(Hq=64, Hkv=8, D=128, ps=1, kv="bf16", q_lens=[8], past=[131072], window=0),
+    # u8 with 64 query rows per KV head: the warp-level kernel's u8 path
+    "long_u8_T8_L32768": dict(Hq=64, Hkv=8, D=128, ps=16, kv="u8", q_lens=[8], past=[32768], window=0),
+    # the cache update before each verify step (64 sequences of 4 new tokens)
+    "update_batch64_T4_L4096": dict(Hq=32, Hkv=8, D=128, ps=16, kv="bf16", q_lens=[4] * 64, past=[4096] * 64,
+                                    window=0, update=True),
     "prefill_T512_L32768": dict(Hq=32, Hkv=8, D=128, ps=16, kv="bf16", q_lens=[512], past=[32768], window=0,
                                 mixed=True),
 }
@@ -839,6 +844,8 @@ def run_profile(args):
     step = wl.forward_mixed if spec.get("mixed") else wl.forward
     with torch.cuda.stream(stream):
         for s in range(args.warmup + args.steps):
+            if spec.get("update"):
+                wl.cache_update(s % wl.replicas, stream)
             step(s % wl.replicas, stream)
     torch.cuda.synchronize()
     log(f"[profile] {spec['name']}: {args.warmup + args.steps} steps, plan {wl.plan().as_dict()}, "
