@@ -166,6 +166,22 @@ __device__ __forceinline__ void store_out(void* out, int dtype, size_t idx, floa
   }
 }
 
+// Four consecutive output elements (idx a multiple of 4), packed as the output
+// type: one 16-byte (fp32) or 8-byte (16-bit) store.
+__device__ __forceinline__ void store_out4(void* out, int dtype, size_t idx, float4 v) {
+  if (dtype == PA_F32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + idx) = v;
+  } else if (dtype == PA_BF16) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + idx) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  } else {
+    const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(out) + idx) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory barriers and asynchronous copies (PTX).
 // ---------------------------------------------------------------------------

@@ -621,29 +621,48 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
   consumer_sync();
 
   const bool poisoned = s_timeout != 0;
-  for (int idx = threadIdx.x; idx < R * D; idx += kConsumerWarps * 32) {
-    const int r = idx / D, d = idx % D;
+  // One warp per row: the row's key-split weights and its output offset once
+  // (no per-element index arithmetic), then four head dims per lane.
+  for (int r = warp; r < R; r += kConsumerWarps) {
     const int rgr = r / RPW, rl = r % RPW;
     float M = -INFINITY;
     for (int k2 = 0; k2 < KS; ++k2) M = fmaxf(M, mm[(k2 * RG + rgr) * RPW + rl]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
-    float acc = 0.f, lsum = 0.f;
-    for (int k2 = 0; k2 < KS; ++k2) {
-      const int wr = (k2 * RG + rgr) * RPW + rl;
-      const float wgt = ex2(mm[wr] - Mu);
-      acc += wgt * mo[wr * S::MERGE_LD + d];
-      lsum += wgt * ml[wr];
-    }
-    const size_t row = static_cast<size_t>(si.t0 + r / a.G) * a.Hq + g * a.G + r % a.G;
-    if (si.nparts == 1) {
-      store_out(a.out, a.out_dtype, row * D + d, (poisoned || !(lsum > 0.f)) ? 0.f : acc / lsum);
-    } else {
-      const size_t pr = prow(row, si, a.Hq) * a.num_parts + p;
-      a.po[pr * D + d] = acc;
-      if (d == 0) {
-        a.pm[pr] = M;
-        a.pl[pr] = poisoned ? -1.f : lsum;
+    float wgt[kConsumerWarps];
+    float lsum = 0.f;
+#pragma unroll
+    for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
+      wgt[k2] = 0.f;
+      if (k2 < KS) {
+        const int wr = (k2 * RG + rgr) * RPW + rl;
+        wgt[k2] = ex2(mm[wr] - Mu);
+        lsum += wgt[k2] * ml[wr];
       }
+    }
+    const int tq = r / a.G;
+    const size_t row = static_cast<size_t>(si.t0 + tq) * a.Hq + g * a.G + (r - tq * a.G);
+    const float inv = (poisoned || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+    const size_t pr = prow(row, si, a.Hq) * a.num_parts + p;
+    for (int d = 4 * lane; d < D; d += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
+        if (k2 < KS) {
+          const float4 x = *reinterpret_cast<const float4*>(mo + ((k2 * RG + rgr) * RPW + rl) * S::MERGE_LD + d);
+          acc.x = fmaf(wgt[k2], x.x, acc.x);
+          acc.y = fmaf(wgt[k2], x.y, acc.y);
+          acc.z = fmaf(wgt[k2], x.z, acc.z);
+          acc.w = fmaf(wgt[k2], x.w, acc.w);
+        }
+      }
+      if (si.nparts == 1)
+        store_out4(a.out, a.out_dtype, row * D + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+      else
+        *reinterpret_cast<float4*>(a.po + pr * D + d) = acc;
+    }
+    if (si.nparts > 1 && lane == 0) {
+      a.pm[pr] = M;
+      a.pl[pr] = poisoned ? -1.f : lsum;
     }
   }
 }
