@@ -480,7 +480,7 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.role = c.role;
   const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + pa::kCombineRows - 1) / pa::kCombineRows));
   cfg.blockDim = dim3(pa::kCombineWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = c.stream;
