@@ -283,6 +283,18 @@ __device__ __forceinline__ void bar_sync_n(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// L2 prefetches: a hint only, nothing returns to the program.  Issued before
+// griddepcontrol.wait they warm L2 with lines the kernel will read once the
+// previous kernel is done; a later write by that kernel updates the line.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+// bytes: a multiple of 16, src 16-byte aligned.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 // 4-byte asynchronous global -> shared copy (completion: cp_async_wait_all).
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");

@@ -83,6 +83,20 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
 
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // While the previous kernel may still be running (programmatic dependent
+  // launch), warm L2 with the sequence metadata and this partition's
+  // block-table slice (prefetches only: every value the kernel uses is
+  // loaded after griddepcontrol.wait).
+  if (!GATHER && warp == 3 && a.window == 0) {
+    if (lane == 0) {
+      prefetch_l2(a.begins + b);
+      prefetch_l2(a.past_lens + b);
+    }
+    const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
+    const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
+                                       max(0LL, static_cast<long long>(a.max_blocks) - lpg)));
+    for (int j = 32 * lane; j < n; j += 32 * 32) prefetch_l2(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lpg + j);
+  }
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so the producer starts fetching its

@@ -175,6 +175,20 @@ __global__ void __launch_bounds__(640, 1)
   const bool soft = warp < 16 && (warp & 4) == 0;           // softmax warps 0-3, 8-11
   const bool conv = warp < 16 && (warp & 4) != 0;           // converter warps 4-7, 12-15
   const int st_id = hh * 128 + q4 * 32 + lane;              // index among the 256 threads of a role
+  // While the previous kernel may still be running (programmatic dependent
+  // launch), warm L2 with the sequence metadata and this partition's
+  // block-table slice (prefetches only: every value the kernel uses is
+  // loaded after griddepcontrol.wait).
+  if (warp == 16 && a.window == 0) {
+    if (lane == 0) {
+      prefetch_l2(a.begins + b);
+      prefetch_l2(a.past_lens + b);
+    }
+    const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
+    const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
+                                       max(0LL, static_cast<long long>(a.max_blocks) - lpg)));
+    for (int j = 32 * lane; j < n; j += 32 * 32) prefetch_l2(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lpg + j);
+  }
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so its block-table slice is fetched
