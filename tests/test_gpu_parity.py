@@ -51,6 +51,14 @@ SMALL = [
                         head_dim=128, page_size=16, kv_dtype="u8"),
     lambda: W.make_case("window1", seed=17, query_lens=[4], past_lens=[200], num_q_heads=8, num_kv_heads=2,
                         head_dim=128, page_size=16, sliding_window=1),
+    # odd numbers of output rows (the combine packs two rows per CTA; its last
+    # CTA then has one row past the end), on each partition kernel
+    lambda: W.make_case("odd_rows_tc", seed=21, query_lens=[3], past_lens=[3000], num_q_heads=5, num_kv_heads=1,
+                        head_dim=128, page_size=16),
+    lambda: W.make_case("odd_rows_u8", seed=22, query_lens=[5], past_lens=[2600], num_q_heads=3, num_kv_heads=1,
+                        head_dim=128, page_size=16, kv_dtype="u8"),
+    lambda: W.make_case("odd_rows_d256", seed=23, query_lens=[3, 1], past_lens=[2200, 1700], num_q_heads=3,
+                        num_kv_heads=1, head_dim=256, page_size=64),
 ]
 
 
