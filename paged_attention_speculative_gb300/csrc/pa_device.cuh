@@ -149,6 +149,38 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Reduces each of a lane's NV values (NV a power of two, <= 32) over the
+// warp's 32 lanes by recursive halving: at each exchange a lane keeps one half
+// of its values, sends the other half to its partner and combines what comes
+// back, so the warp spends NV - 1 + log2(32 / NV) shuffles instead of 5 NV.
+// v is overwritten.  Returns, in lane l, the reduction of value l / (32 / NV).
+template <int NV, typename Op>
+__device__ __forceinline__ float warp_reduce_split(float* v, int lane, Op op) {
+  static_assert(NV >= 1 && NV <= 32 && (NV & (NV - 1)) == 0, "NV: a power of two up to 32");
+  int o = 16;
+#pragma unroll
+  for (int n = NV; n > 1; n >>= 1) {
+    const bool up = (lane & o) != 0;  // this lane keeps the upper half
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? v[i] : v[i + n / 2];
+      const float keep = up ? v[i + n / 2] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+    o >>= 1;
+  }
+  float t = v[0];
+#pragma unroll
+  for (int k = 32 / NV / 2; k > 0; k >>= 1) t = op(t, __shfl_xor_sync(0xffffffffu, t, k));
+  return t;
+}
+struct OpAdd {
+  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
+struct OpMax {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+
 __device__ __forceinline__ float load_q_elem(const void* q, int dtype, size_t idx) {
   if (dtype == PA_F32) return __ldg(reinterpret_cast<const float*>(q) + idx);
   const unsigned short bits = __ldg(reinterpret_cast<const unsigned short*>(q) + idx);

@@ -96,7 +96,7 @@ struct U8Cfg {
   static constexpr int SIDE = SK * 16;                 // float4 per key: ks * scale * log2e, kz + 1024, vs, vz
   static constexpr int Q_BYTES = N * D * 2;            // Q tile (f16), K-major: [chunk][row][128 B]
   static constexpr int P_BYTES = SK * 128;             // P'^T tile (f16), MN-major: [key][64 row slots x 2 B]
-  static constexpr int MISC = 6656;
+  static constexpr int MISC = 7168;
   static constexpr int FIXED = NBV * SIDE + Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + MISC + 1024;
   static constexpr int NS_FIT = (226 * 1024 - FIXED) / STAGE;
   // stages in the ring; a fifth stage measured slower (every CTA's first
@@ -109,15 +109,21 @@ struct U8Cfg {
   static constexpr int BLK_OFF = SIDE_OFF + NBV * SIDE;
   static constexpr int MISC_OFF = BLK_OFF + 4 * kMaxPagesPerCta;
   static constexpr int BYTES = MISC_OFF + MISC + 1024;
-  // TMEM columns: O^T [0, N), S^T [N, 3N), K codes [K_COL + 64 b, +64),
+  // TMEM columns: O^T [0, NACC N), S^T [NACC N, (NACC + 2) N), K codes [K_COL + 64 b, +64),
   // V^T codes [V_COL + 64 b, +64) (two f16 per column)
   static constexpr int K_COL = 128;
   static constexpr int V_COL = K_COL + 64 * NBK;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = tk_idesc(128, N, false, false, false);
   static constexpr uint32_t IDESC_PV = tk_idesc(128, N, false, false, true);
-  static constexpr int NH = N / 2;                     // query rows per softmax thread
-  static_assert(3 * N <= K_COL, "tensor-memory budget");
+  // 16-row tiles: the two softmax halves take alternate stages, each over all
+  // 16 rows with its own running maxima and O^T accumulator (merged in the
+  // epilogue), so a stage's softmax chain overlaps the next one's; 32-row
+  // tiles: each half takes 16 of the rows of every stage (one accumulator).
+  static constexpr bool ALT = N == 16;
+  static constexpr int NH = ALT ? N : N / 2;           // query rows per softmax thread
+  static constexpr int NACC = ALT ? 2 : 1;             // O^T accumulators
+  static_assert((NACC + 2) * N <= K_COL, "tensor-memory budget");
   static_assert(V_COL + 64 * NBV <= TMEM_COLS, "tensor-memory budget");
   static_assert(NS >= 3, "the ring needs a few stages");
   static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0, "128-byte-swizzled tiles are 1024-aligned");
@@ -158,11 +164,11 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* s_free = s_full + 2;         // [2] S^T buffer read (8 softmax warps)
   uint64_t* p_full = s_free + 2;         // [2] P'^T buffer written (8 softmax warps)
   uint64_t* pv_done = p_full + 2;        // [2] PV that read that P'^T buffer done (MMA commit)
-  float* m_sm = reinterpret_cast<float*>(smem + C::MISC_OFF + 512);   // [64] row reference maxima
-  float* xch = m_sm + 64;                                             // [8][64] per-warp row values
-  float* m_next = xch + 512;                                          // [64]
-  float* alpha_sm = m_next + 64;                                      // [64]
-  long long* rowoff = reinterpret_cast<long long*>(alpha_sm + 64);    // [64]
+  float* m_sm = reinterpret_cast<float*>(smem + C::MISC_OFF + 512);   // [2][64] row reference maxima (per half when ALT)
+  float* xch = m_sm + 128;                                            // [8][64] per-warp row values
+  float* m_next = xch + 512;                                          // [2][64]
+  float* alpha_sm = m_next + 128;                                     // [2][64]
+  long long* rowoff = reinterpret_cast<long long*>(alpha_sm + 128);   // [64]
   float* qsum_sm = reinterpret_cast<float*>(rowoff + 64);             // [64] sum_d of each f16 query row
   float* xch2 = qsum_sm + 64;                                         // [8][64] second exchange
   uint32_t* tree_rows = reinterpret_cast<uint32_t*>(xch2 + 512);      // [8] rows that see new token k
@@ -247,8 +253,8 @@ __global__ void __launch_bounds__(640, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 8);
-      mbar_init(&p_full[i], 8);
+      mbar_init(&s_free[i], C::ALT ? 4 : 8);  // the softmax warps reading / writing stage s
+      mbar_init(&p_full[i], C::ALT ? 4 : 8);
       mbar_init(&pv_done[i], 1);
     }
     fence_barrier_init();
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(640, 1)
     // visible key always exceeds it by more than the rescale threshold; the
     // weights 2^(x - m) of masked keys (x = -inf) stay 0 and the rescale
     // factor 2^(floor - m) of the first rescale is 0).
-    if (st_id < 64) m_sm[st_id] = kNoMax;
+    if (st_id < 128) m_sm[st_id] = kNoMax;
     fence_proxy_async();  // the Q tile is read by the tensor cores
     bar_sync_n(1, 256);
     if (st_id < N) {
@@ -384,8 +390,8 @@ __global__ void __launch_bounds__(640, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t tm_o = tmem;            // O^T: lane = head dim, column = row
-  const uint32_t tm_s0 = tmem + N;       // S^T buffers: lane = key, column = row
+  const uint32_t tm_o = tmem;            // O^T accumulators: lane = head dim, column = row
+  const uint32_t tm_s0 = tmem + C::NACC * N;  // S^T buffers: lane = key, column = row
   const uint32_t tm_k = tmem + C::K_COL; // K codes + 1024: lane = key, two f16 per column
   const uint32_t tm_v = tmem + C::V_COL; // V^T codes: lane = head dim, two keys per column
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
@@ -544,7 +550,8 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
         for (int j = 0; j < C::SK / 16; ++j) {
           const uint64_t bd = sw128_desc(p_base + j * 16 * 128, 0, 1024);
-          tc_mma_ta(tm_o, tm_v + vb * 64 + 8 * j, bd, C::IDESC_PV, (np > 0 || j > 0) ? 1u : 0u);
+          tc_mma_ta(tm_o + (C::ALT ? (np & 1) * N : 0), tm_v + vb * 64 + 8 * j, bd, C::IDESC_PV,
+                    (np >= C::NACC || j > 0) ? 1u : 0u);
         }
         tc_commit(&pv_done[pb]);
         tc_commit(&vfree[vb]);
@@ -561,15 +568,21 @@ __global__ void __launch_bounds__(640, 1)
   float l[NH], zc[NH];
   if (soft) {
     const int kq = q4 * 32 + lane;     // key of the stage
-    const int n0 = hh * NH;            // this thread's rows [n0, n0 + NH)
+    const int n0 = C::ALT ? 0 : hh * NH;  // this thread's rows [n0, n0 + NH)
     const int hbar = 3 + hh;           // named barrier of this half's four warps
+    // this half's running state: with ALT its own maxima and accumulator
+    float* ms = m_sm + (C::ALT ? hh * 64 : 0);
+    float* mnx = m_next + (C::ALT ? hh * 64 : 0);
+    float* al = alpha_sm + (C::ALT ? hh * 64 : 0);
+    const uint32_t tm_og = tm_o + (C::ALT ? hh * N : 0);
+    constexpr int kStep = C::ALT ? 2 : 1;  // stages between this half's stages
 #pragma unroll
     for (int e = 0; e < NH; ++e) {
       l[e] = 0.f;
       zc[e] = 0.f;
     }
     const bool tree = a.tree_mask != nullptr;
-    for (int s = 0; s < n_stages; ++s) {
+    for (int s = C::ALT ? hh : 0; s < n_stages; s += kStep) {
       const int sb = s & 1, vb = s % C::NBV;
       if (ok) ok = mbar_wait(&s_full[sb], (s >> 1) & 1);
       tc_fence_after();
@@ -608,7 +621,7 @@ __global__ void __launch_bounds__(640, 1)
       bool need = false;
 #pragma unroll
       for (int e4 = 0; e4 < NH; e4 += 4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(m_sm + n0 + e4);
+        const float4 m4 = *reinterpret_cast<const float4*>(ms + n0 + e4);
         const float4 qq = *reinterpret_cast<const float4*>(qsum_sm + n0 + e4);
         const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
         const float qs[4] = {qq.x, qq.y, qq.z, qq.w};
@@ -620,44 +633,46 @@ __global__ void __launch_bounds__(640, 1)
           need |= x > mm[e] + 8.f;
         }
       }
-      // A half's four warps own the same rows, so the rescale decision and
-      // the new maxima involve only them (named barrier 3 + h).
+      // A half's four warps share one set of running maxima (the same rows
+      // of every stage, or with ALT all rows of the same stages), so the
+      // rescale decision and the new maxima involve only them (named
+      // barrier 3 + h).
       if (bar_any(hbar, 128, need)) {
         const int xw = hh * 4 + q4;  // this warp's slot in the exchange
+        float t[NH];
 #pragma unroll
-        for (int e = 0; e < NH; ++e) {
-          float t = v[e];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-          if (lane == 0) xch[xw * 64 + n0 + e] = t;
-        }
+        for (int e = 0; e < NH; ++e) t[e] = v[e];
+        const float tm = warp_reduce_split<NH>(t, lane, OpMax());  // row lane / (32 / NH)
+        if (lane % (32 / NH) == 0) xch[xw * 64 + n0 + lane / (32 / NH)] = tm;
         bar_sync_n(hbar, 128);
         const int hr = q4 * 32 + lane;  // a row of this half, for the first NH threads
         if (hr < NH) {
           const int n = n0 + hr;
           const float rm = fmaxf(fmaxf(xch[(hh * 4) * 64 + n], xch[(hh * 4 + 1) * 64 + n]),
                                  fmaxf(xch[(hh * 4 + 2) * 64 + n], xch[(hh * 4 + 3) * 64 + n]));
-          const float mo = m_sm[n];
+          const float mo = ms[n];
           const float mn = rm > mo + 8.f ? rm : mo;
-          m_next[n] = mn;
-          alpha_sm[n] = (mn == mo) ? 1.f : ex2(mo - mn);
+          mnx[n] = mn;
+          al[n] = (mn == mo) ? 1.f : ex2(mo - mn);
         }
         bar_sync_n(hbar, 128);
 #pragma unroll
         for (int e = 0; e < NH; ++e) {
-          l[e] *= alpha_sm[n0 + e];
-          zc[e] *= alpha_sm[n0 + e];
+          l[e] *= al[n0 + e];
+          zc[e] *= al[n0 + e];
         }
-        if (hr < NH) m_sm[n0 + hr] = m_next[n0 + hr];
-        if (s >= 1) {
-          // rescale this half's columns of O^T once the previous PV has landed
-          if (ok) ok = mbar_wait(&pv_done[(s - 1) & 1], ((s - 1) >> 1) & 1);
+        if (hr < NH) ms[n0 + hr] = mnx[n0 + hr];
+        if (s >= kStep) {
+          // rescale this half's columns of its O^T accumulator once the
+          // previous PV into it has landed
+          const int sp = s - kStep;
+          if (ok) ok = mbar_wait(&pv_done[sp & 1], (sp >> 1) & 1);
           tc_fence_after();
           float o[NH];
-          tmem_ld_small<NH>(tm_o + n0 + lane_off, o);
+          tmem_ld_small<NH>(tm_og + n0 + lane_off, o);
 #pragma unroll
-          for (int e = 0; e < NH; ++e) o[e] *= alpha_sm[n0 + e];
-          tmem_st_small<NH>(tm_o + n0 + lane_off, reinterpret_cast<const uint32_t*>(o));
+          for (int e = 0; e < NH; ++e) o[e] *= al[n0 + e];
+          tmem_st_small<NH>(tm_og + n0 + lane_off, reinterpret_cast<const uint32_t*>(o));
           tc_fence_before();
         }
         bar_sync_n(hbar, 128);
@@ -670,8 +685,8 @@ __global__ void __launch_bounds__(640, 1)
       uint8_t* prow = pt + sb * C::P_BYTES + kq * 128;
 #pragma unroll
       for (int u = 0; u < NH / 8; ++u) {
-        const float4 ma = *reinterpret_cast<const float4*>(m_sm + n0 + 8 * u);
-        const float4 mb = *reinterpret_cast<const float4*>(m_sm + n0 + 8 * u + 4);
+        const float4 ma = *reinterpret_cast<const float4*>(ms + n0 + 8 * u);
+        const float4 mb = *reinterpret_cast<const float4*>(ms + n0 + 8 * u + 4);
         const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
         uint32_t pk[4];
 #pragma unroll
@@ -700,22 +715,79 @@ __global__ void __launch_bounds__(640, 1)
     }
   }
   __syncthreads();  // every role is done; s_bad / s_timeout are final
-  if (soft) {
+  if (soft && C::ALT) {
+    // ---- epilogue, alternating halves: each half's row sums and corrections
+    // over its stages' keys, the two halves merged (log-sum-exp), then O^T ----
+    const int xw = hh * 4 + q4;
+    const int dd = q4 * 32 + lane;  // head dim of this thread's O^T lane
+    {
+      const float t = warp_reduce_split<NH>(l, lane, OpAdd());  // row lane / (32 / NH)
+      const float z = warp_reduce_split<NH>(zc, lane, OpAdd());
+      if (lane % (32 / NH) == 0) {
+        xch[xw * 64 + lane / (32 / NH)] = t;
+        xch2[xw * 64 + lane / (32 / NH)] = z;
+      }
+    }
+    bar_sync_n(1, 256);
+    const bool poisoned = s_bad != 0 || s_timeout != 0;
+    float* linv = alpha_sm;        // [64]
+    float* zrow = m_next;          // [64]
+    float* wa = alpha_sm + 64;     // half 0's weight per row
+    float* wb = m_next + 64;       // half 1's weight per row
+    if (st_id < R) {
+      const int n = st_id;
+      const float la = (xch[0 * 64 + n] + xch[1 * 64 + n]) + (xch[2 * 64 + n] + xch[3 * 64 + n]);
+      const float lb = (xch[4 * 64 + n] + xch[5 * 64 + n]) + (xch[6 * 64 + n] + xch[7 * 64 + n]);
+      const float za = (xch2[0 * 64 + n] + xch2[1 * 64 + n]) + (xch2[2 * 64 + n] + xch2[3 * 64 + n]);
+      const float zb = (xch2[4 * 64 + n] + xch2[5 * 64 + n]) + (xch2[6 * 64 + n] + xch2[7 * 64 + n]);
+      const float ma = m_sm[n], mb = m_sm[64 + n];
+      const float M = fmaxf(ma, mb);
+      const float wA = ex2(ma - M), wB = ex2(mb - M);
+      const float lt = wA * la + wB * lb;
+      zrow[n] = wA * za + wB * zb;
+      wa[n] = wA;
+      wb[n] = wB;
+      const long long row = static_cast<long long>(si.t0 + n / a.G) * a.Hq + g * a.G + n % a.G;
+      if (si.nparts == 1) {
+        rowoff[n] = row * D;
+        linv[n] = (poisoned || !(lt > 0.f)) ? 0.f : 1.f / lt;
+      } else {
+        rowoff[n] = (prow(row, si, a.Hq) * a.num_parts + p) * D;
+        a.pm[prow(row, si, a.Hq) * a.num_parts + p] = M;
+        a.pl[prow(row, si, a.Hq) * a.num_parts + p] = poisoned ? -1.f : lt;
+      }
+    }
+    bar_sync_n(1, 256);
+    tc_fence_after();
+    // this thread: head dim dd of rows [8h, 8h + 8), both accumulators (the
+    // second one holds nothing when the partition has a single stage)
+    const int r0 = hh * 8;
+    const bool has_b = n_stages >= 2;
+    float oa[8], ob[8];
+    tmem_ld8(tm_o + r0 + lane_off, oa);
+    tmem_ld8(tm_o + N + r0 + lane_off, ob);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int n = r0 + e;
+      if (n < R) {
+        const float o = fmaf(wa[n], oa[e], has_b ? wb[n] * ob[e] : 0.f) - zrow[n];
+        if (si.nparts > 1) a.po[rowoff[n] + dd] = o;
+        else store_out(a.out, a.out_dtype, rowoff[n] + dd, o * linv[n]);
+      }
+    }
+    tc_fence_before();
+  }
+  if (soft && !C::ALT) {
     // ---- epilogue: row sums and corrections over all keys -> output ----
     const int n0 = hh * NH;
     const int xw = hh * 4 + q4;
     const int dd = q4 * 32 + lane;  // head dim of this thread's O^T lane
-#pragma unroll
-    for (int e = 0; e < NH; ++e) {
-      float t = l[e], z = zc[e];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        t += __shfl_xor_sync(0xffffffffu, t, o);
-        z += __shfl_xor_sync(0xffffffffu, z, o);
-      }
-      if (lane == 0) {
-        xch[xw * 64 + n0 + e] = t;
-        xch2[xw * 64 + n0 + e] = z;
+    {
+      const float t = warp_reduce_split<NH>(l, lane, OpAdd());  // row n0 + lane / (32 / NH)
+      const float z = warp_reduce_split<NH>(zc, lane, OpAdd());
+      if (lane % (32 / NH) == 0) {
+        xch[xw * 64 + n0 + lane / (32 / NH)] = t;
+        xch2[xw * 64 + n0 + lane / (32 / NH)] = z;
       }
     }
     bar_sync_n(1, 256);
