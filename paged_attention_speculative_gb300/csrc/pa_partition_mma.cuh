@@ -93,6 +93,22 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
 
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Set-up that reads no input -- barriers, the tensor maps' descriptors --
+  // runs before the wait, overlapping the previous kernel's tail.
+  if (threadIdx.x == 0) {
+    s_timeout = 0;
+    s_bad = 0;
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncthreads();  // barriers ready
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so the producer starts fetching its
@@ -133,23 +149,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
   const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
   const int R = si.T * a.G;
 
-  if (threadIdx.x == 0) {
-    s_timeout = 0;
-    s_bad = 0;
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();  // barriers ready; no global loads are in front of this
-
   // =========================== producer warp ===============================
   if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
     // Stage this partition's block ids in one coalesced pass and validate
     // them.  A bad id is reported, clamped to page 0 (so every copy stays in
     // bounds) and the partition's result is discarded after the loop.

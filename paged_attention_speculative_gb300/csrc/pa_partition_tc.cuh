@@ -97,6 +97,35 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
                                        max(0LL, static_cast<long long>(a.max_blocks) - lpg)));
     for (int j = 32 * lane; j < n; j += 32 * 32) prefetch_l2(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lpg + j);
   }
+  // Set-up that reads no input -- barriers, tensor memory, the tensor maps'
+  // descriptors -- also runs before the wait.
+  if (threadIdx.x == 96) {
+    s_bad = 0;
+    s_timeout = 0;
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], GATHER ? kGatherWarps : 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 2);
+      mbar_init(&p_full[i], 2);
+      mbar_init(&pv_done[i], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (!GATHER && warp == 3 && lane == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();  // barriers and the TMEM address published
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so the producer starts fetching its
@@ -125,9 +154,11 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
                   0.f);
       }
     }
+  }
+  if (si.err || si.T <= 0 || p >= si.nparts) {
+    if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);  // nothing has used it
     return;
   }
-  if (si.T <= 0 || p >= si.nparts) return;
 
   const int kstart = si.kbase + p * a.part_tokens;
   const int kend = min(kstart + a.part_tokens, si.khi + 1);
@@ -136,34 +167,8 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
   const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
   const int R = si.T * a.G;
 
-  // ---- set-up: barriers; then the producer starts while warps 0-2
-  // allocate tensor memory and stage Q ----
-  if (threadIdx.x == 96) {
-    s_bad = 0;
-    s_timeout = 0;
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], GATHER ? kGatherWarps : 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 2);
-      mbar_init(&p_full[i], 2);
-      mbar_init(&pv_done[i], 1);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-  uint32_t tmem = 0;
+  // ---- the producer starts while warps 0-1 stage Q ----
   if (warp < 3) {
-    if (warp == 0) {
-      tmem_alloc(&s_tmem, C::TMEM_COLS);
-      tmem_relinquish();
-    }
-    tc_fence_before();
-    bar_sync_n(2, 96);  // the TMEM address is published
-    tc_fence_after();
-    tmem = s_tmem;
     if (warp < 2) {
       // Q rows into TMEM (lane = query row r = token r/G, head g*G + r%G; two
       // 16-bit elements per column), lanes R..63 zero.  Lanes 64..127 are
@@ -285,10 +290,6 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
     // no role in the gather variant
   } else if (warp == 3) {
     // =========================== TMA producer ===============================
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
     int bad = 0;
     if (prefetch) {
       cp_async_wait_all();

@@ -195,6 +195,41 @@ __global__ void __launch_bounds__(640, 1)
                                        max(0LL, static_cast<long long>(a.max_blocks) - lpg)));
     for (int j = 32 * lane; j < n; j += 32 * 32) prefetch_l2(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lpg + j);
   }
+  // Set-up that reads no input -- barriers, tensor memory, the tensor map's
+  // descriptor -- also runs before the wait.
+  if (threadIdx.x == 160) {
+    s_bad = 0;
+    s_timeout = 0;
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(&full_k[i], 1);
+      mbar_init(&full_v[i], 1);
+      mbar_init(&empty[i], 8);
+    }
+    for (int i = 0; i < C::NBK; ++i) {
+      mbar_init(&kfull[i], 8);
+      mbar_init(&kfree[i], 1);
+    }
+    for (int i = 0; i < C::NBV; ++i) {
+      mbar_init(&vfull[i], 8);
+      mbar_init(&vfree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], C::ALT ? 4 : 8);  // the softmax warps reading / writing stage s
+      mbar_init(&p_full[i], C::ALT ? 4 : 8);
+      mbar_init(&pv_done[i], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 16 && lane == 0) prefetch_tensormap(&tmK);
+  tc_fence_before();
+  __syncthreads();  // barriers and the TMEM address published
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
   pdl_wait_primary();  // inputs and outputs may belong to the previous kernel
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so its block-table slice is fetched
@@ -223,9 +258,11 @@ __global__ void __launch_bounds__(640, 1)
                   0.f);
       }
     }
+  }
+  if (si.err || si.T <= 0 || p >= si.nparts) {
+    if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);  // nothing has used it
     return;
   }
-  if (si.T <= 0 || p >= si.nparts) return;
 
   const int kstart = si.kbase + p * a.part_tokens;
   const int kend = min(kstart + a.part_tokens, si.khi + 1);
@@ -234,32 +271,6 @@ __global__ void __launch_bounds__(640, 1)
   const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
   const int R = si.T * a.G;
   const float sl2 = a.scale_log2;
-
-  if (threadIdx.x == 160) {
-    s_bad = 0;
-    s_timeout = 0;
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(&full_k[i], 1);
-      mbar_init(&full_v[i], 1);
-      mbar_init(&empty[i], 8);
-    }
-    for (int i = 0; i < C::NBK; ++i) {
-      mbar_init(&kfull[i], 8);
-      mbar_init(&kfree[i], 1);
-    }
-    for (int i = 0; i < C::NBV; ++i) {
-      mbar_init(&vfull[i], 8);
-      mbar_init(&vfree[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], C::ALT ? 4 : 8);  // the softmax warps reading / writing stage s
-      mbar_init(&p_full[i], C::ALT ? 4 : 8);
-      mbar_init(&pv_done[i], 1);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
 
   // Stage s's copies from a producer warp, one lane per page: the K records
   // (warp 16, one TMA instruction) or the V records (warp 19, one bulk
@@ -295,7 +306,6 @@ __global__ void __launch_bounds__(640, 1)
   // partition's result discarded. ----
   const int32_t* bt_row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0;
   if (warp == 16) {
-    prefetch_tensormap(&tmK);
     int bad = 0;
     if (prefetch) {
       cp_async_wait_all();
@@ -327,10 +337,6 @@ __global__ void __launch_bounds__(640, 1)
     };
     for (int s = 0; s < min(C::NS, n_stages); ++s) issue_stage(s, clamped);
     bar_sync_n(2, 64);
-  }
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, C::TMEM_COLS);
-    tmem_relinquish();
   }
   if (soft) {
     // Q rows -> f16, K-major swizzled tile (rows R..N-1 zero); then the sum of
@@ -385,11 +391,8 @@ __global__ void __launch_bounds__(640, 1)
       tree_rows[k] = rows;
     }
   }
-  // TMEM address, Q tile and row sums published to all warps
-  tc_fence_before();
+  // Q tile and row sums published to all warps
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
   const uint32_t tm_o = tmem;            // O^T accumulators: lane = head dim, column = row
   const uint32_t tm_s0 = tmem + C::NACC * N;  // S^T buffers: lane = key, column = row
   const uint32_t tm_k = tmem + C::K_COL; // K codes + 1024: lane = key, two f16 per column
