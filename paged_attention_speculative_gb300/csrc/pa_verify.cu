@@ -184,7 +184,12 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
     smem = info.smem_bytes;
     ctas_per_sm = info.ctas_per_sm;
   }
-  const long long quantum = std::max(sk, ps);
+  // Partitions are whole stages, except on the u8 tensor-memory kernel: its
+  // stages may end at a partition boundary (codes are finite and the scales
+  // of keys past the boundary are zeroed), so a page quantum evens out the
+  // bytes per CTA (32k keys on 152 CTAs: 1728 keys each, not 1792 and a
+  // short last partition).
+  const long long quantum = kernel == 4 ? ps : std::max(sk, ps);
   const long long ctx = std::max<long long>(max_ctx, 1);
   long long span = window > 0 ? std::min<long long>(ctx, static_cast<long long>(window) + tmax - 1 + ps - 1) : ctx;
   const long long units = static_cast<long long>(d->num_seqs) * d->num_kv_heads;

@@ -56,6 +56,17 @@ def test_plan_fills_the_sms_once_at_long_context(lib):
     assert 0.8 * 152 <= t.ctas <= 1.1 * 152
 
 
+def test_plan_u8_partitions_on_page_quantum(lib):
+    # the u8 tensor-memory kernel's partitions are whole pages, not whole
+    # 128-key stages: 32771 keys over 152 CTAs -> 1728 keys each (13.5 stages)
+    u = pa.plan(dims(total_tokens=3), 32771, 0, pa.PA_U8, 152)
+    assert u.kernel == 4 and u.stage_keys == 128
+    assert u.part_tokens == 1728 and u.num_partitions == 19
+    u64 = pa.plan(dims(total_tokens=1, page_size=64), 65536, 0, pa.PA_U8, 152)
+    assert u64.kernel == 4 and u64.part_tokens % 64 == 0
+    assert (u64.num_partitions - 1) * u64.part_tokens < 65536 <= u64.num_partitions * u64.part_tokens
+
+
 def test_plan_independent_of_query_count(lib):
     """The split must not collapse when a sequence brings more than one
     query token (the failure both OpenVINO issue 38153 and the
