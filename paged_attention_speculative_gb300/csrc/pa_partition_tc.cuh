@@ -489,13 +489,20 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
       tmem_st32(tm_p0 + sb * (C::SK / 2) + lane_off, reinterpret_cast<const float*>(pk));
       // V rows of keys outside every row's range may hold garbage (even NaN);
       // their weights are 0 but 0 * NaN is not: clear those rows.
+      // Thread k clears key row k (the 64 softmax threads cover the stage),
+      // its 16-byte units in an order rotated by k so that the eight threads
+      // of a store phase hit eight different bank groups.
+      static_assert(C::SK == 64, "one softmax thread per key row of the stage");
       if (key0 < si.klo || key0 + C::SK - 1 > si.khi) {
-        uint8_t* vt = smem + (s % C::NS) * C::STAGE + C::TILE;
-        for (int idx = threadIdx.x; idx < C::SK * C::CH * 8; idx += 64) {
-          const int k = idx / (C::CH * 8), rem = idx % (C::CH * 8);
-          const int key = key0 + k;
-          if (key < si.klo || key > si.khi)
-            *reinterpret_cast<uint4*>(vt + ((rem >> 3) * C::SK + k) * 128 + 16 * (rem & 7)) = make_uint4(0u, 0u, 0u, 0u);
+        const int k = threadIdx.x;
+        const int key = key0 + k;
+        if (key < si.klo || key > si.khi) {
+          uint8_t* vrow = smem + (s % C::NS) * C::STAGE + C::TILE + k * 128;
+#pragma unroll
+          for (int c = 0; c < C::CH; ++c)
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(vrow + c * C::SK * 128 + 16 * ((u + k) & 7)) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async();
