@@ -413,34 +413,24 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
 
       const int key0 = kstart + s * C::SK;
       const bool clean = key0 >= lo && key0 + C::SK - 1 <= clean_hi;
-      // tree masks: the stage's 64 keys as one validity mask per row (inside
-      // [lo, hi], and a past key or a new token the mask names), so the
-      // unrolled loop below tests one constant bit per key
+      // The stage's 64 keys as one validity mask per row (inside [lo, hi],
+      // and with a tree mask a past key or a new token the mask names), so
+      // the unrolled loop below tests one constant bit per key.
       uint64_t vmask = ~0ull;
-      if constexpr (TREE) {
-        if (!clean) {
-          const long long a0 = max(0LL, static_cast<long long>(lo) - key0);
-          const long long b0 = min(63LL, static_cast<long long>(hi) - key0);
-          const uint64_t range =
-              (a0 > b0) ? 0ull : ((b0 - a0 == 63) ? ~0ull : (((1ull << (b0 - a0 + 1)) - 1ull) << a0));
+      if (!clean) {
+        const long long a0 = max(0LL, static_cast<long long>(lo) - key0);
+        const long long b0 = min(63LL, static_cast<long long>(hi) - key0);
+        vmask = (a0 > b0) ? 0ull : ((b0 - a0 == 63) ? ~0ull : (((1ull << (b0 - a0 + 1)) - 1ull) << a0));
+        if constexpr (TREE) {
           const long long sh = static_cast<long long>(si.L) - key0;  // bit of new token 0
           const uint64_t past = sh <= 0 ? 0ull : (sh >= 64 ? ~0ull : ((1ull << sh) - 1ull));
           const uint64_t named = (sh >= 64 || sh <= -64) ? 0ull
                                  : (sh >= 0 ? (static_cast<uint64_t>(tmask) << sh)
                                             : (static_cast<uint64_t>(tmask) >> -sh));
-          vmask = range & (past | named);
+          vmask &= past | named;
         }
-      }
-      if (!clean) {
 #pragma unroll
-        for (int j = 0; j < C::SK; ++j) {
-          if constexpr (TREE) {
-            x[j] = ((vmask >> j) & 1ull) ? x[j] : -INFINITY;
-          } else {
-            const int key = key0 + j;
-            x[j] = (key >= lo && key <= hi) ? x[j] : -INFINITY;
-          }
-        }
+        for (int j = 0; j < C::SK; ++j) x[j] = ((vmask >> j) & 1ull) ? x[j] : -INFINITY;
       }
       // row max in four independent chains; scaling by sl2 > 0 commutes
       // with the max (-inf stays -inf)
