@@ -324,6 +324,33 @@ def time_graph(wl, steps, warmup, stream, min_seconds=0.0):
     return statistics.median(trials), exact, trials
 
 
+def time_steps_eager(wl, n, warmup, stream):
+    """Per-call device time (µs) of n single verify steps, each between two
+    events on the launching stream (replicas rotated so the KV cache exceeds
+    L2): the distribution the graph-replayed mean hides."""
+    import torch
+    out = []
+    with torch.cuda.stream(stream):
+        for i in range(max(1, warmup)):
+            wl.forward(i % wl.replicas, stream)
+        torch.cuda.synchronize()
+        for i in range(n):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            wl.forward(i % wl.replicas, stream)
+            e1.record(stream)
+            e1.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e3)
+    return out
+
+
+def pct(xs, q):
+    """q-th percentile (0..100) of xs, nearest rank."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q / 100.0 * (len(ys) - 1)))))]
+
+
 def time_calls(fn, replicas, stream, reps=64, trials=20):
     """Median device time (µs) of one fn(r) call: a CUDA graph of `reps`
     back-to-back calls rotating r over the replicas, replayed between two
@@ -745,6 +772,7 @@ def run_ours(args, rank, world):
         dist.barrier()
     value = whole_job_gbs(wl.kv_bytes, world, us)
 
+    eager = time_steps_eager(wl, 60, 10, stream)
     part_mean, part_med = time_partition_kernel(wl, max(args.steps, 20), stream)
     achieved = wl.kv_bytes / (part_mean * 1e-6) / 1e9
     e2e_us, h2d, d2h = time_e2e_pipelined(wl, max(args.steps, 64), args.warmup, stream)
@@ -866,8 +894,13 @@ def run_ours(args, rank, world):
                    "heads": "32q/8kv", "head_dim": 128, "page_size": 16, "kv_dtype": "bf16",
                    "l2": f"KV cache rotated over {wl.replicas} replicas ({wl.replicas * wl.total_device_bytes / 2**20:.0f}"
                          f" MiB > 2x L2)", "launch": "CUDA graph replay", "trials": len(trials)},
+        "us_per_step_trials": {"p10": pct(trials, 10), "p50": pct(trials, 50), "p90": pct(trials, 90),
+                               "n": len(trials), "what": f"graph replay, each trial the mean of {exact} steps"},
+        "us_per_call_eager": {"p10": pct(eager, 10), "p50": pct(eager, 50), "p90": pct(eager, 90), "n": len(eager),
+                              "what": "one pa_verify_forward call between two events, 10 warm-up calls"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": measured_traffic(H["name"]),
+                     "frac_of_nominal_8tbs": achieved / 8000.0,
                      "kernel": kernel_name(wl),
                      "kernel_us_mean": part_mean, "kernel_timing": "CUDA graph of back-to-back partition launches",
                      "kernel_us_median": part_med, "algorithmic_bytes_per_launch": wl.kv_bytes,
