@@ -15,6 +15,15 @@ cudaError_t launch_u8_t(const CUtensorMap& k, const PartArgs& a, dim3 grid, cuda
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !__atomic_load_n(&configured_for[dev], __ATOMIC_ACQUIRE)) {
+    if constexpr (U8Cfg<N, PS>::kRegSplit) {
+      // the warpgroups' register targets are sized for this pool: a kernel
+      // built with fewer registers per thread would wait forever in the
+      // increase, so it is never launched
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs < U8Cfg<N, PS>::kLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);

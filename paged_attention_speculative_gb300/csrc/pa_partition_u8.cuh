@@ -37,11 +37,13 @@
 //
 // Warp roles (640 threads, 20 warps; for warps 0-15, q = warp % 4 is the
 // TMEM lane quarter a warp may access and h = warp / 8 its half):
-//   warps 0-3, 8-11   softmax: thread = key 32q + lane of the stage (TMEM lane
-//                     of S^T), rows [h N/2, (h+1) N/2); head dim 32q + lane
-//                     of O^T in the epilogue; they also stage Q.  The four
-//                     warps of a half share their rows' maxima and rescale
-//                     decisions (named barrier 3 + h), not the other half.
+//   warps 0-3, 8-11   softmax: half h takes the stages s with s % 2 == h;
+//                     thread = key 32q + lane of the stage (TMEM lane of
+//                     S^T), all N rows, the half's own running maxima and
+//                     O^T accumulator (merged in the epilogue); head dim
+//                     32q + lane of O^T in the epilogue; they also stage Q.
+//                     A half's four warps share its maxima and rescale
+//                     decisions (named barrier 3 + h).
 //   warps 4-7, 12-15  converters: thread t = 32q + lane turns head dims
 //                     [64h, 64h + 64) of key t's K codes into f16 in TMEM (A
 //                     operand of S^T), turns head dim t of keys [64h,
@@ -116,13 +118,19 @@ struct U8Cfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = tk_idesc(128, N, false, false, false);
   static constexpr uint32_t IDESC_PV = tk_idesc(128, N, false, false, true);
-  // 16-row tiles: the two softmax halves take alternate stages, each over all
-  // 16 rows with its own running maxima and O^T accumulator (merged in the
-  // epilogue), so a stage's softmax chain overlaps the next one's; 32-row
-  // tiles: each half takes 16 of the rows of every stage (one accumulator).
-  static constexpr bool ALT = N == 16;
-  static constexpr int NH = ALT ? N : N / 2;           // query rows per softmax thread
-  static constexpr int NACC = ALT ? 2 : 1;             // O^T accumulators
+  // The two softmax halves take alternate stages, each over all N rows with
+  // its own running maxima and O^T accumulator (merged in the epilogue), so
+  // a stage's softmax chain overlaps the next one's.
+  static constexpr int NH = N;                         // query rows per softmax thread
+  static constexpr int NACC = 2;                       // O^T accumulators (one per softmax half)
+  // 32-row tiles: the softmax threads hold 32 rows' scores, sums and
+  // corrections, more than the 96 registers a thread has at launch, so the
+  // softmax warpgroups (warps 0-3, 8-11) take registers from the other three:
+  // 2 x 128 x 152 + 3 x 128 x 56 = 60,416 <= 640 x 96 (the launcher checks
+  // the 96).
+  static constexpr bool kRegSplit = N == 32;
+  static constexpr int kSoftRegs = 152, kOtherRegs = 56, kLaunchRegs = 96;
+  static_assert(!kRegSplit || 2 * 128 * kSoftRegs + 3 * 128 * kOtherRegs <= 640 * kLaunchRegs, "register pool");
   static_assert((NACC + 2) * N <= K_COL, "tensor-memory budget");
   static_assert(V_COL + 64 * NBV <= TMEM_COLS, "tensor-memory budget");
   static_assert(NS >= 3, "the ring needs a few stages");
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* s_free = s_full + 2;         // [2] S^T buffer read (8 softmax warps)
   uint64_t* p_full = s_free + 2;         // [2] P'^T buffer written (8 softmax warps)
   uint64_t* pv_done = p_full + 2;        // [2] PV that read that P'^T buffer done (MMA commit)
-  float* m_sm = reinterpret_cast<float*>(smem + C::MISC_OFF + 512);   // [2][64] row reference maxima (per half when ALT)
+  float* m_sm = reinterpret_cast<float*>(smem + C::MISC_OFF + 512);   // [2][64] row reference maxima (per half)
   float* xch = m_sm + 128;                                            // [8][64] per-warp row values
   float* m_next = xch + 512;                                          // [2][64]
   float* alpha_sm = m_next + 128;                                     // [2][64]
@@ -215,8 +223,8 @@ __global__ void __launch_bounds__(640, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], C::ALT ? 4 : 8);  // the softmax warps reading / writing stage s
-      mbar_init(&p_full[i], C::ALT ? 4 : 8);
+      mbar_init(&s_free[i], 4);  // the softmax half reading / writing stage s
+      mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
     }
     fence_barrier_init();
@@ -400,6 +408,10 @@ __global__ void __launch_bounds__(640, 1)
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
   bool ok = true;
 
+  // The roles part here; each ends at the kernel's two closing barriers, so
+  // that a warpgroup's register budget holds from its role to its exit.
+  if (!soft) {
+  if constexpr (C::kRegSplit) regs_decrease<C::kOtherRegs>();
   if (conv) {
     // =========================== converters =================================
     const int ct = q4 * 32 + lane;                             // key (K) and head dim (V^T), 0..127
@@ -553,7 +565,7 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
         for (int j = 0; j < C::SK / 16; ++j) {
           const uint64_t bd = sw128_desc(p_base + j * 16 * 128, 0, 1024);
-          tc_mma_ta(tm_o + (C::ALT ? (np & 1) * N : 0), tm_v + vb * 64 + 8 * j, bd, C::IDESC_PV,
+          tc_mma_ta(tm_o + (np & 1) * N, tm_v + vb * 64 + 8 * j, bd, C::IDESC_PV,
                     (np >= C::NACC || j > 0) ? 1u : 0u);
         }
         tc_commit(&pv_done[pb]);
@@ -566,26 +578,31 @@ __global__ void __launch_bounds__(640, 1)
     }
     __syncwarp();
   }
+  __syncthreads();  // every role is done
+  __syncthreads();  // the softmax warps' epilogue is done
+  return;
+  }
 
   // =========================== softmax warps (keys) ==========================
+  if constexpr (C::kRegSplit) regs_increase<C::kSoftRegs>();
   float l[NH], zc[NH];
-  if (soft) {
+  {
     const int kq = q4 * 32 + lane;     // key of the stage
-    const int n0 = C::ALT ? 0 : hh * NH;  // this thread's rows [n0, n0 + NH)
+    const int n0 = 0;                  // this thread's rows [n0, n0 + NH): all of them
     const int hbar = 3 + hh;           // named barrier of this half's four warps
-    // this half's running state: with ALT its own maxima and accumulator
-    float* ms = m_sm + (C::ALT ? hh * 64 : 0);
-    float* mnx = m_next + (C::ALT ? hh * 64 : 0);
-    float* al = alpha_sm + (C::ALT ? hh * 64 : 0);
-    const uint32_t tm_og = tm_o + (C::ALT ? hh * N : 0);
-    constexpr int kStep = C::ALT ? 2 : 1;  // stages between this half's stages
+    // this half's running state: its own maxima and accumulator
+    float* ms = m_sm + hh * 64;
+    float* mnx = m_next + hh * 64;
+    float* al = alpha_sm + hh * 64;
+    const uint32_t tm_og = tm_o + hh * N;
+    constexpr int kStep = 2;           // stages between this half's stages
 #pragma unroll
     for (int e = 0; e < NH; ++e) {
       l[e] = 0.f;
       zc[e] = 0.f;
     }
     const bool tree = a.tree_mask != nullptr;
-    for (int s = C::ALT ? hh : 0; s < n_stages; s += kStep) {
+    for (int s = hh; s < n_stages; s += kStep) {
       const int sb = s & 1, vb = s % C::NBV;
       if (ok) ok = mbar_wait(&s_full[sb], (s >> 1) & 1);
       tc_fence_after();
@@ -636,10 +653,9 @@ __global__ void __launch_bounds__(640, 1)
           need |= x > mm[e] + 8.f;
         }
       }
-      // A half's four warps share one set of running maxima (the same rows
-      // of every stage, or with ALT all rows of the same stages), so the
-      // rescale decision and the new maxima involve only them (named
-      // barrier 3 + h).
+      // A half's four warps share one set of running maxima (all rows of
+      // the half's stages), so the rescale decision and the new maxima
+      // involve only them (named barrier 3 + h).
       if (bar_any(hbar, 128, need)) {
         const int xw = hh * 4 + q4;  // this warp's slot in the exchange
         float t[NH];
@@ -718,7 +734,7 @@ __global__ void __launch_bounds__(640, 1)
     }
   }
   __syncthreads();  // every role is done; s_bad / s_timeout are final
-  if (soft && C::ALT) {
+  {
     // ---- epilogue, alternating halves: each half's row sums and corrections
     // over its stages' keys, the two halves merged (log-sum-exp), then O^T ----
     const int xw = hh * 4 + q4;
@@ -762,70 +778,22 @@ __global__ void __launch_bounds__(640, 1)
     }
     bar_sync_n(1, 256);
     tc_fence_after();
-    // this thread: head dim dd of rows [8h, 8h + 8), both accumulators (the
-    // second one holds nothing when the partition has a single stage)
-    const int r0 = hh * 8;
+    // this thread: head dim dd of rows [hN/2, (h+1)N/2), both accumulators
+    // (the second one holds nothing when the partition has a single stage)
+    constexpr int RH = N / 2;
+    const int r0 = hh * RH;
     const bool has_b = n_stages >= 2;
-    float oa[8], ob[8];
-    tmem_ld8(tm_o + r0 + lane_off, oa);
-    tmem_ld8(tm_o + N + r0 + lane_off, ob);
+    float oa[RH], ob[RH];
+    tmem_ld_small<RH>(tm_o + r0 + lane_off, oa);
+    tmem_ld_small<RH>(tm_o + N + r0 + lane_off, ob);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < RH; ++e) {
       const int n = r0 + e;
       if (n < R) {
         const float o = fmaf(wa[n], oa[e], has_b ? wb[n] * ob[e] : 0.f) - zrow[n];
         if (si.nparts > 1) a.po[rowoff[n] + dd] = o;
         else store_out(a.out, a.out_dtype, rowoff[n] + dd, o * linv[n]);
       }
-    }
-    tc_fence_before();
-  }
-  if (soft && !C::ALT) {
-    // ---- epilogue: row sums and corrections over all keys -> output ----
-    const int n0 = hh * NH;
-    const int xw = hh * 4 + q4;
-    const int dd = q4 * 32 + lane;  // head dim of this thread's O^T lane
-    {
-      const float t = warp_reduce_split<NH>(l, lane, OpAdd());  // row n0 + lane / (32 / NH)
-      const float z = warp_reduce_split<NH>(zc, lane, OpAdd());
-      if (lane % (32 / NH) == 0) {
-        xch[xw * 64 + n0 + lane / (32 / NH)] = t;
-        xch2[xw * 64 + n0 + lane / (32 / NH)] = z;
-      }
-    }
-    bar_sync_n(1, 256);
-    const bool poisoned = s_bad != 0 || s_timeout != 0;
-    float* linv = alpha_sm;
-    float* zrow = m_next;
-    if (st_id < R) {
-      const int n = st_id, hn = n / NH;
-      const float lt = (xch[(hn * 4) * 64 + n] + xch[(hn * 4 + 1) * 64 + n]) +
-                       (xch[(hn * 4 + 2) * 64 + n] + xch[(hn * 4 + 3) * 64 + n]);
-      zrow[n] = (xch2[(hn * 4) * 64 + n] + xch2[(hn * 4 + 1) * 64 + n]) +
-                (xch2[(hn * 4 + 2) * 64 + n] + xch2[(hn * 4 + 3) * 64 + n]);
-      const long long row = static_cast<long long>(si.t0 + n / a.G) * a.Hq + g * a.G + n % a.G;
-      if (si.nparts == 1) {
-        rowoff[n] = row * D;
-        linv[n] = (poisoned || !(lt > 0.f)) ? 0.f : 1.f / lt;
-      } else {
-        rowoff[n] = (prow(row, si, a.Hq) * a.num_parts + p) * D;
-        a.pm[prow(row, si, a.Hq) * a.num_parts + p] = m_sm[n];
-        a.pl[prow(row, si, a.Hq) * a.num_parts + p] = poisoned ? -1.f : lt;
-      }
-    }
-    bar_sync_n(1, 256);
-    tc_fence_after();
-    float o[NH];
-    tmem_ld_small<NH>(tm_o + n0 + lane_off, o);
-    if (si.nparts > 1) {
-#pragma unroll
-      for (int e = 0; e < NH; ++e)
-        if (n0 + e < R) a.po[rowoff[n0 + e] + dd] = o[e] - zrow[n0 + e];
-    } else {
-#pragma unroll
-      for (int e = 0; e < NH; ++e)
-        if (n0 + e < R)
-          store_out(a.out, a.out_dtype, rowoff[n0 + e] + dd, (o[e] - zrow[n0 + e]) * linv[n0 + e]);
     }
     tc_fence_before();
   }

@@ -202,12 +202,27 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
 template <int N>
 __device__ __forceinline__ void tmem_ld_small(uint32_t taddr, float* v) {
   if constexpr (N == 8) tmem_ld8(taddr, v);
-  else tmem_ld16(taddr, v);
+  else if constexpr (N == 16) tmem_ld16(taddr, v);
+  else tmem_ld32(taddr, v);
 }
 template <int N>
 __device__ __forceinline__ void tmem_st_small(uint32_t taddr, const uint32_t* r) {
   if constexpr (N == 8) tmem_st8(taddr, r);
-  else tmem_st16(taddr, r);
+  else if constexpr (N == 16) tmem_st16(taddr, r);
+  else tmem_st32(taddr, reinterpret_cast<const float*>(r));
+}
+
+// Warpgroup register re-allocation: every warp of a warpgroup executes the
+// same one.  An increase waits until the CTA's pool (threads x registers at
+// launch) has the registers, so the warpgroups' targets must sum to at most
+// that pool.
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 }  // namespace pa
