@@ -149,6 +149,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// c + a * b with f16 a, b and f32 c: the product is exact in f32 and the sum
+// is rounded once, as fmaf on the widened operands would, without widening.
+__device__ __forceinline__ float fma_f16_f32(uint16_t a_bits, uint16_t b_bits, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a_bits), "h"(b_bits), "f"(c));
+  return d;
+}
+
 // Reduces each of a lane's NV values (NV a power of two, <= 32) over the
 // warp's 32 lanes by recursive halving: at each exchange a lane keeps one half
 // of its values, sends the other half to its partner and combines what comes

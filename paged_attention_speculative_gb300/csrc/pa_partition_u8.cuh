@@ -98,7 +98,7 @@ struct U8Cfg {
   static constexpr int SIDE = SK * 16;                 // float4 per key: ks * scale * log2e, kz + 1024, vs, vz
   static constexpr int Q_BYTES = N * D * 2;            // Q tile (f16), K-major: [chunk][row][128 B]
   static constexpr int P_BYTES = SK * 128;             // P'^T tile (f16), MN-major: [key][64 row slots x 2 B]
-  static constexpr int MISC = 7168;
+  static constexpr int MISC = 7680;
   static constexpr int FIXED = NBV * SIDE + Q_BYTES + 2 * P_BYTES + 4 * kMaxPagesPerCta + MISC + 1024;
   static constexpr int NS_FIT = (226 * 1024 - FIXED) / STAGE;
   // stages in the ring; a fifth stage measured slower (every CTA's first
@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(640, 1)
   float* qsum_sm = reinterpret_cast<float*>(rowoff + 64);             // [64] sum_d of each f16 query row
   float* xch2 = qsum_sm + 64;                                         // [8][64] second exchange
   uint32_t* tree_rows = reinterpret_cast<uint32_t*>(xch2 + 512);      // [8] rows that see new token k
+  float* thr_sm = reinterpret_cast<float*>(tree_rows + 8);            // [2][64] maxima + 8: the rescale thresholds
   __shared__ uint32_t s_tmem;
   __shared__ int s_bad, s_timeout;
 
@@ -372,7 +373,10 @@ __global__ void __launch_bounds__(640, 1)
     // visible key always exceeds it by more than the rescale threshold; the
     // weights 2^(x - m) of masked keys (x = -inf) stay 0 and the rescale
     // factor 2^(floor - m) of the first rescale is 0).
-    if (st_id < 128) m_sm[st_id] = kNoMax;
+    if (st_id < 128) {
+      m_sm[st_id] = kNoMax;
+      thr_sm[st_id] = kNoMax + 8.f;
+    }
     fence_proxy_async();  // the Q tile is read by the tensor cores
     bar_sync_n(1, 256);
     if (st_id < N) {
@@ -594,6 +598,7 @@ __global__ void __launch_bounds__(640, 1)
     float* ms = m_sm + hh * 64;
     float* mnx = m_next + hh * 64;
     float* al = alpha_sm + hh * 64;
+    float* th = thr_sm + hh * 64;
     const uint32_t tm_og = tm_o + hh * N;
     constexpr int kStep = 2;           // stages between this half's stages
 #pragma unroll
@@ -617,10 +622,9 @@ __global__ void __launch_bounds__(640, 1)
 
       // Every row sees every key of the stage (the common case: past keys
       // inside every row's window and the partition) -- the same for all
-      // threads, so the per-key row mask is skipped.  Only for 16-row tiles:
-      // with 16 rows per thread the extra code spills and measured slower.
+      // threads, so the per-key row mask is skipped.
       const int k0 = kstart + s * C::SK;
-      const bool stage_clean = NH <= 8 && !tree && k0 + C::SK - 1 <= si.L && k0 + C::SK <= kend &&
+      const bool stage_clean = !tree && k0 + C::SK - 1 <= si.L && k0 + C::SK <= kend &&
                                (a.window == 0 || k0 - si.L + a.window >= si.T);
       uint32_t vrows = 0xffffffffu;
       if (!stage_clean) {
@@ -641,16 +645,16 @@ __global__ void __launch_bounds__(640, 1)
       bool need = false;
 #pragma unroll
       for (int e4 = 0; e4 < NH; e4 += 4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(ms + n0 + e4);
+        const float4 t4 = *reinterpret_cast<const float4*>(th + n0 + e4);
         const float4 qq = *reinterpret_cast<const float4*>(qsum_sm + n0 + e4);
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
         const float qs[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float x = fmaf(-sd.y, qs[e], v[e4 + e]) * sd.x;
           if (!stage_clean) x = ((vrows >> (n0 + e4 + e)) & 1u) ? x : -INFINITY;
           v[e4 + e] = x;
-          need |= x > mm[e] + 8.f;
+          need |= x > tt[e];
         }
       }
       // A half's four warps share one set of running maxima (all rows of
@@ -680,7 +684,10 @@ __global__ void __launch_bounds__(640, 1)
           l[e] *= al[n0 + e];
           zc[e] *= al[n0 + e];
         }
-        if (hr < NH) ms[n0 + hr] = mnx[n0 + hr];
+        if (hr < NH) {
+          ms[n0 + hr] = mnx[n0 + hr];
+          th[n0 + hr] = mnx[n0 + hr] + 8.f;
+        }
         if (s >= kStep) {
           // rescale this half's columns of its O^T accumulator once the
           // previous PV into it has landed
@@ -702,6 +709,7 @@ __global__ void __launch_bounds__(640, 1)
       // free once the PV two stages back has finished.
       if (s >= 2 && ok) ok = mbar_wait(&pv_done[sb], ((s >> 1) - 1) & 1);
       uint8_t* prow = pt + sb * C::P_BYTES + kq * 128;
+      const uint16_t vz_bits = __half_as_ushort(__float2half_rn(sd.w));  // the stored f16 zero-point
 #pragma unroll
       for (int u = 0; u < NH / 8; ++u) {
         const float4 ma = *reinterpret_cast<const float4*>(ms + n0 + 8 * u);
@@ -715,9 +723,8 @@ __global__ void __launch_bounds__(640, 1)
           l[i] += p0;
           l[i + 1] += p1;
           const __half2 h = __floats2half2_rn(p0 * sd.z, p1 * sd.z);
-          const float2 hr = __half22float2(h);
-          zc[i] = fmaf(hr.x, sd.w, zc[i]);
-          zc[i + 1] = fmaf(hr.y, sd.w, zc[i + 1]);
+          zc[i] = fma_f16_f32(__half_as_ushort(__low2half(h)), vz_bits, zc[i]);
+          zc[i + 1] = fma_f16_f32(__half_as_ushort(__high2half(h)), vz_bits, zc[i + 1]);
           pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
         }
         *reinterpret_cast<uint4*>(prow + swz(n0 / 8 + u, kq)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
