@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(320, 1)
     s_bad = 0;
     s_timeout = 0;
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], two ? 1 : 2);  // one producer, or K and V producers (one tile)
       mbar_init(&empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -174,12 +174,40 @@ __global__ void __launch_bounds__(320, 1)
     tmem = s_tmem;
   }
 
-  if (warp == 9) {
-    // =========================== TMA producer ===============================
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
+  // MMA issue steps (one thread each: warp 8, and warp 4 for PV with one tile)
+  // S of tile t for stage s into score buffer bi
+  auto issue_s = [&](int t, int bi, int s) {
+    const uint32_t k_base = smem_u32(ring + (s % C::NS) * C::STAGE);
+    const uint32_t q_base = smem_u32(smem + t * C::QT);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int c = kk >> 2, w = kk & 3;
+      const uint64_t ad = sw128_desc(q_base + c * 128 * 128 + 32 * w, 16, 1024);
+      const uint64_t bd = sw128_desc(k_base + c * C::SK * 128 + 32 * w, 16, 1024);
+      tc_mma(tmem + C::S_COL + bi * C::SK, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
     }
+    tc_commit(&s_full[bi]);
+  };
+  // O_t += P (buffer bi, written in phase ph) . V_s
+  auto issue_pv = [&](int t, int bi, uint32_t ph, int s) -> bool {
+    if (!mbar_wait(&p_full[bi], ph)) return false;
+    tc_fence_after();
+    const uint32_t v_base = smem_u32(ring + (s % C::NS) * C::STAGE + C::TILE);
+#pragma unroll
+    for (int j = 0; j < C::SK / 16; ++j) {
+      const uint64_t bd = sw128_desc(v_base + j * 16 * 128, C::SK * 128, 1024);
+      tc_mma_ta(tmem + t * D, tmem + C::P_COL + bi * (C::SK / 2) + 8 * j, bd, C::IDESC_PV,
+                (s > 0 || j > 0) ? 1u : 0u);
+    }
+    tc_commit(&pv_done[bi]);
+    return true;
+  };
+
+  // The stage ring's copies: K and V tiles of each page segment, one
+  // (segment, chunk) pair per lane.  With two tiles warp 9 issues both; with
+  // one, warp 9 issues K and the idle warp 5 V -- a copy instruction costs
+  // its warp hundreds of cycles, and one producer paced the ring.
+  auto produce = [&](bool do_k, bool do_v) {
     const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
     const int br_log2 = a.box_log2, br = 1 << br_log2;  // rows per tile load (page size, at most 64)
     int bad = 0;
@@ -188,6 +216,7 @@ __global__ void __launch_bounds__(320, 1)
       const int key = kstart + s * C::SK + (lane << br_log2);
       return (lane < (C::SK >> br_log2) && key < kend) ? __ldg(bt + (key >> a.ps_log2)) : 0;
     };
+    const int parts = (do_k ? 1 : 0) + (do_v ? 1 : 0);
     int nid = load_id(0);
     for (int s = 0; s < n_stages; ++s) {
       const int slot = s % C::NS;
@@ -208,54 +237,39 @@ __global__ void __launch_bounds__(320, 1)
       const int nk = min(C::SK, kend - key0);
       const int nseg = (nk + br - 1) >> br_log2;
       uint8_t* st = ring + slot * C::STAGE;
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nseg * br * D * 2 * 2));
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(parts * nseg * br * D * 2));
       __syncwarp();
       const int seg = lane / C::CH, c = lane % C::CH;  // one (segment, chunk) pair per lane: nseg * CH <= 16
       const int sid = __shfl_sync(0xffffffffu, id, seg & 31);
       if (lane < nseg * C::CH) {
         const int key = key0 + (seg << br_log2);
         const uint32_t off = static_cast<uint32_t>((c * C::SK + (seg << br_log2)) * 128);
-        tma_load_4d(st + off, &tmK, c * 64, key & (a.ps - 1), g, sid, &full[slot]);
-        tma_load_4d(st + C::TILE + off, &tmV, c * 64, key & (a.ps - 1), g, sid, &full[slot]);
+        if (do_k) tma_load_4d(st + off, &tmK, c * 64, key & (a.ps - 1), g, sid, &full[slot]);
+        if (do_v) tma_load_4d(st + C::TILE + off, &tmV, c * 64, key & (a.ps - 1), g, sid, &full[slot]);
       }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) {
       s_bad = 1;
       atomicOr(a.status, PA_STATUS_BLOCK_ID);
     }
+  };
+
+  if (warp == 9) {
+    // =========================== TMA producer ===============================
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    produce(true, two);
+  } else if (warp == 5 && !two) {
+    // ===================== V producer (one tile) ============================
+    produce(false, true);
   } else if (warp == 8) {
     // =========================== MMA issuer =================================
     // Per stage s: S_0(s); [PV_1(s-1); S_1(s)]; PV_0(s).  A stage's slot is
     // released after the last PV that reads it.
     if (lane == 0) {
       bool ok = true;
-      // S of tile t for stage s into score buffer bi
-      auto issue_s = [&](int t, int bi, int s) {
-        const uint32_t k_base = smem_u32(ring + (s % C::NS) * C::STAGE);
-        const uint32_t q_base = smem_u32(smem + t * C::QT);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int c = kk >> 2, w = kk & 3;
-          const uint64_t ad = sw128_desc(q_base + c * 128 * 128 + 32 * w, 16, 1024);
-          const uint64_t bd = sw128_desc(k_base + c * C::SK * 128 + 32 * w, 16, 1024);
-          tc_mma(tmem + C::S_COL + bi * C::SK, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[bi]);
-      };
-      // O_t += P (buffer bi, written in phase ph) . V_s
-      auto issue_pv = [&](int t, int bi, uint32_t ph, int s) -> bool {
-        if (!mbar_wait(&p_full[bi], ph)) return false;
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(ring + (s % C::NS) * C::STAGE + C::TILE);
-#pragma unroll
-        for (int j = 0; j < C::SK / 16; ++j) {
-          const uint64_t bd = sw128_desc(v_base + j * 16 * 128, C::SK * 128, 1024);
-          tc_mma_ta(tmem + t * D, tmem + C::P_COL + bi * (C::SK / 2) + 8 * j, bd, C::IDESC_PV,
-                    (s > 0 || j > 0) ? 1u : 0u);
-        }
-        tc_commit(&pv_done[bi]);
-        return true;
-      };
       if (two) {
         // two tiles, one buffer each (index t, phase s & 1):
         // S_0(s); PV_1(s-1); S_1(s); PV_0(s)
@@ -283,8 +297,10 @@ __global__ void __launch_bounds__(320, 1)
           if (ok) tc_commit(&empty[(n_stages - 1) % C::NS]);
         }
       } else {
-        // one tile, two buffers (index s & 1, phase (s >> 1) & 1):
-        // S(s) before PV(s-1), so the tensor cores work during the softmax
+        // one tile, two buffers (index s & 1, phase (s >> 1) & 1): this
+        // thread issues the scores only, as soon as the stage has landed
+        // and its buffer is read; warp 4 issues the PVs, so a score MMA
+        // never waits behind a PV for the softmax
         for (int s = 0; s < n_stages && ok; ++s) {
           const int sb = s & 1;
           if (!mbar_wait(&full[s % C::NS], (s / C::NS) & 1) ||
@@ -294,15 +310,21 @@ __global__ void __launch_bounds__(320, 1)
           }
           tc_fence_after();
           issue_s(0, sb, s);
-          if (s >= 1) {
-            if (!(ok = issue_pv(0, (s - 1) & 1, ((s - 1) >> 1) & 1, s - 1))) break;
-            tc_commit(&empty[(s - 1) % C::NS]);
-          }
         }
-        if (ok && n_stages >= 1) {
-          ok = issue_pv(0, (n_stages - 1) & 1, ((n_stages - 1) >> 1) & 1, n_stages - 1);
-          if (ok) tc_commit(&empty[(n_stages - 1) % C::NS]);
-        }
+      }
+      if (!ok) {
+        atomicOr(a.status, PA_STATUS_TIMEOUT);
+        atomicOr(&s_timeout, 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 4 && !two) {
+    // ===================== PV issuer (one tile) =============================
+    if (lane == 0) {
+      bool ok = true;
+      for (int s = 0; s < n_stages && ok; ++s) {
+        ok = issue_pv(0, s & 1, (s >> 1) & 1, s);
+        if (ok) tc_commit(&empty[s % C::NS]);  // its score MMA finished before the softmax began
       }
       if (!ok) {
         atomicOr(a.status, PA_STATUS_TIMEOUT);
