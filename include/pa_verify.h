@@ -320,6 +320,21 @@ int pa_forward_mixed(const void* q, const void* k_cache, const void* v_cache, co
                      float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
                      void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/*
+ * pa_forward_mixed_tree — pa_forward_mixed whose verify steps are trees of
+ * draft tokens: a sequence with T_b <= 8 sees its own new tokens through
+ * tree_mask exactly as in pa_verify_forward_tree; prefill chunks (T_b > 8)
+ * keep the causal chain and their tree_mask entries are not read.
+ *
+ *  tree_mask  device uint8 [total_tokens], as for pa_verify_forward_tree.
+ *
+ * Other arguments, errors and the workspace as for pa_forward_mixed;
+ * PA_ERR_NULL if tree_mask is NULL. */
+int pa_forward_mixed_tree(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                          float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                          void* workspace, size_t workspace_bytes, const uint8_t* tree_mask, void* cuda_stream);
+
 /* Synchronises cuda_stream, then reads and clears the workspace's status word
  * into *bits (PA_STATUS_* flags, 0 = clean). */
 int pa_verify_get_device_status(void* workspace, void* cuda_stream, uint32_t* bits);

@@ -8,8 +8,9 @@ fallback: if the library is missing, loading raises.
 
 Entry points mirror the C ABI:
   forward / forward_traced / forward_tree / partition / combine / workspace_size / plan /
-  device_status / status_string, and cache_update (the step before the
-  verify: the new tokens' K/V written into their pages)
+  device_status / status_string, forward_mixed / forward_mixed_tree (verify
+  steps and prefill chunks in one call), and cache_update (the step before
+  the verify: the new tokens' K/V written into their pages)
 Tensors are torch CUDA tensors (torch supplies device memory and streams).
 """
 from __future__ import annotations
@@ -20,7 +21,8 @@ import threading
 
 __all__ = ["PA_F32", "PA_F16", "PA_BF16", "PA_U8", "PaDims", "PaPlan", "load_library", "library_path",
            "forward", "forward_traced", "partition", "combine", "workspace_size", "plan", "device_status",
-           "status_string", "dims_for", "cache_update", "forward_tree", "PaVerifyError"]
+           "status_string", "dims_for", "cache_update", "forward_tree", "forward_mixed", "forward_mixed_tree",
+           "PaVerifyError"]
 
 PA_F32, PA_F16, PA_BF16, PA_U8 = 0, 1, 2, 3
 PA_MAX_QUERY_LEN = 8
@@ -29,7 +31,7 @@ STATUS_BITS = {0x1: "QUERY_LEN", 0x2: "CONTEXT", 0x4: "BLOCK_ID", 0x8: "BEGINS",
 EXPORTED = ["pa_verify_workspace_size", "pa_verify_plan", "pa_verify_forward", "pa_verify_forward_traced",
             "pa_verify_partition", "pa_verify_combine", "pa_verify_get_device_status", "pa_verify_status_string",
             "pa_verify_forward_no_alloc", "pa_cache_update", "pa_verify_forward_tree", "pa_mixed_workspace_size",
-            "pa_forward_mixed"]
+            "pa_forward_mixed", "pa_forward_mixed_tree"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -99,6 +101,8 @@ def load_library():
         lib.pa_mixed_workspace_size.restype = sz
         lib.pa_forward_mixed.argtypes = fwd
         lib.pa_forward_mixed.restype = ctypes.c_int
+        lib.pa_forward_mixed_tree.argtypes = fwd[:14] + [vp, vp]
+        lib.pa_forward_mixed_tree.restype = ctypes.c_int
         lib.pa_cache_update.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, vp, dp,
                                         vp, vp]
         lib.pa_cache_update.restype = ctypes.c_int
@@ -239,6 +243,16 @@ def forward_mixed(q, k_cache, v_cache, block_tables, past_lens, subsequence_begi
     _check(load_library().pa_forward_mixed(*_fwd_args(q, k_cache, v_cache, block_tables, past_lens,
                                                       subsequence_begins, max_context_len, scale, sliding_window,
                                                       kv_dtype, out, dims, workspace, stream)), "pa_forward_mixed")
+    return out
+
+
+def forward_mixed_tree(q, k_cache, v_cache, block_tables, past_lens, subsequence_begins, max_context_len, scale,
+                       sliding_window, kv_dtype, out, dims: PaDims, workspace, tree_mask, stream=None):
+    """pa_forward_mixed_tree: forward_mixed with the verify steps' new tokens
+    seeing each other through tree_mask (prefill chunks stay causal)."""
+    args = _fwd_args(q, k_cache, v_cache, block_tables, past_lens, subsequence_begins, max_context_len, scale,
+                     sliding_window, kv_dtype, out, dims, workspace, stream)
+    _check(load_library().pa_forward_mixed_tree(*args[:14], _ptr(tree_mask), args[14]), "pa_forward_mixed_tree")
     return out
 
 

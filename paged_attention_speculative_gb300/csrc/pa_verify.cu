@@ -546,6 +546,7 @@ int launch_prefill(const Call& c, const pa_plan& plan, const Workspace& w) {
   const pa_dims* d = c.d;
   PartArgs a = part_args(c, plan, w);
   a.role = pa::kRoleLong;
+  a.tree_mask = nullptr;  // prefill chunks follow the causal chain
   cudaError_t e;
   if (c.kv == PA_F32) {
     a.part_tokens = 1 << 30;  // one partition: the output row directly
@@ -706,6 +707,17 @@ int pa_forward_mixed(const void* q, const void* k_cache, const void* v_cache, co
   const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
                max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
                static_cast<cudaStream_t>(cuda_stream), nullptr};
+  return run_mixed(c);
+}
+
+int pa_forward_mixed_tree(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          const int32_t* past_lens, const int32_t* subsequence_begins, int32_t max_context_len,
+                          float scale, int32_t sliding_window, pa_dtype kv_dtype, void* out, const pa_dims* dims,
+                          void* workspace, size_t workspace_bytes, const uint8_t* tree_mask, void* cuda_stream) {
+  if (tree_mask == nullptr) return PA_ERR_NULL;
+  const Call c{q,     k_cache,        v_cache, block_tables, past_lens, subsequence_begins,
+               max_context_len, scale, sliding_window, kv_dtype, out, dims, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(cuda_stream), nullptr, tree_mask};
   return run_mixed(c);
 }
 

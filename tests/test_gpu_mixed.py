@@ -124,3 +124,66 @@ def test_context_overflow_in_a_prefill_chunk_sets_the_status():
     got, bits, _ = run_mixed(case, max_context_len=220)
     assert bits & 0x2  # PA_STATUS_CONTEXT
     assert np.all(got[2:] == 0.0)
+
+
+def _sub_case(case, seqs):
+    """The sub-batch of `case` holding sequences `seqs` (same caches and block
+    tables), with the token map back into the full batch."""
+    import dataclasses
+    sb = case.subsequence_begins
+    rows, begins = [], [0]
+    for b in seqs:
+        rows.extend(range(int(sb[b]), int(sb[b + 1])))
+        begins.append(begins[-1] + int(sb[b + 1] - sb[b]))
+    sub = dataclasses.replace(case, q=case.q[rows], block_tables=case.block_tables[list(seqs)],
+                              past_lens=case.past_lens[list(seqs)],
+                              subsequence_begins=np.asarray(begins, dtype=np.int32))
+    return sub, rows
+
+
+@pytest.mark.parametrize("idx", [1, 3, 7])
+def test_mixed_tree_masks(idx):
+    """pa_forward_mixed_tree: the verify steps' draft tokens see each other
+    through random tree masks, the prefill chunks stay causal (their mask
+    entries are set to all ones and must not be read).  Expected: the
+    oracle's tree definition on the verify sequences, its causal definition
+    on the prefill ones."""
+    import torch
+    make, derived = CASES[idx]
+    case = make()
+    # masks for the verify sequences only; prefill tokens get 0xff (ignored)
+    rng = np.random.default_rng(400 + idx)
+    mask = np.full(case.total_tokens, 0xFF, dtype=np.uint8)
+    verify = [b for b in range(case.num_seqs) if 0 < int(case.query_lens[b]) <= 8]
+    prefill = [b for b in range(case.num_seqs) if int(case.query_lens[b]) > 8]
+    for b in verify:
+        t0 = int(case.subsequence_begins[b])
+        for i in range(int(case.query_lens[b])):
+            parent = -1 if i == 0 else int(rng.integers(-1, i))
+            mask[t0 + i] = (1 << i) | (mask[t0 + parent] if parent >= 0 else 0)
+    dev = to_device(case)
+    d = dims(case, dev)
+    kvc = KV_CODE[case.kv_dtype]
+    ws = pa.alloc_mixed_workspace(d, case.max_context_len, case.sliding_window, kvc)
+    pa.forward_mixed_tree(dev["q"], dev["k"], dev["v"], dev["bt"], dev["pl"], dev["sb"], case.max_context_len,
+                          case.scale, case.sliding_window, kvc, dev["out"], d, ws, torch.from_numpy(mask).cuda())
+    torch.cuda.synchronize()
+    assert pa.device_status(ws) == 0
+    got = dev["out"].float().cpu().numpy().astype(np.float64)
+    want = np.zeros_like(got)
+    for seqs, tree in ((verify, True), (prefill, False)):
+        if not seqs:
+            continue
+        sub, rows = _sub_case(case, seqs)
+        kw = dict(num_q_heads=sub.num_q_heads, num_kv_heads=sub.num_kv_heads, head_dim=sub.head_dim,
+                  page_size=sub.page_size, num_blocks=sub.num_blocks, scale=sub.scale,
+                  sliding_window=sub.sliding_window)
+        want[rows] = oracle.forward(sub.q, sub.q_dtype, sub.k_cache, sub.v_cache, sub.kv_dtype, sub.block_tables,
+                                    sub.past_lens, sub.subsequence_begins, tree_mask=mask[rows] if tree else None,
+                                    **kw)
+    err = max_abs_err(got, want)
+    if derived:
+        worst = float(np.max(np.abs(got - want) - derived_tolerance(case, want)))
+        assert worst <= 0.0, f"{case.name}: exceeds the derived bound by {worst:.3e} (max abs {err:.3e})"
+    else:
+        assert err <= TOL, f"{case.name}: max abs err {err:.3e}"
