@@ -219,14 +219,16 @@ def mixed_sweep(stream, hbm_peak, l2):
 
 
 def small_page_sweep(stream, hbm_peak, l2):
-    """The same verify step with the cache in 16-token pages and in 1-, 2- or
-    4-token pages (one block-table lookup per key at page size 1)."""
+    """The same verify step with the cache in 16-token (head_dim 256: 64-token)
+    pages and in 1-, 2- or 4-token pages (one block-table lookup per key at
+    page size 1)."""
     import torch
     rows = []
     for name, hq, hkv, d, T, L, sizes in (("long_T8_L131072", 64, 8, 128, 8, 131072, (16, 4, 2, 1)),
                                           ("long_T8_L184320", 64, 8, 128, 8, 184320, (16, 1)),
                                           ("qwen_gqa_T4_L32768", 32, 8, 128, 4, 32768, (16, 1)),
-                                          ("qwen_gqa_T1_L32768", 32, 8, 128, 1, 32768, (16, 1))):
+                                          ("qwen_gqa_T1_L32768", 32, 8, 128, 1, 32768, (16, 1)),
+                                          ("gemma_global_T2_L32768", 32, 16, 256, 2, 32768, (64, 4, 1))):
         base = None
         for ps in sizes:
             w = DeviceWorkload(hq, hkv, d, ps, "bf16", [T], [L], 0, min_bytes=2 * l2, seed=13)
@@ -273,6 +275,8 @@ def kernel_name(wl) -> str:
         return f"pa_partition_u8<N={p.row_tiles}, page {wl.ps}> (tcgen05, keys on M, u8 codes converted into TMEM)"
     if p.kernel == 1:
         return f"pa_partition_f32<D={wl.D}>"
+    if wl.ps < 8:
+        return f"pa_partition_mma<D={wl.D},{wl.kv},gather> (mma.sync, one bulk copy per key row)"
     return f"pa_partition_mma<D={wl.D}, {wl.kv}, n-tiles={p.row_tiles}> (mma.sync)"
 
 
@@ -925,9 +929,11 @@ def run_ours(args, rank, world):
 
 
 # Workloads the ncu summaries of the other kernels are taken on: the
-# cp.async page gather (one token per page) and a prefill chunk alone.
+# page gathers (one token per page), a prefill chunk alone, and others.
 PROFILE_EXTRA = {
     "long_T8_L131072_ps1": dict(Hq=64, Hkv=8, D=128, ps=1, kv="bf16", q_lens=[8], past=[131072], window=0),
+    # head_dim 256 in one-token pages: the warp-level kernel's per-key bulk copies
+    "gemma_global_T2_L32768_ps1": dict(Hq=32, Hkv=16, D=256, ps=1, kv="bf16", q_lens=[2], past=[32768], window=0),
     # u8 with 64 query rows per KV head: the warp-level kernel's u8 path
     "long_u8_T8_L32768": dict(Hq=64, Hkv=8, D=128, ps=16, kv="u8", q_lens=[8], past=[32768], window=0),
     # the cache update before each verify step (64 sequences of 4 new tokens)

@@ -64,11 +64,10 @@ enum {
   PA_ERR_SHAPE = -3,       /* non-positive count, Hq % Hkv != 0, bad table width  */
   PA_ERR_HEAD_DIM = -4,    /* head_dim not in {64, 128, 256} (u8: {128, 256})     */
   PA_ERR_PAGE_SIZE = -5,   /* page_size not a power of two in [1, 256]; pages of
-                              1, 2 or 4 tokens need an fp32 cache, or a 16-bit
-                              cache with head_dim <= 128 and <= 64 query rows
-                              per KV head; u8 caches need pages of 16 tokens
-                              or more (pa_cache_update: any power of two up
-                              to 256)                                         */
+                              1, 2 or 4 tokens need an fp32 or a 16-bit cache
+                              (head_dim <= 128: <= 64 query rows per KV head);
+                              u8 caches need pages of 16 tokens or more
+                              (pa_cache_update: any power of two up to 256)  */
   PA_ERR_ALIGN = -6,       /* a pointer misses its alignment                      */
   PA_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than pa_verify_workspace_size */
   PA_ERR_CONTEXT = -8,     /* max_context_len < 1 while tokens are present, or too large */
@@ -115,9 +114,10 @@ typedef struct {
                               rows per KV head), 4 = tensor-memory path for u8 KV,
                               keys on the MMA's M dimension (D = 128, pages of
                               16 / 32 / 64 tokens, up to 32 query rows).
-                              Pages of 1, 2 or 4 tokens with 16-bit KV always
-                              take kernel 2, gathering key rows with 16-byte
-                              cp.async copies instead of TMA boxes            */
+                              Pages of 1, 2 or 4 tokens with 16-bit KV take
+                              kernel 2 (D <= 128), gathering key rows with
+                              16-byte cp.async copies instead of TMA boxes, or
+                              kernel 0 (D = 256), one bulk copy per key row  */
   int32_t num_sms;         /* SM count the plan was made for                       */
   int32_t ctas;            /* grid size B * Hkv * P                                */
   int32_t smem_bytes;      /* dynamic shared memory per partition CTA             */

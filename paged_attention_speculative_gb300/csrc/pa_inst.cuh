@@ -6,16 +6,17 @@
 
 namespace pa {
 
-template <int D, int KV, int NT>
+template <int D, int KV, int NT, bool GATHER = false>
 MmaKernelInfo mma_info_t() {
-  return MmaKernelInfo{MmaCfg<D, KV>::SK, MmaSmem<D, KV, NT>::BYTES, MmaSmem<D, KV, NT>::CTAS_PER_SM};
+  using S = MmaSmem<D, KV, NT, GATHER>;
+  return MmaKernelInfo{MmaCfg<D, KV, GATHER>::SK, S::BYTES, S::CTAS_PER_SM};
 }
 
-template <int D, int KV, int NT, bool TREE>
+template <int D, int KV, int NT, bool TREE, bool GATHER = false>
 cudaError_t launch_mma_tt(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                           cudaStream_t st) {
-  auto kern = pa_partition_mma<D, KV, NT, TREE>;
-  const int smem = MmaSmem<D, KV, NT>::BYTES;
+  auto kern = pa_partition_mma<D, KV, NT, TREE, GATHER>;
+  const int smem = MmaSmem<D, KV, NT, GATHER>::BYTES;
   // Raise the dynamic shared-memory limit once per process and device.
   static int configured_for[64] = {0};
   int dev = 0;
@@ -31,11 +32,11 @@ cudaError_t launch_mma_tt(const CUtensorMap& k, const CUtensorMap& v, const Part
 
 // Tree-mask verify runs its own instantiation, so the causal kernels keep
 // their code.
-template <int D, int KV, int NT>
+template <int D, int KV, int NT, bool GATHER = false>
 cudaError_t launch_mma_t(const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                          cudaStream_t st) {
-  return a.tree_mask != nullptr ? launch_mma_tt<D, KV, NT, true>(k, v, a, grid, st)
-                                : launch_mma_tt<D, KV, NT, false>(k, v, a, grid, st);
+  return a.tree_mask != nullptr ? launch_mma_tt<D, KV, NT, true, GATHER>(k, v, a, grid, st)
+                                : launch_mma_tt<D, KV, NT, false, GATHER>(k, v, a, grid, st);
 }
 
 }  // namespace pa

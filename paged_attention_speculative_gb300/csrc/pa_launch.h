@@ -48,6 +48,10 @@ cudaError_t launch_mma_d128(int kv, int nt, const CUtensorMap& k, const CUtensor
                             cudaStream_t st);
 cudaError_t launch_mma_d256(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                             cudaStream_t st);
+// head_dim 256, 16-bit caches, pages of 1, 2 or 4 tokens (one n-tile per
+// warp): each key's K and V rows arrive by a bulk copy of their own.
+MmaKernelInfo mma_info_d256_gather(int kv, bool* ok);
+cudaError_t launch_mma_d256_gather(int kv, const PartArgs& a, dim3 grid, cudaStream_t st);
 
 // Tensor-memory (tcgen05) partition kernels: head_dim 64 / 128 with KV_BF16 /
 // KV_F16 caches.

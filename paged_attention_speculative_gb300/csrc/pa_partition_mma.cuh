@@ -21,6 +21,14 @@
 // and O^T[d, row] += V^T . P^T.  The warps' states merge through shared
 // memory at the end.
 //
+// Pages of 1, 2 or 4 tokens (16-bit caches, head_dim 256): no TMA box fits a
+// swizzle atom, so the producer copies each key's K and V rows with a 1-D bulk
+// copy of their own (one key per lane, the block id looked up a stage ahead)
+// into rows padded by 16 bytes instead of swizzled; the pad spreads the eight
+// rows an ldmatrix phase reads over all 32 banks.  The magik.net article
+// ("The Hypothesis: page_size=1 Scatter-Gather") is the case: every key is its
+// own block-table lookup, and each lookup still feeds a whole-row copy.
+//
 // u8 caches: codes are exact in f16 (code = f16(0x6400 | code) - 1024), so
 // q.K = scale_j (q.code_j - zp_j sum(q)) and the value sum is
 // sum_j p_j scale_j code_j - sum_j p_j scale_j zp_j — the dequantisation costs
@@ -34,7 +42,7 @@
 
 namespace pa {
 
-template <int D, int KV>
+template <int D, int KV, bool GATHER = false>
 struct MmaCfg {
   static constexpr bool kU8 = (KV == KV_U8);
   static constexpr bool kBf16 = (KV == KV_BF16);       // u8 math runs in f16
@@ -43,7 +51,8 @@ struct MmaCfg {
   static constexpr int CHUNKS = ROW_BYTES / 128;       // 128-byte swizzle rows per key
   static constexpr int ELEMS_128 = 128 / EB;           // elements per 128-byte row
   static constexpr int SK = (ROW_BYTES >= 512) ? 32 : 64;  // keys per pipeline stage
-  static constexpr int TILE = SK * ROW_BYTES;          // bytes of one K (or V) stage tile
+  static constexpr int PITCH = GATHER ? ROW_BYTES + 16 : ROW_BYTES;  // bytes between keys' rows
+  static constexpr int TILE = SK * PITCH;              // bytes of one K (or V) stage tile
   static constexpr int SZ = kU8 ? SK * 2 : 0;          // one fp16 scale (or zp) array
   // stages start on 1024-byte boundaries: the 128-byte swizzle pattern is a
   // function of the shared-memory address bits 7..9
@@ -53,11 +62,12 @@ struct MmaCfg {
   static constexpr int MTILES = D / 16;
   static constexpr int CHUNKS_PER_STAGE = SK / 16;
   static_assert(CHUNKS >= 1, "head_dim too small for the swizzled layout");
+  static_assert(!(GATHER && kU8), "u8 V pages are dim-major: no per-key gather");
 };
 
-template <int D, int KV, int NT>
+template <int D, int KV, int NT, bool GATHER = false>
 struct MmaSmem {
-  using C = MmaCfg<D, KV>;
+  using C = MmaCfg<D, KV, GATHER>;
   static constexpr int RPW = 8 * NT;                   // rows per consumer warp
   static constexpr int CTAS_PER_SM = (NT == 2) ? 1 : 2;  // register budget of the launch bounds
   static constexpr int MERGE_LD = D + 4;
@@ -74,12 +84,12 @@ __device__ __forceinline__ int out_dim(int mt, int m) {
   return 16 * mt + m;
 }
 
-template <int D, int KV, int NT, bool TREE = false>
+template <int D, int KV, int NT, bool TREE = false, bool GATHER = false>
 __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     pa_partition_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const PartArgs a) {
-  using C = MmaCfg<D, KV>;
-  using S = MmaSmem<D, KV, NT>;
+  using C = MmaCfg<D, KV, GATHER>;
+  using S = MmaSmem<D, KV, NT, GATHER>;
   constexpr bool kBf = C::kBf16;
   constexpr int RPW = S::RPW;
 
@@ -104,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     }
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (!GATHER && warp == kConsumerWarps && lane == 0) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
@@ -113,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
   // Without a window a partition's first page is p * part_tokens / page_size
   // whatever the sequence's length, so the producer starts fetching its
   // block-table slice before the sequence's bounds are known.
-  const bool prefetch = (warp == kConsumerWarps && a.window == 0);
+  const bool prefetch = (!GATHER && warp == kConsumerWarps && a.window == 0);
   if (prefetch) {
     const long long lpg = (static_cast<long long>(p) * a.part_tokens) >> a.ps_log2;
     const int n = static_cast<int>(min(static_cast<long long>(a.part_tokens >> a.ps_log2),
@@ -151,102 +161,170 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
 
   // =========================== producer warp ===============================
   if (warp == kConsumerWarps) {
-    // Stage this partition's block ids in one coalesced pass and validate
-    // them.  A bad id is reported, clamped to page 0 (so every copy stays in
-    // bounds) and the partition's result is discarded after the loop.
-    int bad = 0;
-    if (prefetch) {
-      cp_async_wait_all();
-      __syncwarp();
-    }
-    for (int j = lane; j < npages; j += 32) {
-      int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
-      if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
-        bad = 1;
-        id = 0;
+    if constexpr (GATHER) {
+      // One key per lane: validate its block id (a bad one is reported,
+      // clamped to page 0 and the partition's result discarded), then copy
+      // the key's K and V rows whole.  The next stage's ids are loaded before
+      // this stage waits for its slot, so the lookups overlap the ring.
+      constexpr int KPL = (C::SK + 31) / 32;  // keys per lane and stage
+      const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
+      int idn[KPL];
+#pragma unroll
+      for (int u = 0; u < KPL; ++u) {
+        const int key = kstart + lane + 32 * u;
+        idn[u] = (lane + 32 * u < C::SK && key < kend) ? __ldg(bt + (key >> a.ps_log2)) : 0;
       }
-      blk[j] = id;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) {
-      s_bad = 1;  // published to the consumers by the first full-barrier arrive
-      atomicOr(a.status, PA_STATUS_BLOCK_ID);
-    }
-    __syncwarp();
-    const int br_log2 = a.box_log2;
-    const int br = 1 << br_log2;
-    int issued = 0;
-    bool ok = true;
-    for (int s = 0; s < n_stages; ++s) {
-      const int slot = s % C::NS;
-      if (s >= C::NS && !mbar_wait(&empty[slot], ((s / C::NS) - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      const int key0 = kstart + s * C::SK;
-      const int nk = min(C::SK, kend - key0);
-      const int nseg = (nk + br - 1) >> br_log2;
-      uint32_t bytes = static_cast<uint32_t>(nseg * br * C::ROW_BYTES * 2);
-      if constexpr (C::kU8) bytes += static_cast<uint32_t>(nseg * br * 2 * 4);
-      uint8_t* st = smem + slot * C::STAGE;
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
-      __syncwarp();
-      // one copy per lane: a copy instruction costs its thread hundreds of
-      // cycles, so copies issued by one lane in a row would pace the stream
-      const int nt = nseg * C::CHUNKS;
-      // K: CHUNKS boxes per segment; V: the same, or for u8 one dim-major
-      // [head dim][key] box per segment
-      const int nv = C::kU8 ? nseg : nt;
-      int ncopy = nt + nv;
-      if constexpr (C::kU8) ncopy += nseg * (br == a.ps ? 2 : 4);
-      for (int c = lane; c < ncopy; c += 32) {
-        if (C::kU8 && c >= nt && c < nt + nv) {
-          const int seg = c - nt;
-          const int key = key0 + (seg << br_log2);
-          const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
-          const int id = blk[lp - lp0];
-          tma_load_4d(st + C::TILE + seg * (D << br_log2), &tmV, slot0, 0, g, id, &full[slot]);
-        } else if (c < (C::kU8 ? nt : 2 * nt)) {
-          const bool is_v = c >= nt;
-          const int j = is_v ? c - nt : c;
-          const int seg = j / C::CHUNKS, ch = j % C::CHUNKS;
-          const int key = key0 + (seg << br_log2);
-          const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
-          const int id = blk[lp - lp0];
-          const uint32_t off = static_cast<uint32_t>(((seg * C::CHUNKS + ch) << br_log2) * 128);
-          tma_load_4d(st + (is_v ? C::TILE : 0) + off, is_v ? &tmV : &tmK, ch * C::ELEMS_128, slot0, g, id, &full[slot]);
-          if (!is_v && a.trace != nullptr && ch == 0 && slot0 == 0)
-            atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
-        } else if constexpr (C::kU8) {
-          // per segment [scales(br) | zero-points(br)]; one copy per cache
-          // when the segment is a whole page (the record keeps both arrays
-          // adjacent), else scales and zero-points separately
-          const size_t rec = static_cast<size_t>(a.ps) * (D + 4);
-          const int idx = c - nt - nv;
-          const bool whole = (br == a.ps);
-          const int seg = whole ? idx >> 1 : idx >> 2;
-          const bool is_v = whole ? (idx & 1) != 0 : (idx & 2) != 0;
-          const int part = whole ? 0 : (idx & 1);  // 0: scales, 1: zero-points
-          const int key = key0 + (seg << br_log2);
-          const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
-          const int id = blk[lp - lp0];
-          const size_t roff = (static_cast<size_t>(id) * a.Hkv + g) * rec + static_cast<size_t>(a.ps) * D;
-          uint8_t* dst = st + 2 * C::TILE + seg * 4 * br + (is_v ? 4 * C::SK : 0);
-          const uint8_t* src = (is_v ? a.v_bytes : a.k_bytes) + roff;
-          if (whole) bulk_load(dst, src, 4 * br, &full[slot]);
-          else bulk_load(dst + 2 * br * part, src + 2 * a.ps * part + 2 * slot0, 2 * br, &full[slot]);
+      int issued = 0;
+      bool ok = true;
+      for (int s = 0; s < n_stages; ++s) {
+        const int slot = s % C::NS;
+        const int key0 = kstart + s * C::SK;
+        const int nk = min(C::SK, kend - key0);
+        int id[KPL];
+        int bad = 0;
+#pragma unroll
+        for (int u = 0; u < KPL; ++u) {
+          id[u] = idn[u];
+          if (lane + 32 * u < nk && static_cast<unsigned>(id[u]) >= static_cast<unsigned>(a.num_blocks)) {
+            bad = 1;
+            id[u] = 0;
+          }
+          const int nkey = key0 + C::SK + lane + 32 * u;
+          idn[u] = (lane + 32 * u < C::SK && nkey < kend) ? __ldg(bt + (nkey >> a.ps_log2)) : 0;
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) {
+          s_bad = 1;  // published to the consumers by this stage's full-barrier arrive
+          atomicOr(a.status, PA_STATUS_BLOCK_ID);
+        }
+        if (s >= C::NS && !mbar_wait(&empty[slot], ((s / C::NS) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + slot * C::STAGE;
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nk * 2 * C::ROW_BYTES));
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < KPL; ++u) {
+          const int j = lane + 32 * u;
+          if (j < nk) {
+            const int key = key0 + j;
+            const size_t off =
+                ((static_cast<size_t>(id[u]) * a.Hkv + g) * a.ps + (key & (a.ps - 1))) * C::ROW_BYTES;
+            bulk_load(st + j * C::PITCH, a.k_bytes + off, C::ROW_BYTES, &full[slot]);
+            bulk_load(st + C::TILE + j * C::PITCH, a.v_bytes + off, C::ROW_BYTES, &full[slot]);
+            if (a.trace != nullptr && (key & (a.ps - 1)) == 0)
+              atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + (key >> a.ps_log2),
+                        id[u] + 1);
+          }
+        }
+        issued = s + 1;
       }
-      issued = s + 1;
-    }
-    if (!ok) {
-      if (lane == 0) {
-        atomicOr(a.status, PA_STATUS_TIMEOUT);
-        atomicOr(&s_timeout, 1);
+      if (!ok) {
+        if (lane == 0) {
+          atomicOr(a.status, PA_STATUS_TIMEOUT);
+          atomicOr(&s_timeout, 1);
+        }
+        for (int s = max(0, issued - C::NS); s < issued; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
       }
-      // let the copies already in flight land before the CTA can retire
-      for (int s = max(0, issued - C::NS); s < issued; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
+      return;
+    } else {
+      // Stage this partition's block ids in one coalesced pass and validate
+      // them.  A bad id is reported, clamped to page 0 (so every copy stays in
+      // bounds) and the partition's result is discarded after the loop.
+      int bad = 0;
+      if (prefetch) {
+        cp_async_wait_all();
+        __syncwarp();
+      }
+      for (int j = lane; j < npages; j += 32) {
+        int id = prefetch ? blk[j] : __ldg(a.block_tables + static_cast<size_t>(b) * a.max_blocks + lp0 + j);
+        if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+          bad = 1;
+          id = 0;
+        }
+        blk[j] = id;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        s_bad = 1;  // published to the consumers by the first full-barrier arrive
+        atomicOr(a.status, PA_STATUS_BLOCK_ID);
+      }
+      __syncwarp();
+      const int br_log2 = a.box_log2;
+      const int br = 1 << br_log2;
+      int issued = 0;
+      bool ok = true;
+      for (int s = 0; s < n_stages; ++s) {
+        const int slot = s % C::NS;
+        if (s >= C::NS && !mbar_wait(&empty[slot], ((s / C::NS) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int key0 = kstart + s * C::SK;
+        const int nk = min(C::SK, kend - key0);
+        const int nseg = (nk + br - 1) >> br_log2;
+        uint32_t bytes = static_cast<uint32_t>(nseg * br * C::ROW_BYTES * 2);
+        if constexpr (C::kU8) bytes += static_cast<uint32_t>(nseg * br * 2 * 4);
+        uint8_t* st = smem + slot * C::STAGE;
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
+        __syncwarp();
+        // one copy per lane: a copy instruction costs its thread hundreds of
+        // cycles, so copies issued by one lane in a row would pace the stream
+        const int nt = nseg * C::CHUNKS;
+        // K: CHUNKS boxes per segment; V: the same, or for u8 one dim-major
+        // [head dim][key] box per segment
+        const int nv = C::kU8 ? nseg : nt;
+        int ncopy = nt + nv;
+        if constexpr (C::kU8) ncopy += nseg * (br == a.ps ? 2 : 4);
+        for (int c = lane; c < ncopy; c += 32) {
+          if (C::kU8 && c >= nt && c < nt + nv) {
+            const int seg = c - nt;
+            const int key = key0 + (seg << br_log2);
+            const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+            const int id = blk[lp - lp0];
+            tma_load_4d(st + C::TILE + seg * (D << br_log2), &tmV, slot0, 0, g, id, &full[slot]);
+          } else if (c < (C::kU8 ? nt : 2 * nt)) {
+            const bool is_v = c >= nt;
+            const int j = is_v ? c - nt : c;
+            const int seg = j / C::CHUNKS, ch = j % C::CHUNKS;
+            const int key = key0 + (seg << br_log2);
+            const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+            const int id = blk[lp - lp0];
+            const uint32_t off = static_cast<uint32_t>(((seg * C::CHUNKS + ch) << br_log2) * 128);
+            tma_load_4d(st + (is_v ? C::TILE : 0) + off, is_v ? &tmV : &tmK, ch * C::ELEMS_128, slot0, g, id, &full[slot]);
+            if (!is_v && a.trace != nullptr && ch == 0 && slot0 == 0)
+              atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
+          } else if constexpr (C::kU8) {
+            // per segment [scales(br) | zero-points(br)]; one copy per cache
+            // when the segment is a whole page (the record keeps both arrays
+            // adjacent), else scales and zero-points separately
+            const size_t rec = static_cast<size_t>(a.ps) * (D + 4);
+            const int idx = c - nt - nv;
+            const bool whole = (br == a.ps);
+            const int seg = whole ? idx >> 1 : idx >> 2;
+            const bool is_v = whole ? (idx & 1) != 0 : (idx & 2) != 0;
+            const int part = whole ? 0 : (idx & 1);  // 0: scales, 1: zero-points
+            const int key = key0 + (seg << br_log2);
+            const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
+            const int id = blk[lp - lp0];
+            const size_t roff = (static_cast<size_t>(id) * a.Hkv + g) * rec + static_cast<size_t>(a.ps) * D;
+            uint8_t* dst = st + 2 * C::TILE + seg * 4 * br + (is_v ? 4 * C::SK : 0);
+            const uint8_t* src = (is_v ? a.v_bytes : a.k_bytes) + roff;
+            if (whole) bulk_load(dst, src, 4 * br, &full[slot]);
+            else bulk_load(dst + 2 * br * part, src + 2 * a.ps * part + 2 * slot0, 2 * br, &full[slot]);
+          }
+        }
+        issued = s + 1;
+      }
+      if (!ok) {
+        if (lane == 0) {
+          atomicOr(a.status, PA_STATUS_TIMEOUT);
+          atomicOr(&s_timeout, 1);
+        }
+        // let the copies already in flight land before the CTA can retire
+        for (int s = max(0, issued - C::NS); s < issued; ++s) mbar_wait(&full[s % C::NS], (s / C::NS) & 1);
+      }
+      return;
     }
-    return;
   }
 
   // =========================== consumer warps ==============================
@@ -343,6 +421,12 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
   const int mV = ((lane >> 4) & 1) * 8 + (lane & 7), hiV = (lane >> 3) & 1;
   const float sl2 = a.scale_log2;
   bool timed_out = false;
+  // Byte offset of 16-byte unit `unit` of 128-byte column chunk `ch` of the
+  // stage's key kk: the TMA's swizzled boxes, or the gather's padded rows.
+  auto row_unit = [&](int kk, int ch, int unit) -> uint32_t {
+    if constexpr (GATHER) return static_cast<uint32_t>(kk * C::PITCH + ch * 128 + unit * 16);
+    else return tile_row_off(kk, ch, a.box_log2, C::CHUNKS) + swz(unit, kk);
+  };
 
   for (int s = 0; s < n_stages; ++s) {
     const int slot = s % C::NS;
@@ -380,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
             const int ch = col / C::ELEMS_128;
             const int unit = ((col % C::ELEMS_128) >> 3) + hiK;
             uint32_t af[4];
-            ldsm_x4(kt + tile_row_off(kk, ch, a.box_log2, C::CHUNKS) + swz(unit, kk), af[0], af[1], af[2], af[3]);
+            ldsm_x4(kt + row_unit(kk, ch, unit), af[0], af[1], af[2], af[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               if (nt < nt_active) mma16816<kBf>(sa[k & 1][nt], af, qf[k][nt][0], qf[k][nt][1]);
@@ -513,8 +597,10 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
               const int m = idx / UNITS, u = idx % UNITS;
               const int key = ck0 + m;
               if (key < si.klo || key > si.khi)
-                *reinterpret_cast<uint4*>(st + C::TILE + tile_row_off(16 * c + m, u >> 3, a.box_log2, C::CHUNKS) +
-                                          16 * (u & 7)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(st + C::TILE + (GATHER ? (16 * c + m) * C::PITCH + 16 * u
+                                                                 : tile_row_off(16 * c + m, u >> 3, a.box_log2,
+                                                                                C::CHUNKS) + 16 * (u & 7))) =
+                    make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async();
             __syncwarp();
@@ -526,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
             const int ch = col / C::ELEMS_128;
             const int unit = ((col % C::ELEMS_128) >> 3) + hiV;
             uint32_t af[4];
-            ldsm_x4_t(vt + tile_row_off(kk, ch, a.box_log2, C::CHUNKS) + swz(unit, kk), af[0], af[1], af[2], af[3]);
+            ldsm_x4_t(vt + row_unit(kk, ch, unit), af[0], af[1], af[2], af[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               if (nt < nt_active) mma16816<kBf>(o[mt][nt], af, pb[nt][0], pb[nt][1]);

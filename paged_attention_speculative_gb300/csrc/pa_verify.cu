@@ -111,11 +111,12 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   const int ps = d->page_size;
   if (!pow2(ps) || ps > 256) return PA_ERR_PAGE_SIZE;
   // Pages of 1, 2 or 4 tokens: fp32 caches (the FFMA kernel looks every key
-  // up anyway) and 16-bit caches with head_dim <= 128 (the tensor-memory
-  // kernel's cp.async-gather producer).  The other kernels stage whole pages
-  // with TMA boxes and take 8 tokens or more.
+  // up anyway), 16-bit caches with head_dim <= 128 (the tensor-memory
+  // kernel's cp.async-gather producer) and with head_dim 256 (the warp-level
+  // kernel's per-key bulk copies).  The other kernels stage whole pages with
+  // TMA boxes and take 8 tokens or more.
   const bool small_pages = ps < pa::kGatherBelowPageSize;
-  if (small_pages && !(kv == PA_F32 || ((kv == PA_BF16 || kv == PA_F16) && D <= 128))) return PA_ERR_PAGE_SIZE;
+  if (small_pages && !(kv == PA_F32 || kv == PA_BF16 || kv == PA_F16)) return PA_ERR_PAGE_SIZE;
   // u8 V pages are copied as [head dim][key] boxes at least 16 keys wide
   if (kv == PA_U8 && ps < 16) return PA_ERR_PAGE_SIZE;
   const pa_dtype qd = d->q_dtype, od = d->out_dtype;
@@ -141,8 +142,9 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
   // 29.4 us on the warp-level kernel).  With head_dim 64 the warp-level
   // kernel stays ahead below 8 rows (10.8 vs 10.9 us).
   const bool tc16 = (kv == PA_BF16 || kv == PA_F16) && (D == 64 || D == 128);
-  // Small pages always take the rows-on-M tensor-memory kernel (16-bit caches).
-  const int choice = small_pages ? 2 : env_kernel_choice();
+  // Small pages always take the rows-on-M tensor-memory kernel (16-bit
+  // caches, head_dim <= 128) or the warp-level one (head_dim 256).
+  const int choice = small_pages ? (D == 256 ? 1 : 2) : env_kernel_choice();
   // u8 caches with head_dim 128, pages of 16 / 32 / 64 tokens and up to 32
   // query rows per KV head take the u8 tensor-memory kernel: each code is
   // converted once per stage whatever the row count, so its cost does not
@@ -169,7 +171,8 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
       ctas_per_sm = info.ctas_per_sm;
     }
   }
-  if (small_pages && kernel != 1 && kernel != 2) return PA_ERR_PAGE_SIZE;  // more than 64 rows per KV head
+  // more than 64 rows per KV head (head_dim <= 128)
+  if (small_pages && kernel != 1 && kernel != 2 && D != 256) return PA_ERR_PAGE_SIZE;
   if (kernel == 0) {
     // one 8-row n-tile per warp keeps a warp's accumulators within the
     // register budget of two CTAs per SM; rows beyond 8 go to more warps
@@ -178,7 +181,8 @@ int make_plan(const pa_dims* d, int32_t max_ctx, int32_t window, pa_dtype kv, in
     const int cap = pa::kConsumerWarps * 8 * nt;
     if (rows > cap) return PA_ERR_UNSUPPORTED;
     bool ok = false;
-    pa::MmaKernelInfo info = mma_info(D, mma_kind(kv), nt, &ok);
+    pa::MmaKernelInfo info =
+        small_pages ? pa::mma_info_d256_gather(mma_kind(kv), &ok) : mma_info(D, mma_kind(kv), nt, &ok);
     if (!ok) return PA_ERR_UNSUPPORTED;
     sk = info.stage_keys;
     smem = info.smem_bytes;
@@ -438,6 +442,8 @@ int launch_partition(const Call& c, const pa_plan& plan, const Workspace& w) {
     if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
     if (rc != PA_OK) return rc;
     e = pa::launch_tc(d->head_dim, mma_kind(c.kv), mk, mv, a, grid, c.stream);
+  } else if (plan.kernel == 0 && d->page_size < pa::kGatherBelowPageSize) {
+    e = pa::launch_mma_d256_gather(mma_kind(c.kv), a, grid, c.stream);
   } else if (plan.kernel == 0) {
     CUtensorMap mk, mv;
     int rc = encode_cache_map(&mk, c.k, c.kv, d, box_rows);

@@ -117,7 +117,8 @@ def test_plan_rejections(lib):
         (dims(page_size=3), pa.PA_BF16, -5),
         (dims(page_size=512), pa.PA_BF16, -5),
         (dims(page_size=4), pa.PA_U8, -5),
-        (dims(page_size=2, head_dim=256), pa.PA_BF16, -5),
+        (dims(page_size=2, head_dim=256, num_q_heads=64, total_tokens=8), pa.PA_BF16, -10),  # 64 rows > 32
+        (dims(page_size=1, head_dim=256), pa.PA_U8, -5),
         (dims(page_size=1, num_q_heads=128, num_kv_heads=8, total_tokens=8, max_blocks_per_seq=8192), pa.PA_BF16,
          -5),
         (dims(num_q_heads=30), pa.PA_BF16, -3),
@@ -135,7 +136,9 @@ def test_plan_rejections(lib):
 def test_plan_small_pages(lib):
     """Pages of 1, 2 or 4 tokens: 16-bit caches take the tensor-memory kernel
     (its cp.async-gather producer) whatever the row count, with partitions
-    free of the per-CTA page-list cap; fp32 caches keep the FFMA kernel."""
+    free of the per-CTA page-list cap; head_dim 256 takes the warp-level
+    kernel with per-key bulk copies (two CTAs per SM, the same partitions as
+    8-token pages); fp32 caches keep the FFMA kernel."""
     p = pa.PaPlan()
     for ps in (1, 2, 4):
         for hq, t in ((32, 1), (32, 4), (64, 8)):
@@ -150,6 +153,18 @@ def test_plan_small_pages(lib):
         d = dims(page_size=ps, q_dtype=pa.PA_F32, max_blocks_per_seq=4096)
         assert lib.pa_verify_plan(ctypes.byref(d), 4000, 0, pa.PA_F32, 152, ctypes.byref(p)) == 0
         assert p.kernel == 1
+        for hq, t, window in ((32, 2, 0), (32, 8, 0), (64, 4, 0), (32, 2, 1024)):
+            d = dims(page_size=ps, head_dim=256, num_q_heads=hq, num_kv_heads=16, total_tokens=t,
+                     max_blocks_per_seq=32768 // ps + 8)
+            assert lib.pa_verify_plan(ctypes.byref(d), 32768 + t, window, pa.PA_BF16, 152, ctypes.byref(p)) == 0
+            assert p.kernel == 0 and p.stage_keys == 32 and p.row_tiles == 1
+            assert 2 * (p.smem_bytes + 1024) <= 233472  # two CTAs per SM
+            assert p.num_partitions * p.part_tokens >= (window + t - 1 if window else 32768 + t)
+            d8 = dims(page_size=8, head_dim=256, num_q_heads=hq, num_kv_heads=16, total_tokens=t,
+                      max_blocks_per_seq=32768 // 8 + 8)
+            q = pa.PaPlan()
+            assert lib.pa_verify_plan(ctypes.byref(d8), 32768 + t, window, pa.PA_BF16, 152, ctypes.byref(q)) == 0
+            assert (q.kernel, q.num_partitions, q.part_tokens) == (0, p.num_partitions, p.part_tokens)
 
 
 def test_forward_host_errors_need_no_gpu(lib):
