@@ -200,7 +200,8 @@ def mixed_sweep(stream, hbm_peak, l2):
     for name, hq, hkv, d, vq, vl, pq, plen in (
             ("qwen_4xT4_L32768+T512_L32768", 32, 8, 128, [4] * 4, [32768] * 4, [512], [32768]),
             ("qwen_4xT4_L32768+T2048_L0", 32, 8, 128, [4] * 4, [32768] * 4, [2048], [0]),
-            ("long_T8_L131072+T256_L131072", 64, 8, 128, [8], [131072], [256], [131072])):
+            ("long_T8_L131072+T256_L131072", 64, 8, 128, [8], [131072], [256], [131072]),
+            ("qwen_4xT4_L32768+T64_L32768", 32, 8, 128, [4] * 4, [32768] * 4, [64], [32768])):
         us = {}
         for part, ql, pl in (("mixed", vq + pq, vl + plen), ("verify", vq, vl), ("prefill", pq, plen)):
             w = DeviceWorkload(hq, hkv, d, 16, "bf16", ql, pl, 0, min_bytes=2 * l2, seed=17)

@@ -300,15 +300,20 @@ int pa_verify_forward_tree(const void* q, const void* k_cache, const void* v_cac
  *  Sequences with T_b <= 8 (verify steps) run on the split-KV partition
  *  kernels and the combine, exactly as in pa_verify_forward, their partials
  *  indexed by slot b * 8 + i.  Sequences with T_b > 8 (prefill chunks) run
- *  on a prefill kernel: 128 query rows per CTA (128 / G tokens x the G heads
- *  of a KV head) streaming the tile's keys once on the tensor cores (16-bit
- *  caches), or the fp32 FFMA kernel (fp32 caches); their rows are written
- *  directly.  The three launches are ordered on cuda_stream.
+ *  on a prefill kernel: 128 or 256 query rows per CTA (rows / G tokens x the
+ *  G heads of a KV head) streaming the block's keys once on the tensor cores
+ *  (16-bit caches), or the fp32 FFMA kernel (fp32 caches); their rows are
+ *  written directly.  When the chunks' blocks fill at most half the SMs
+ *  (judged from total_tokens and the SM count) and max_context_len gives
+ *  each piece >= 4096 keys, each block's keys are split into as many pieces
+ *  (at most 16) as fit in one wave; a fourth kernel merges their partial
+ *  rows.  The launches are ordered on cuda_stream.
  *
  *  Arguments as for pa_verify_forward; dims.total_tokens counts both kinds.
  *  The workspace is pa_mixed_workspace_size bytes (status word + partials
- *  for 8 token slots per sequence); its status word is shared by all three
- *  kernels.  Supported: bf16 / f16 caches with head_dim 64 or 128, pages of
+ *  for 8 token slots per sequence, + total_tokens x Hq x pieces prefill
+ *  partial rows when the keys are split); its status word is shared by all
+ *  the kernels.  Supported: bf16 / f16 caches with head_dim 64 or 128, pages of
  *  8 tokens or more and Hq / Hkv <= 128, or fp32 caches (any head_dim and
  *  page size); otherwise PA_ERR_UNSUPPORTED (PA_ERR_PAGE_SIZE for 16-bit
  *  caches with smaller pages).  Device errors as for pa_verify_forward,

@@ -142,8 +142,75 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 4) pa_combine(const Combin
       v.w += wgt[w] * s_acc[w0 + w][d + 3];
     }
     store_out4(a.out, a.out_dtype, static_cast<size_t>(row) * D + d,
-               make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv));
+               zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv));
   }
+}
+
+}  // namespace pa
+
+namespace pa {
+
+// Prefill chunks whose blocks' keys were split into S pieces (S <=
+// a.num_parts, the partial rows' stride; the same count the prefill kernel
+// derives from the batch): one warp per output row (token t, query head h)
+// of a prefill sequence merges the row's S partials [t * Hq + h][piece] with
+// the same log-sum-exp rule.  Rows of verify steps (T_b <= 8) and of sequences with malformed
+// metadata (which the prefill kernel zeroed and reported) are left alone.
+template <int D>
+__global__ void __launch_bounds__(128) pa_prefill_combine(const CombineArgs a) {
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const long long rows = static_cast<long long>(a.total_tokens) * a.Hq;
+  const int t = row < rows ? static_cast<int>(row / a.Hq) : 0;
+  int lo = 0, hi = a.num_seqs - 1;  // sequence of token t: last b with begins[b] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.begins + mid) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const SeqInfo si = seq_info(a.begins, a.past_lens, lo, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
+                              a.part_tokens, a.row_cap, kRoleLong);
+  const int S = prefill_pieces(a.begins, a.num_seqs, a.row_cap / a.G, a.Hkv, a.num_parts, a.num_sms);
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  if (S <= 1 || row >= rows || si.foreign || si.err || t < si.t0 || t >= si.t0 + si.T) return;
+  // the pieces of this row's block (its TQ tokens and their keys), as the
+  // prefill kernel counts them; one piece: the kernel wrote the row itself
+  const int TQ = a.row_cap / a.G;
+  const int i0 = (t - si.t0) / TQ * TQ, ntok = min(TQ, si.T - i0);
+  const int klo = a.window > 0 ? max(0, si.L + i0 - a.window + 1) : 0;
+  const int pieces = prefill_block_pieces(S, si.L + i0 + ntok - (klo / a.ps) * a.ps);
+  if (pieces <= 1) return;
+  const size_t pr = static_cast<size_t>(row) * a.num_parts;  // pieces [0, pieces) of at most 32, one per lane
+  const float mj = lane < pieces ? a.pm[pr + lane] : -INFINITY;
+  const float lj = lane < pieces ? a.pl[pr + lane] : 0.f;
+  float M = mj;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  const float wj = ex2(mj - Mu);
+  float lsum = wj * lj;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+  const bool poisoned = __any_sync(0xffffffffu, lj < 0.f);
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  const float* po = a.po + pr * D + lane * PER;
+  for (int j = 0; j < pieces; ++j) {
+    const float w = __shfl_sync(0xffffffffu, wj, j);
+#pragma unroll
+    for (int e = 0; e < PER; e += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(po + static_cast<size_t>(j) * D + e);
+      acc[e] = fmaf(w, v.x, acc[e]);
+      acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+    }
+  }
+  const float inv = (poisoned || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) store_out(a.out, a.out_dtype, static_cast<size_t>(row) * D + lane * PER + e,
+                                 poisoned ? 0.f : acc[e] * inv);
 }
 
 }  // namespace pa

@@ -51,6 +51,7 @@ struct PartArgs {
   int max_ctx, window, part_tokens, num_parts, box_log2, row_cap;
   int q_dtype, out_dtype;
   int role;                     // kRoleAll / kRoleShort / kRoleLong
+  int num_sms;                  // SMs of the device (prefill key pieces)
   float scale_log2;             // softmax scale * log2(e)
 };
 
@@ -64,6 +65,7 @@ struct CombineArgs {
   uint32_t* status;
   int num_seqs, total_tokens, Hq, Hkv, G, ps, max_ctx, window, part_tokens, num_parts, row_cap, out_dtype;
   int role;
+  int num_sms;
 };
 
 // ---------------------------------------------------------------------------
@@ -133,6 +135,34 @@ __device__ __forceinline__ SeqInfo seq_info(const int32_t* begins, const int32_t
   s.kbase = (s.klo / ps) * ps;
   s.nparts = (s.err || s.T <= 0) ? 0 : (s.khi + 1 - s.kbase + part_tokens - 1) / part_tokens;
   return s;
+}
+
+// Fewest keys a prefill block's key piece takes: a block with fewer keys than
+// pieces x this uses fewer pieces (prefill_block_pieces).
+constexpr int kPrefillMinPieceKeys = 4096;
+
+__device__ __forceinline__ int prefill_block_pieces(int pieces, int keys) {
+  return max(1, min(pieces, keys / kPrefillMinPieceKeys));
+}
+
+// Key pieces of a mixed call's prefill blocks, from the blocks the batch
+// really has (sequences with T_b > 8, TQ tokens per block): as many as fit in
+// one wave of the SMs, at most `max_pieces` (the launch's grid.z and the
+// partial rows' stride).  Warp-collective: every lane returns the count.
+__device__ __forceinline__ int prefill_pieces(const int32_t* begins, int num_seqs, int TQ, int Hkv, int max_pieces,
+                                              int num_sms) {
+  if (max_pieces <= 1) return 1;
+  const int lane = threadIdx.x & 31;
+  long long blocks = 0;
+  for (int s = lane; s < num_seqs; s += 32) {
+    const int T = ld_once(begins + s + 1) - ld_once(begins + s);
+    if (T > PA_MAX_QUERY_LEN) blocks += (T + TQ - 1) / TQ;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) blocks += __shfl_xor_sync(0xffffffffu, blocks, off);
+  const long long ctas = blocks * Hkv;
+  if (ctas <= 0) return 1;
+  return static_cast<int>(max(1LL, min(static_cast<long long>(max_pieces), num_sms / ctas)));
 }
 
 // Partial-buffer row of output row `row` (= t * Hq + h) of a sequence.

@@ -65,9 +65,12 @@ cudaError_t launch_tc_gather(int D, int kv, const PartArgs& a, dim3 grid, cudaSt
 
 // Prefill tiles of a mixed batch (sequences with more than 8 new tokens):
 // up to 256 query rows (two 128-row tiles) per CTA, head_dim 64 / 128,
-// KV_BF16 / KV_F16 caches; grid (row blocks, Hkv), 320 threads.
+// KV_BF16 / KV_F16 caches; grid (row blocks, Hkv, key pieces), 320 threads.
 cudaError_t launch_prefill_tc(int D, int kv, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a,
                               dim3 grid, cudaStream_t st);
+// Merge of the prefill blocks' key pieces (a.num_parts of them, at most 32)
+// into the output rows of the prefill sequences; one warp per row.
+cudaError_t launch_prefill_combine(int D, const CombineArgs& a, cudaStream_t st);
 
 // u8 caches, head_dim 128, pages of 16 / 32 / 64 tokens, row tiles n = 16 /
 // 32: the keys-on-M tensor-memory kernel with converter warps; stage_keys =

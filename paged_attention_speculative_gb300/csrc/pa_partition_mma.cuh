@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
             const int lp = key >> a.ps_log2, slot0 = key & (a.ps - 1);
             const int id = blk[lp - lp0];
             const uint32_t off = static_cast<uint32_t>(((seg * C::CHUNKS + ch) << br_log2) * 128);
-            tma_load_4d(st + (is_v ? C::TILE : 0) + off, is_v ? &tmV : &tmK, ch * C::ELEMS_128, slot0, g, id, &full[slot]);
+            tma_load_4d(st + (is_v ? C::TILE : 0) + off, is_v ? &tmV : &tmK, ch * C::ELEMS_128, slot0, g, id,
+                        &full[slot]);
             if (!is_v && a.trace != nullptr && ch == 0 && slot0 == 0)
               atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + lp, id + 1);
           } else if constexpr (C::kU8) {
@@ -743,7 +744,9 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
         }
       }
       if (si.nparts == 1)
-        store_out4(a.out, a.out_dtype, row * D + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        store_out4(a.out, a.out_dtype, row * D + d,
+                   poisoned ? make_float4(0.f, 0.f, 0.f, 0.f)
+                            : make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
       else
         *reinterpret_cast<float4*>(a.po + pr * D + d) = acc;
     }

@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(GATHER ? 128 + 32 * kGatherWarps : 128, 1)
         if (si.nparts == 1) {
           const float inv = (poisoned || !(l > 0.f)) ? 0.f : 1.f / l;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, o[e] * inv);
+          for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, poisoned ? 0.f : o[e] * inv);
         } else {
           float4* dst = reinterpret_cast<float4*>(a.po + (prow(row, si, a.Hq) * a.num_parts + p) * D + 32 * c);
 #pragma unroll

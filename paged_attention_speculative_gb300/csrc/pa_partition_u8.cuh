@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(640, 1)
       if (n < R) {
         const float o = fmaf(wa[n], oa[e], has_b ? wb[n] * ob[e] : 0.f) - zrow[n];
         if (si.nparts > 1) a.po[rowoff[n] + dd] = o;
-        else store_out(a.out, a.out_dtype, rowoff[n] + dd, o * linv[n]);
+        else store_out(a.out, a.out_dtype, rowoff[n] + dd, poisoned ? 0.f : o * linv[n]);
       }
     }
     tc_fence_before();

@@ -13,7 +13,12 @@
 //   S_t(s) = Q_t . K_s^T   tcgen05.mma M=128, N=64, K=D  (Q_t from smem)
 //   P_t(s) = 2^(S*scale*log2e - m) per row, causal / window mask per row
 //   O_t   += P_t(s) . V_s  tcgen05.mma M=128, N=D, K=64  (P_t in TMEM)
-// and writes the normalised rows directly (no split over keys).
+// and writes the normalised rows directly -- or, when the blocks' keys are
+// split (chunks whose blocks fill at most half the SMs: as many pieces as
+// still fit in one wave, up to grid.z), each CTA streams one contiguous run
+// of the block's stages and writes unnormalised partial rows (max,
+// denominator, output) that pa_prefill_combine merges, as the verify path's
+// combine does.
 //
 // With two tiles they ping-pong, one S and one P buffer each: the MMA thread
 // issues S_0(s), PV_1(s-1), S_1(s), PV_0(s), so tile 0's softmax of stage s
@@ -64,7 +69,9 @@ struct PfCfg {
   static_assert(P_COL + SK <= TMEM_COLS, "tensor-memory budget");
 };
 
-template <int D, int KV>
+// SPLIT: the launch may split the blocks' keys into pieces (grid.z > 1); the
+// instantiation without it keeps the unsplit kernel's code exactly.
+template <int D, int KV, bool SPLIT>
 __global__ void __launch_bounds__(320, 1)
     pa_prefill_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const PartArgs a) {
@@ -80,7 +87,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = s_free + 2;         // [2] P_t written (4 softmax warps of tile t)
   uint64_t* pv_done = p_full + 2;        // [2] PV_t done (MMA commit)
   __shared__ uint32_t s_tmem;
-  __shared__ int s_bad, s_timeout;
+  __shared__ int s_bad, s_timeout, s_pieces;
 
   const int g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -103,15 +110,19 @@ __global__ void __launch_bounds__(320, 1)
       blk -= nb;
     }
   }
+  // pieces in use: the launch's grid.z is an upper bound made on the host,
+  // which does not know the chunks' lengths
+  int npieces = 1;
+  if constexpr (SPLIT) npieces = prefill_pieces(a.begins, a.num_seqs, TQ, a.Hkv, gridDim.z, a.num_sms);
   pdl_launch_dependents();
-  if (b < 0) return;
+  if (b < 0 || (SPLIT && static_cast<int>(blockIdx.z) >= npieces)) return;
   const SeqInfo si = seq_info(a.begins, a.past_lens, b, a.total_tokens, a.G, a.ps, a.max_ctx, a.window,
                               a.part_tokens, a.row_cap, kRoleLong);
   const int ntok = min(TQ, si.T - i0);  // tokens of this row block
   const int R = ntok * a.G;             // real rows (at most 256)
   if (si.err) {
     if (threadIdx.x == 0) atomicOr(a.status, si.err);
-    if (si.rows_ok)
+    if (si.rows_ok && (!SPLIT || blockIdx.z == 0))
       for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
         const int r = idx / D, d = idx % D;
         store_out(a.out, a.out_dtype, (static_cast<size_t>(si.t0 + i0 + r / a.G) * a.Hq + g * a.G + r % a.G) * D + d,
@@ -124,13 +135,21 @@ __global__ void __launch_bounds__(320, 1)
 
   const int klo = a.window > 0 ? max(0, si.L + i0 - a.window + 1) : 0;
   const int khi = si.L + i0 + ntok - 1;
-  const int kstart = (klo >> a.ps_log2) << a.ps_log2;  // page aligned
-  const int kend = khi + 1;
-  const int n_stages = (kend - kstart + C::SK - 1) / C::SK;
+  const int kfirst = (klo >> a.ps_log2) << a.ps_log2;  // page aligned
+  // piece blockIdx.z of this block's `pieces` streams its stages [st0, st1)
+  const int pieces = SPLIT ? prefill_block_pieces(npieces, khi + 1 - kfirst) : 1;
+  if (SPLIT && static_cast<int>(blockIdx.z) >= pieces) return;
+  const int n_all = (khi + 1 - kfirst + C::SK - 1) / C::SK;
+  const int st0 = SPLIT ? static_cast<int>(static_cast<long long>(n_all) * blockIdx.z / pieces) : 0;
+  const int st1 = SPLIT ? static_cast<int>(static_cast<long long>(n_all) * (blockIdx.z + 1) / pieces) : n_all;
+  const int kstart = kfirst + st0 * C::SK;             // this piece's first key
+  const int kend = SPLIT ? min(kfirst + st1 * C::SK, khi + 1) : khi + 1;  // one past its last
+  const int n_stages = st1 - st0;
 
   if (threadIdx.x == 288) {
     s_bad = 0;
     s_timeout = 0;
+    if constexpr (SPLIT) s_pieces = pieces;  // read back by the epilogue (no register held over the loop)
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&full[s], two ? 1 : 2);  // one producer, or K and V producers (one tile)
       mbar_init(&empty[s], 1);
@@ -439,7 +458,8 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[bi]);
     }
-    // ---- epilogue: normalised O row from TMEM -> output ----
+    // ---- epilogue: normalised O row from TMEM -> output (or the piece's
+    // partial row) ----
     if (ok && n_stages >= 1) {
       const int n1 = n_stages - 1;
       if (!mbar_wait(&pv_done[two ? t : (n1 & 1)], two ? (n1 & 1) : ((n1 >> 1) & 1))) ok = false;
@@ -452,14 +472,37 @@ __global__ void __launch_bounds__(320, 1)
     const bool poisoned = s_bad != 0 || s_timeout != 0 || !ok;
     const bool real = r < R;
     const size_t row = real ? static_cast<size_t>(si.t0 + i0 + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
-    const float inv = (poisoned || !(l > 0.f)) ? 0.f : 1.f / l;
+    if (SPLIT && s_pieces > 1) {
+      // partial row of this piece (stride: the launch's grid.z); a piece
+      // without stages holds nothing (its accumulator was never written) and
+      // gets weight 0
+      const size_t pr = row * gridDim.z + blockIdx.z;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      float o[32];
-      tmem_ld32(tm_o + 32 * c, o);
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tm_o + 32 * c, o);
+        if (real) {
+          float4* dst = reinterpret_cast<float4*>(a.po + pr * D + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            dst[e / 4] = n_stages > 0 ? make_float4(o[e], o[e + 1], o[e + 2], o[e + 3])
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
       if (real) {
+        a.pm[pr] = n_stages > 0 ? m_ref : -INFINITY;
+        a.pl[pr] = poisoned ? -1.f : (n_stages > 0 ? l : 0.f);
+      }
+    } else {
+      const float inv = (poisoned || !(l > 0.f)) ? 0.f : 1.f / l;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, o[e] * inv);
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tm_o + 32 * c, o);
+        if (real) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) store_out(a.out, a.out_dtype, row * D + 32 * c + e, poisoned ? 0.f : o[e] * inv);
+        }
       }
     }
     tc_fence_before();

@@ -77,6 +77,16 @@ int env_row_tiles() {
   return v;
 }
 
+// Optional tuning override of the prefill blocks' key pieces (1..32), read once.
+int env_prefill_splits() {
+  static const int v = [] {
+    const char* s = std::getenv("PA_PREFILL_SPLITS");
+    const int n = s ? std::atoi(s) : 0;
+    return (n >= 1 && n <= 32) ? n : 0;
+  }();
+  return v;
+}
+
 // Optional tuning override of the prefill kernel's rows per CTA (128 or 256), read once.
 int env_prefill_rows() {
   static const int v = [] {
@@ -271,6 +281,64 @@ Workspace carve(void* ws, const pa_dims* d, const pa_plan& plan, bool mixed = fa
   return w;
 }
 
+// Row blocks of a mixed call's prefill chunks and the pieces their keys are
+// split into, from what the host knows (dims, max_context_len, the window and
+// the SM count; the chunks' lengths are device data, so `tiles` is an upper
+// bound: every token in full blocks plus one partial block per possible
+// chunk).  Blocks of 256 rows (two 128-row tiles sharing each K/V stage,
+// about 18 % more work per SM) when they still give two waves of CTAs;
+// otherwise 128 rows, so that chunks spread over more SMs (measured: a
+// 512-token chunk at 32k keys takes 475 us in 128-row blocks, 805 us in
+// 256-row blocks).  When the blocks fill at most half the SMs and every
+// piece keeps >= 4096 keys, each block's keys are split into pieces, as many
+// as still fit in one wave (measured, chunk alone: 64 tokens at 32k keys
+// 361 -> 76 us, 128 tokens at 64k keys 696 -> 247 us).  Blocks that fill a
+// wave or more are not split: a split over several waves can add one (512
+// tokens at 32k keys in 6 pieces: 376 -> 400 us).  The host bounds the
+// pieces (`splits`, the grid's z extent and the partial rows' stride) by the
+// fewest blocks the batch can have -- its tokens beyond 8 per sequence -- and
+// the kernels count the blocks the batch really has and use as many of the
+// pieces as fit in one wave (prefill_pieces); the others exit at once.
+struct PrefillGeometry {
+  int rows_per_block;
+  long long tiles;
+  int splits;
+};
+
+PrefillGeometry prefill_geometry(const pa_dims* d, int32_t max_ctx, int32_t window, int sms) {
+  PrefillGeometry pg;
+  const int G = d->num_q_heads / d->num_kv_heads;
+  const long long rows = static_cast<long long>(d->total_tokens) * G;
+  pg.rows_per_block = ceil_div(rows, 256) * d->num_kv_heads >= 2LL * sms ? 256 : 128;
+  if (env_prefill_rows() > 0) pg.rows_per_block = env_prefill_rows();
+  const long long TQ = pg.rows_per_block / G;
+  pg.tiles = ceil_div(d->total_tokens, TQ) +
+             std::min<long long>(d->num_seqs, d->total_tokens / (PA_MAX_QUERY_LEN + 1));
+  const long long keys = window > 0 ? std::min<long long>(max_ctx, static_cast<long long>(window) + TQ) : max_ctx;
+  const long long min_blocks =
+      std::max<long long>(1, ceil_div(std::max<long long>(0, d->total_tokens - 8LL * d->num_seqs), TQ));
+  const long long S_fit = std::min<long long>(std::min<long long>(16, keys / pa::kPrefillMinPieceKeys),
+                                              sms / (min_blocks * d->num_kv_heads));
+  int S = static_cast<int>(std::max<long long>(1, S_fit));
+  if (env_prefill_splits() > 0) S = env_prefill_splits();
+  pg.splits = S;
+  return pg;
+}
+
+// Prefill partials [token * Hq + head][piece] behind the verify part's
+// workspace; none when the chunks' keys are not split.
+size_t prefill_partial_bytes(const pa_dims* d, int splits) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(d->total_tokens) * d->num_q_heads * splits;
+  return align256(rows * d->head_dim * 4) + 2 * align256(rows * 4);
+}
+
+size_t mixed_workspace_bytes(const pa_dims* d, const pa_plan& plan, int32_t max_ctx, int32_t window, pa_dtype kv,
+                             int sms) {
+  const int splits = kv == PA_F32 ? 1 : prefill_geometry(d, max_ctx, window, sms).splits;  // fp32: one pass
+  return workspace_bytes_for(d, plan, true) + prefill_partial_bytes(d, splits);
+}
+
 int device_sm_count(int* out) {
   static std::atomic<int> cache[64];
   int dev = 0;
@@ -419,6 +487,7 @@ PartArgs part_args(const Call& c, const pa_plan& plan, const Workspace& w) {
   a.out_dtype = d->out_dtype;
   a.scale_log2 = c.scale * 1.4426950408889634f;
   a.role = c.role;
+  a.num_sms = plan.num_sms;
   return a;
 }
 
@@ -489,6 +558,7 @@ int launch_combine(const Call& c, const pa_plan& plan, const Workspace& w) {
                                  : (1 << 30);
   a.out_dtype = d->out_dtype;
   a.role = c.role;
+  a.num_sms = plan.num_sms;
   const long long rows = static_cast<long long>(d->total_tokens) * d->num_q_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((rows + pa::kCombineRows - 1) / pa::kCombineRows));
@@ -562,25 +632,21 @@ int launch_prefill(const Call& c, const pa_plan& plan, const Workspace& w) {
     else if (d->head_dim == 128) e = pa::launch_dependent(pa::pa_partition_f32<128>, grid, dim3(128), 0, c.stream, a);
     else e = pa::launch_dependent(pa::pa_partition_f32<256>, grid, dim3(128), 0, c.stream, a);
   } else {
-    // Row blocks of 256 rows (two 128-row tiles sharing each K/V stage, about
-    // 18 % more work per SM) when the chunk tokens, at most total_tokens,
-    // still give two waves of CTAs; otherwise 128 rows, so that chunks
-    // spread over more SMs (measured: a 512-token chunk at 32k keys takes
-    // 475 us in 128-row blocks, 805 us in 256-row blocks).  Blocks
-    // of TQ tokens: at most total / TQ full ones plus one partial one per
-    // prefill sequence (each has at least 9 tokens).
-    const int G = d->num_q_heads / d->num_kv_heads;
     int sms = 0;
     if (device_sm_count(&sms) != PA_OK) return PA_ERR_CUDA;
-    const long long rows = static_cast<long long>(d->total_tokens) * G;
-    int rows_per_block = ceil_div(rows, 256) * d->num_kv_heads >= 2LL * sms ? 256 : 128;
-    if (env_prefill_rows() > 0) rows_per_block = env_prefill_rows();
-    a.row_cap = rows_per_block;
-    const long long TQ = rows_per_block / G;
-    const long long tiles = ceil_div(d->total_tokens, TQ) +
-                            std::min<long long>(d->num_seqs, d->total_tokens / (PA_MAX_QUERY_LEN + 1));
-    if (tiles > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    if (tiles == 0) return PA_OK;
+    const PrefillGeometry pg = prefill_geometry(d, c.max_ctx, c.window, sms);
+    a.row_cap = pg.rows_per_block;
+    if (pg.tiles > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (pg.tiles == 0) return PA_OK;
+    if (pg.splits > 1) {
+      // the pieces' partial rows, after the verify part's workspace
+      const size_t rows = static_cast<size_t>(d->total_tokens) * d->num_q_heads * pg.splits;
+      uint8_t* base = reinterpret_cast<uint8_t*>(w.status) + workspace_bytes_for(d, plan, true);
+      a.po = reinterpret_cast<float*>(base);
+      a.pm = reinterpret_cast<float*>(base + align256(rows * d->head_dim * 4));
+      a.pl = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a.pm) + align256(rows * 4));
+      a.num_parts = pg.splits;
+    }
     const int box_rows = std::min(d->page_size, 64);
     a.box_log2 = ilog2(box_rows);
     CUtensorMap mk, mv;
@@ -588,7 +654,32 @@ int launch_prefill(const Call& c, const pa_plan& plan, const Workspace& w) {
     if (rc == PA_OK) rc = encode_cache_map(&mv, c.v, c.kv, d, box_rows);
     if (rc != PA_OK) return rc;
     e = pa::launch_prefill_tc(d->head_dim, mma_kind(c.kv), mk, mv, a,
-                              dim3(static_cast<unsigned>(tiles), d->num_kv_heads), c.stream);
+                              dim3(static_cast<unsigned>(pg.tiles), d->num_kv_heads, pg.splits), c.stream);
+    if (e == cudaSuccess && pg.splits > 1) {
+      CombineArgs ca;
+      ca.past_lens = c.past_lens;
+      ca.begins = c.begins;
+      ca.out = c.out;
+      ca.po = a.po;
+      ca.pm = a.pm;
+      ca.pl = a.pl;
+      ca.status = w.status;
+      ca.num_seqs = d->num_seqs;
+      ca.total_tokens = d->total_tokens;
+      ca.Hq = d->num_q_heads;
+      ca.Hkv = d->num_kv_heads;
+      ca.G = d->num_q_heads / d->num_kv_heads;
+      ca.ps = d->page_size;
+      ca.max_ctx = c.max_ctx;
+      ca.window = c.window;
+      ca.part_tokens = a.part_tokens;
+      ca.num_parts = pg.splits;
+      ca.row_cap = pg.rows_per_block;
+      ca.out_dtype = d->out_dtype;
+      ca.role = pa::kRoleLong;
+      ca.num_sms = sms;
+      e = pa::launch_prefill_combine(d->head_dim, ca, c.stream);
+    }
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -617,7 +708,7 @@ int run_mixed(Call c) {
   if (rc != PA_OK) return rc;
   rc = make_plan(c.d, c.max_ctx, c.window, c.kv, sms, &plan);
   if (rc != PA_OK) return rc;
-  if (c.ws_bytes < workspace_bytes_for(c.d, plan, true)) return PA_ERR_WORKSPACE;
+  if (c.ws_bytes < mixed_workspace_bytes(c.d, plan, c.max_ctx, c.window, c.kv, sms)) return PA_ERR_WORKSPACE;
   const Workspace w = carve(c.ws, c.d, plan, true);
   c.role = pa::kRoleShort;  // verify steps: split-KV partitions + combine
   rc = launch_partition(c, plan, w);
@@ -703,7 +794,7 @@ size_t pa_mixed_workspace_size(const pa_dims* dims, int32_t max_context_len, int
   pa_plan plan;
   if (make_plan(dims, max_context_len, sliding_window, kv_dtype, sms, &plan) != PA_OK) return 0;
   if (mixed_support(dims, kv_dtype) != PA_OK) return 0;
-  return workspace_bytes_for(dims, plan, true);
+  return mixed_workspace_bytes(dims, plan, max_context_len, sliding_window, kv_dtype, sms);
 }
 
 int pa_forward_mixed(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

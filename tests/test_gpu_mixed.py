@@ -4,8 +4,9 @@ prefill tile kernel, in one call, against the oracle (whose causal rule holds
 for any number of new tokens).  Cases cover the query-head group sizes the
 tiles handle (G = 1, 2, 4, 6, 8: blocks of 128 / G or 256 / G tokens, ragged
 last blocks, one-tile and two-tile blocks), windows, f16 / bf16 / fp32
-caches, large pages, and device errors in a prefill chunk; a mixed call with
-no prefill chunk is pa_verify_forward bit for bit."""
+caches, large pages, keys split into pieces (few blocks at long context),
+and device errors in a prefill chunk; a mixed call with no prefill chunk is
+pa_verify_forward bit for bit."""
 import numpy as np
 import pytest
 
@@ -50,13 +51,49 @@ CASES = [
     (mk("prefill_ps8_win1", 79, [40], [100], 8, 2, ps=8, sliding_window=1), True),
     # enough rows for two waves of 256-row blocks: the two-tile ping-pong path
     (mk("prefill_256_rows", 85, [1200, 2], [100, 300], 64, 32, d=64), True),
+    # few blocks at long context: the blocks' keys split into pieces merged by
+    # the prefill combine (2 pieces; 2 inside a window; 6 for the long
+    # chunk beside a short one at past 0, which stays whole; 4 at head_dim 64)
+    (mk("split_small_chunk", 90, [24, 4, 1], [12000, 9000, 500], 32, 8), False),
+    (mk("split_window", 91, [40, 2], [30000, 100], 32, 8, sliding_window=9000), False),
+    (mk("split_short_and_long", 92, [20, 60, 3], [0, 40000, 800], 32, 8), True),
+    (mk("split_f16_d64", 93, [30], [16384], 8, 4, d=64, q_dtype="f16", kv_dtype="f16"), False),
+    # six real blocks: 3 of the 4 pieces the host provides for
+    (mk("split_fewer_than_launched", 94, [40, 40, 40], [20000, 20000, 20000], 32, 8), False),
 ]
+# pieces the host provides for (the grid's z extent); the kernels use as many
+# as fit in one wave for the blocks the batch really has
+SPLIT = {"split_small_chunk": 2, "split_window": 2, "split_short_and_long": 9, "split_f16_d64": 4,
+         "split_fewer_than_launched": 4}
+
+
+def prefill_pieces(case):
+    """Key pieces of the case's prefill blocks, read back from the size of
+    the mixed workspace: the verify part's bytes plus total_tokens x Hq x
+    pieces partial rows when the keys are split."""
+    import torch
+    a256 = lambda x: (x + 255) // 256 * 256
+    d = dims(case, to_device(case))
+    kvc = KV_CODE[case.kv_dtype]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = pa.plan(d, case.max_context_len, case.sliding_window, kvc, sms)
+    rows = case.num_seqs * 8 * case.num_q_heads * p.num_partitions
+    extra = pa.mixed_workspace_size(d, case.max_context_len, case.sliding_window, kvc) - (
+        256 + a256(rows * case.head_dim * 4) + 2 * a256(rows * 4))
+    if extra == 0:
+        return 1
+    prow = case.total_tokens * case.num_q_heads
+    for S in range(2, 33):
+        if a256(prow * S * case.head_dim * 4) + 2 * a256(prow * S * 4) == extra:
+            return S
+    raise AssertionError(f"workspace tail of {extra} bytes matches no piece count")
 
 
 @pytest.mark.parametrize("idx", range(len(CASES)))
 def test_mixed_matches_the_oracle(idx):
     make, derived = CASES[idx]
     case = make()
+    assert prefill_pieces(case) == SPLIT.get(case.name, 1)
     got, bits, _ = run_mixed(case)
     assert bits == 0, f"device status {bits:#x}"
     want = run_oracle(case)
@@ -74,6 +111,7 @@ def test_mixed_full_size():
     (Qwen-like heads)."""
     case = W.make_case("mixed_32k", seed=80, query_lens=[4, 130, 4, 4], past_lens=[32768, 32768, 30000, 32000],
                        num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    assert prefill_pieces(case) == 4
     got, bits, _ = run_mixed(case)
     assert bits == 0
     assert max_abs_err(got, run_oracle(case)) <= TOL
@@ -116,6 +154,21 @@ def test_bad_block_id_in_a_prefill_chunk_sets_the_status():
     good = run_oracle(case)
     # the verify step is untouched; the chunk's tiles that read the bad page are zero
     assert max_abs_err(got[:3], good[:3]) <= TOL
+
+
+def test_bad_block_id_in_a_split_prefill_chunk_zeroes_its_rows():
+    """A bad id read by one key piece poisons that piece's partial rows; the
+    prefill combine zeroes the rows, the verify step is untouched."""
+    case = W.make_case("bad_split", seed=86, query_lens=[3, 40], past_lens=[500, 12000], num_q_heads=32,
+                       num_kv_heads=8, head_dim=128, page_size=16)
+    assert prefill_pieces(case) == 2
+    bt = case.block_tables.copy()
+    bt[1, 600] = case.num_blocks + 3  # keys 9600..9615: the second piece of every block
+    bad = W.Case(**{**case.__dict__, "block_tables": bt})
+    got, bits, _ = run_mixed(bad)
+    assert bits & 0x4  # PA_STATUS_BLOCK_ID
+    assert max_abs_err(got[:3], run_oracle(case)[:3]) <= TOL
+    assert np.all(got[3:] == 0.0)
 
 
 def test_context_overflow_in_a_prefill_chunk_sets_the_status():
