@@ -942,6 +942,9 @@ PROFILE_EXTRA = {
                                     window=0, update=True),
     "prefill_T512_L32768": dict(Hq=32, Hkv=8, D=128, ps=16, kv="bf16", q_lens=[512], past=[32768], window=0,
                                 mixed=True),
+    # a short chunk at long context: its blocks' keys split into pieces
+    "prefill_T64_L32768": dict(Hq=32, Hkv=8, D=128, ps=16, kv="bf16", q_lens=[64], past=[32768], window=0,
+                               mixed=True),
 }
 
 
