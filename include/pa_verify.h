@@ -117,7 +117,8 @@ typedef struct {
                               Pages of 1, 2 or 4 tokens with 16-bit KV take
                               kernel 2 (D <= 128), gathering key rows with
                               16-byte cp.async copies instead of TMA boxes, or
-                              kernel 0 (D = 256), one bulk copy per key row  */
+                              kernel 0 (D = 256), a bulk copy per K row and
+                              16-byte cp.async copies of the V rows          */
   int32_t num_sms;         /* SM count the plan was made for                       */
   int32_t ctas;            /* grid size B * Hkv * P                                */
   int32_t smem_bytes;      /* dynamic shared memory per partition CTA             */

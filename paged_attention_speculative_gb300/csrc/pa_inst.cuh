@@ -27,7 +27,7 @@ cudaError_t launch_mma_tt(const CUtensorMap& k, const CUtensorMap& v, const Part
     if (e != cudaSuccess) return e;
     __atomic_store_n(&configured_for[dev], 1, __ATOMIC_RELEASE);
   }
-  return launch_dependent(kern, grid, dim3(kThreads), smem, st, k, v, a);
+  return launch_dependent(kern, grid, dim3(GATHER ? kThreads + 32 : kThreads), smem, st, k, v, a);
 }
 
 // Tree-mask verify runs its own instantiation, so the causal kernels keep

@@ -49,7 +49,8 @@ cudaError_t launch_mma_d128(int kv, int nt, const CUtensorMap& k, const CUtensor
 cudaError_t launch_mma_d256(int kv, int nt, const CUtensorMap& k, const CUtensorMap& v, const PartArgs& a, dim3 grid,
                             cudaStream_t st);
 // head_dim 256, 16-bit caches, pages of 1, 2 or 4 tokens (one n-tile per
-// warp): each key's K and V rows arrive by a bulk copy of their own.
+// warp, 192 threads): each key's K row arrives by a bulk copy of its own, its
+// V row by 16-byte cp.async from a second producer warp.
 MmaKernelInfo mma_info_d256_gather(int kv, bool* ok);
 cudaError_t launch_mma_d256_gather(int kv, const PartArgs& a, dim3 grid, cudaStream_t st);
 

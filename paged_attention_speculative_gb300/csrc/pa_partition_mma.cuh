@@ -22,12 +22,14 @@
 // memory at the end.
 //
 // Pages of 1, 2 or 4 tokens (16-bit caches, head_dim 256): no TMA box fits a
-// swizzle atom, so the producer copies each key's K and V rows with a 1-D bulk
-// copy of their own (one key per lane, the block id looked up a stage ahead)
-// into rows padded by 16 bytes instead of swizzled; the pad spreads the eight
-// rows an ldmatrix phase reads over all 32 banks.  The magik.net article
-// ("The Hypothesis: page_size=1 Scatter-Gather") is the case: every key is its
-// own block-table lookup, and each lookup still feeds a whole-row copy.
+// swizzle atom, so two producer warps gather whole rows into rows padded by
+// 16 bytes instead of swizzled (the pad spreads the eight rows an ldmatrix
+// phase reads over all 32 banks): warp 4 copies each key's K row with a 1-D
+// bulk copy of its own (one key per lane, the block id looked up a stage
+// ahead), warp 5 its V row with 16-byte cp.async (the warp's 32 lanes on one
+// row).  The magik.net article ("The
+// Hypothesis: page_size=1 Scatter-Gather") describes this layout: every key
+// is its own block-table lookup, and each lookup still feeds whole-row copies.
 //
 // u8 caches: codes are exact in f16 (code = f16(0x6400 | code) - 1024), so
 // q.K = scale_j (q.code_j - zp_j sum(q)) and the value sum is
@@ -85,7 +87,7 @@ __device__ __forceinline__ int out_dim(int mt, int m) {
 }
 
 template <int D, int KV, int NT, bool TREE = false, bool GATHER = false>
-__global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
+__global__ void __launch_bounds__(GATHER ? kThreads + 32 : kThreads, (NT == 2) ? 1 : 2)
     pa_partition_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const PartArgs a) {
   using C = MmaCfg<D, KV, GATHER>;
@@ -109,7 +111,9 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     s_timeout = 0;
     s_bad = 0;
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
+      // gather: the producer's lane 0 (K bytes expected) and its 32 lanes'
+      // cp.async arrivals (V rows)
+      mbar_init(&full[s], GATHER ? 33 : 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
     fence_barrier_init();
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
     if (p == 0 && threadIdx.x == 0) atomicOr(a.status, si.err);
     if (p == 0 && si.rows_ok) {  // leave the sequence's rows of this KV group zero
       const int n = si.T * a.G * D;
-      for (int idx = threadIdx.x; idx < n; idx += kThreads) {
+      for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
         const int r = idx / D, d = idx % D;
         const int t = si.t0 + r / a.G, h = g * a.G + r % a.G;
         store_out(a.out, a.out_dtype, (static_cast<size_t>(t) * a.Hq + h) * D + d, 0.f);
@@ -160,12 +164,18 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
   const int R = si.T * a.G;
 
   // =========================== producer warp ===============================
-  if (warp == kConsumerWarps) {
+  if (warp >= kConsumerWarps) {
     if constexpr (GATHER) {
+      const bool vwarp = warp == kConsumerWarps + 1;  // V rows by cp.async; warp kConsumerWarps: K by bulk copy
       // One key per lane: validate its block id (a bad one is reported,
-      // clamped to page 0 and the partition's result discarded), then copy
-      // the key's K and V rows whole.  The next stage's ids are loaded before
-      // this stage waits for its slot, so the lookups overlap the ring.
+      // clamped to page 0 and the partition's result discarded), then warp 4
+      // copies the key's K row whole with a bulk copy and warp 5 the V rows
+      // by 16-byte cp.async, all 32 lanes on one row at a time.  Measured at
+      // Gemma global T=2, 32k keys, page 1: both rows by bulk copy from one
+      // warp 120.0 us (one 512-byte copy per ~36 SM cycles); V by cp.async
+      // from the same warp 109.1 us; V from a warp of its own 92.0 us.  The
+      // next stage's ids are loaded before this stage waits for its slot.
+      static_assert(C::SK == 32 && C::ROW_BYTES == 512, "gather layout: one key per lane, 32 units per row");
       constexpr int KPL = (C::SK + 31) / 32;  // keys per lane and stage
       const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
       int idn[KPL];
@@ -192,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
           const int nkey = key0 + C::SK + lane + 32 * u;
           idn[u] = (lane + 32 * u < C::SK && nkey < kend) ? __ldg(bt + (nkey >> a.ps_log2)) : 0;
         }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        if (!vwarp && __any_sync(0xffffffffu, bad) && lane == 0) {
           s_bad = 1;  // published to the consumers by this stage's full-barrier arrive
           atomicOr(a.status, PA_STATUS_BLOCK_ID);
         }
@@ -201,21 +211,24 @@ __global__ void __launch_bounds__(kThreads, (NT == 2) ? 1 : 2)
           break;
         }
         uint8_t* st = smem + slot * C::STAGE;
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nk * 2 * C::ROW_BYTES));
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < KPL; ++u) {
-          const int j = lane + 32 * u;
+        const int j = lane;
+        const size_t off = ((static_cast<size_t>(id[0]) * a.Hkv + g) * a.ps + ((key0 + j) & (a.ps - 1))) * C::ROW_BYTES;
+        if (!vwarp) {
+          if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nk * C::ROW_BYTES));
+          __syncwarp();
           if (j < nk) {
-            const int key = key0 + j;
-            const size_t off =
-                ((static_cast<size_t>(id[u]) * a.Hkv + g) * a.ps + (key & (a.ps - 1))) * C::ROW_BYTES;
             bulk_load(st + j * C::PITCH, a.k_bytes + off, C::ROW_BYTES, &full[slot]);
-            bulk_load(st + C::TILE + j * C::PITCH, a.v_bytes + off, C::ROW_BYTES, &full[slot]);
-            if (a.trace != nullptr && (key & (a.ps - 1)) == 0)
-              atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + (key >> a.ps_log2),
-                        id[u] + 1);
+            if (a.trace != nullptr && ((key0 + j) & (a.ps - 1)) == 0)
+              atomicAdd(a.trace + (static_cast<size_t>(b) * a.Hkv + g) * a.max_blocks + ((key0 + j) >> a.ps_log2),
+                        id[0] + 1);
           }
+        } else {
+          // V: row k's unit `lane`, row offsets passed along the warp
+          for (int k = 0; k < nk; ++k) {
+            const size_t roff = __shfl_sync(0xffffffffu, off, k);
+            cp_async16(st + C::TILE + k * C::PITCH + 16 * lane, a.v_bytes + roff + 16 * lane, 16);
+          }
+          cp_async_mbar_arrive_noinc(&full[slot]);
         }
         issued = s + 1;
       }
