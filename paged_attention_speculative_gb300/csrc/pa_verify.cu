@@ -285,11 +285,11 @@ Workspace carve(void* ws, const pa_dims* d, const pa_plan& plan, bool mixed = fa
 // split into, from what the host knows (dims, max_context_len, the window and
 // the SM count; the chunks' lengths are device data, so `tiles` is an upper
 // bound: every token in full blocks plus one partial block per possible
-// chunk).  Blocks of 256 rows (two 128-row tiles sharing each K/V stage,
-// about 18 % more work per SM) when they still give two waves of CTAs;
-// otherwise 128 rows, so that chunks spread over more SMs (measured: a
-// 512-token chunk at 32k keys takes 475 us in 128-row blocks, 805 us in
-// 256-row blocks).  When the blocks fill at most half the SMs and every
+// chunk).  Blocks are 128 rows (one tile; measured faster than 256-row
+// blocks of two ping-ponging tiles at every chunk size since the one-tile
+// blocks split their producers and issuers: 2.5k-4k-token chunks 10-24 %,
+// same box).  PA_PREFILL_ROWS=256 keeps the two-tile blocks reachable for
+// tuning.  When the blocks fill at most half the SMs and every
 // piece keeps >= 4096 keys, each block's keys are split into pieces, as many
 // as still fit in one wave (measured, chunk alone: 64 tokens at 32k keys
 // 361 -> 76 us, 128 tokens at 64k keys 696 -> 247 us).  Blocks that fill a
@@ -308,9 +308,7 @@ struct PrefillGeometry {
 PrefillGeometry prefill_geometry(const pa_dims* d, int32_t max_ctx, int32_t window, int sms) {
   PrefillGeometry pg;
   const int G = d->num_q_heads / d->num_kv_heads;
-  const long long rows = static_cast<long long>(d->total_tokens) * G;
-  pg.rows_per_block = ceil_div(rows, 256) * d->num_kv_heads >= 2LL * sms ? 256 : 128;
-  if (env_prefill_rows() > 0) pg.rows_per_block = env_prefill_rows();
+  pg.rows_per_block = env_prefill_rows() > 0 ? env_prefill_rows() : 128;
   const long long TQ = pg.rows_per_block / G;
   pg.tiles = ceil_div(d->total_tokens, TQ) +
              std::min<long long>(d->num_seqs, d->total_tokens / (PA_MAX_QUERY_LEN + 1));

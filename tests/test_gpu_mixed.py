@@ -2,8 +2,9 @@
 steps (T_b <= 8) on the split-KV kernels and prefill chunks (T_b > 8) on the
 prefill tile kernel, in one call, against the oracle (whose causal rule holds
 for any number of new tokens).  Cases cover the query-head group sizes the
-tiles handle (G = 1, 2, 4, 6, 8: blocks of 128 / G or 256 / G tokens, ragged
-last blocks, one-tile and two-tile blocks), windows, f16 / bf16 / fp32
+tiles handle (G = 1, 2, 4, 6, 8: blocks of 128 / G tokens, or 256 / G in the
+two-tile blocks a tuning override selects, ragged last blocks), windows,
+f16 / bf16 / fp32
 caches, large pages, keys split into pieces (few blocks at long context),
 and device errors in a prefill chunk; a mixed call with no prefill chunk is
 pa_verify_forward bit for bit."""
@@ -49,8 +50,8 @@ CASES = [
     (mk("mixed_f32", 77, [3, 20], [40, 10], 4, 2, d=64, q_dtype="f32", kv_dtype="f32"), True),
     (mk("prefill_ps128", 78, [70, 2], [1000, 130], 32, 8, ps=128), False),
     (mk("prefill_ps8_win1", 79, [40], [100], 8, 2, ps=8, sliding_window=1), True),
-    # enough rows for two waves of 256-row blocks: the two-tile ping-pong path
-    (mk("prefill_256_rows", 85, [1200, 2], [100, 300], 64, 32, d=64), True),
+    # many blocks (several waves of 128-row blocks), head_dim 64
+    (mk("prefill_many_blocks", 85, [1200, 2], [100, 300], 64, 32, d=64), True),
     # few blocks at long context: the blocks' keys split into pieces merged by
     # the prefill combine (2 pieces; 2 inside a window; 6 for the long
     # chunk beside a short one at past 0, which stays whole; 4 at head_dim 64)
@@ -103,6 +104,39 @@ def test_mixed_matches_the_oracle(idx):
         assert worst <= 0.0, f"{case.name}: exceeds the derived bound by {worst:.3e} (max abs {err:.3e})"
     else:
         assert err <= TOL, f"{case.name}: max abs err {err:.3e}"
+
+
+_TWO_TILE_CHILD = r"""
+import sys, numpy as np
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + "/tests")
+from paged_attention_speculative_gb300 import workloads as W
+import test_gpu_mixed as M
+from pa_testing import derived_tolerance, run_oracle
+for name, seed, ql, pl, hq, hkv, d in (("two_tile_g4", 87, [300, 3], [2000, 700], 32, 8, 128),
+                                        ("two_tile_g2_d64", 88, [260], [5000], 16, 8, 64)):
+    case = W.make_case(name, seed=seed, query_lens=ql, past_lens=pl, num_q_heads=hq, num_kv_heads=hkv,
+                       head_dim=d, page_size=16)
+    got, bits, _ = M.run_mixed(case)
+    assert bits == 0, bits
+    want = run_oracle(case)
+    assert float(np.max(np.abs(got - want) - derived_tolerance(case, want))) <= 0.0, name
+print("two-tile ok")
+"""
+
+
+def test_two_tile_blocks_by_override():
+    """Blocks of 256 rows (two tiles ping-ponging on shared K/V stages) are
+    not the default (128-row blocks measured faster); PA_PREFILL_ROWS=256
+    selects them, read once per process, so a child process checks them
+    against the oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PA_PREFILL_ROWS="256")
+    r = subprocess.run([sys.executable, "-c", _TWO_TILE_CHILD, root], env=env, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0 and "two-tile ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
 
 
 @pytest.mark.slow
